@@ -1,0 +1,150 @@
+/*
+ * bsattn.h -- C ABI of the block-sparse flash-attention forward pass for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per batch b, head h, query row i, with S keys):
+ *
+ *   allowed(j) = M[b][h][i/128][j/128] != 0  and  (not causal or j <= i)
+ *   s_j        = scale * <Q[b][h][i], K[b][h][j]>  if allowed(j), else -inf
+ *   O[b][h][i] = sum_j softmax(s)_j * V[b][h][j]
+ *   LSE[b][h][i] = ln sum_j exp(s_j)            (natural log)
+ *   rows with no allowed key: O = 0, LSE = -inf
+ *
+ * Defined by "Writing Pallas Kernels for JAX: Stepping Outside the XLA Safety
+ * Net": section "Designing the Block Specification" (Q of shape (batch,
+ * seq_len, head_dim) handled in 128-token query blocks; a block mask fed per
+ * (query block, key block) pair) and section "Writing the Kernel Logic: Load,
+ * Compute, Store" (scores q.k * 1/sqrt(head_dim), masked scores set to -inf,
+ * softmax over keys, product with V).  The softmax is exact over all live
+ * keys of a row, computed blockwise the flash-attention way ("Pallas-Triton
+ * kernels and kernel auto-tuning", section "Flash Attention": exact,
+ * cache-friendly attention).  Dead blocks are never read: the grid walks only
+ * the live (query block, key block) pairs, which is the point of the block
+ * mask in "Writing the Kernel Logic" (only the small 128x128 block is ever
+ * materialised).  The causal flag, LSE and the O = 0 / LSE = -inf rule for
+ * fully masked rows are this library's definitions; the pages do not state
+ * them.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* and every tensor argument are DEVICE pointers (CUDA
+ *    global memory on the current device); the caller owns them.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *  - Every function returns a bsattn_status and never aborts the process.
+ *    All argument checks run on the host before any launch; on a non-OK
+ *    return nothing has been launched.
+ *  - Layouts: Q, K, V, O are [B][H][S][D] row-major and contiguous; LSE is
+ *    [B][H][S] fp32; the mask is uint8 [B][H][S/128][S/128], nonzero = live.
+ *  - Supported: D in {64, 128}; S a positive multiple of 128 with S/128 <= 4096;
+ *    B*H*S < 2^31; Q, K, V bf16; O bf16 (default) or fp32 (BSATTN_OUT_F32).
+ */
+#ifndef BSATTN_H_
+#define BSATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BSATTN_OK = 0,
+  BSATTN_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size, plan mismatch */
+  BSATTN_ERR_UNSUPPORTED = 2,  /* valid request outside the supported set (e.g. D=96) */
+  BSATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  BSATTN_ERR_OOM = 4,          /* device or host allocation failed */
+  BSATTN_ERR_TIMEOUT = 5,      /* a kernel gave up waiting (bounded wait ran out) */
+  BSATTN_ERR_INTERNAL = 6      /* a kernel detected an inconsistent state */
+} bsattn_status;
+
+/* Opaque plan: the per-query-tile list of live key blocks and the tile order. */
+typedef struct bsattn_plan_s* bsattn_plan_t;
+
+/* Plan flags. */
+enum {
+  BSATTN_CAUSAL = 1u,   /* also require key j <= query i (element level, inclusive) */
+  BSATTN_OUT_F32 = 2u   /* bsattn_fwd writes O as fp32 instead of bf16 */
+};
+
+/*
+ * bsattn_plan -- build the plan for one block mask.
+ *
+ * The plan is the compressed-sparse-row list of live key blocks of every
+ * query tile (row r = (b*H + h)*(S/128) + qb; col_idx ascending; under
+ * BSATTN_CAUSAL only kb <= qb is kept) and a schedule: the non-empty tiles
+ * ordered head-major, most live blocks first inside each head, and the list
+ * of empty tiles.  Built on the device by kernels on `stream`.  This is the
+ * only call that synchronises: it waits for `stream` once to learn the number
+ * of live blocks before allocating.
+ *
+ *   d_mask     device uint8 [B][H][S/128][S/128]; read during the call only.
+ *   B, H, S    sizes; S % 128 == 0.
+ *   flags      BSATTN_CAUSAL | BSATTN_OUT_F32.
+ *   stream     cudaStream_t.
+ *   out_plan   receives the handle; the library owns its device memory until
+ *              bsattn_plan_free.  Unchanged on error.
+ * Errors: INVALID_ARG (null, sizes), UNSUPPORTED (S/128 > 4096), OOM, CUDA.
+ */
+bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned flags,
+                          void* stream, bsattn_plan_t* out_plan);
+
+/* Device pointers to the plan's CSR (row_ptr: B*H*S/128 + 1 int32, col_idx:
+   nnz int32) and its size; valid until bsattn_plan_free.  For tests/tools. */
+bsattn_status bsattn_plan_csr(bsattn_plan_t plan, const int32_t** d_row_ptr,
+                              const int32_t** d_col_idx, int64_t* nnz);
+
+/* Device pointers to the schedule: non-empty tile ids in processing order
+   (n_live int32) and empty tile ids (n_empty int32).  For tests/tools. */
+bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_order,
+                                   int64_t* n_live, const int32_t** d_empty_tiles,
+                                   int64_t* n_empty);
+
+/*
+ * bsattn_fwd -- O, LSE = block-sparse attention(Q, K, V; plan's mask).
+ *
+ *   q, k, v    device bf16 [B][H][S][D], 16-byte aligned.
+ *   plan       from bsattn_plan with the same B, H, S.
+ *   out        device [B][H][S][D], bf16 (or fp32 with BSATTN_OUT_F32), 16-byte aligned.
+ *   lse        device fp32 [B][H][S], 16-byte aligned.
+ *   D          64 or 128.
+ *   scale      finite; multiplies q.k before masking (1/sqrt(D) in the pages).
+ *   stream     cudaStream_t; the call is stream-ordered and never synchronises.
+ * Uses the plan's small device workspace (tile counter, status word), so calls
+ * with the same plan must not overlap on the GPU.  A kernel-side failure
+ * (bounded wait ran out) is recorded in the plan and returned by
+ * bsattn_plan_status.
+ * Errors: INVALID_ARG (null/misaligned, sizes differ from the plan, non-finite
+ * scale), UNSUPPORTED (D), CUDA (launch failure).
+ */
+bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                         void* out, float* lse, int B, int H, int S, int D, float scale,
+                         void* stream);
+
+/* Wait for `stream`, then report and clear the device-side status of the
+   plan's kernels: OK, TIMEOUT or INTERNAL (or CUDA if the wait failed). */
+bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream);
+
+/* Release the plan (waits for the device first).  NULL is ignored. */
+void bsattn_plan_free(bsattn_plan_t plan);
+
+/* Static text for a status code. */
+const char* bsattn_status_string(bsattn_status status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int bsattn_version(void);
+
+/*
+ * bsattn_selftest_wait_timeout -- checks that the library's bounded device
+ * waits end on their own.  Launches one small kernel whose threads wait on a
+ * barrier that nothing completes, with a limit of `timeout_ns` nanoseconds
+ * (1e3 .. 5e9), and synchronises `stream`.  Returns BSATTN_ERR_TIMEOUT when the
+ * kernel gave up and reported it as designed (the expected result), OK if the
+ * barrier somehow completed, CUDA on a CUDA error.  Not part of the
+ * attention path; no counterpart on the pages.
+ */
+bsattn_status bsattn_selftest_wait_timeout(int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSATTN_H_ */
