@@ -1,0 +1,220 @@
+"""Block-sparse flash-attention forward for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI in ``include/bsattn.h`` (``libbsattn.so``,
+built in-tree by ``_build.build()``).  This module only marshals arguments:
+every step of the attention runs in the library's CUDA kernels.  PyTorch is
+used for device memory and streams.  There is no CPU fallback: if the library
+is missing, every call raises.
+
+    plan = bsattn.plan(mask_u8_cuda, causal=False)   # once per mask
+    o, lse = bsattn.fwd(q, k, v, plan, scale)        # q/k/v bf16 [B,H,S,D] on cuda
+
+The operation: "Writing Pallas Kernels for JAX: Stepping Outside the XLA
+Safety Net" (sections "Designing the Block Specification" and "Writing the
+Kernel Logic: Load, Compute, Store"), computed exactly across key blocks as in
+"Pallas-Triton kernels and kernel auto-tuning" (section "Flash Attention").
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import _build
+
+BLOCK = 128
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_INTERNAL = range(7)
+CAUSAL, OUT_F32 = 1, 2
+
+EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
+           "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
+           "bsattn_selftest_wait_timeout"]
+
+
+class BsattnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load():
+    """Load libbsattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise RuntimeError(f"{_build.LIB} is not built; run block_sparse_flash_attn_gb300._build.build()"
+                           " (or __graft_entry__.build()) first -- there is no fallback path")
+    lib = ctypes.CDLL(_build.LIB)
+    vp, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint
+    lib.bsattn_plan.argtypes = [vp, i32, i32, i32, u32, vp, ctypes.POINTER(vp)]
+    lib.bsattn_plan.restype = i32
+    lib.bsattn_plan_csr.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)]
+    lib.bsattn_plan_csr.restype = i32
+    lib.bsattn_plan_schedule.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(i64),
+                                         ctypes.POINTER(vp), ctypes.POINTER(i64)]
+    lib.bsattn_plan_schedule.restype = i32
+    lib.bsattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
+    lib.bsattn_fwd.restype = i32
+    lib.bsattn_plan_status.argtypes = [vp, vp]
+    lib.bsattn_plan_status.restype = i32
+    lib.bsattn_plan_free.argtypes = [vp]
+    lib.bsattn_plan_free.restype = None
+    lib.bsattn_status_string.argtypes = [i32]
+    lib.bsattn_status_string.restype = ctypes.c_char_p
+    lib.bsattn_version.argtypes = []
+    lib.bsattn_version.restype = i32
+    lib.bsattn_selftest_wait_timeout.argtypes = [i64, vp]
+    lib.bsattn_selftest_wait_timeout.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().bsattn_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise BsattnError(status, what)
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class _DeviceView:
+    """Zero-copy int32 view of library-owned device memory (for torch.as_tensor)."""
+
+    def __init__(self, ptr: int, n: int):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i4", "data": (ptr, False),
+                                         "version": 3, "strides": None}
+
+
+def _view_i32(ptr, n: int) -> torch.Tensor:
+    if n == 0:
+        return torch.empty(0, dtype=torch.int32, device="cuda")
+    return torch.as_tensor(_DeviceView(int(ptr), int(n)), device="cuda").clone()
+
+
+class Plan:
+    """Handle to a device-side plan (CSR of live key blocks + tile schedule)."""
+
+    def __init__(self, handle: int, B: int, H: int, S: int, causal: bool, out_f32: bool):
+        self._h = ctypes.c_void_p(handle)
+        self.B, self.H, self.S = B, H, S
+        self.causal, self.out_f32 = causal, out_f32
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if not self._h:
+            raise ValueError("plan was freed")
+        return self._h
+
+    def close(self) -> None:
+        if self._h:
+            load().bsattn_plan_free(self._h)
+            self._h = ctypes.c_void_p(None)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+
+def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream=None) -> Plan:
+    """Build the plan for a uint8 block mask [B, H, S/128, S/128] on the GPU."""
+    if not (isinstance(mask, torch.Tensor) and mask.is_cuda and mask.dtype == torch.uint8):
+        raise TypeError("mask must be a CUDA uint8 tensor")
+    if mask.dim() != 4 or mask.shape[2] != mask.shape[3]:
+        raise ValueError("mask must be [B, H, nb, nb]")
+    mask = mask.contiguous()
+    B, H, nb, _ = mask.shape
+    flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0)
+    h = ctypes.c_void_p()
+    with torch.cuda.device(mask.device):
+        _check(load().bsattn_plan(ctypes.c_void_p(mask.data_ptr()), B, H, nb * BLOCK, flags,
+                                  _stream_handle(stream), ctypes.byref(h)), "bsattn_plan")
+    return Plan(h.value, B, H, nb * BLOCK, causal, out_f32)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float | None = None,
+        out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
+    """O, LSE = block-sparse attention.  q/k/v: CUDA bf16 [B, H, S, D], contiguous."""
+    for t in (q, k, v):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16):
+            raise TypeError("q, k, v must be CUDA bf16 tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share the shape [B, H, S, D]")
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    odt = torch.float32 if p.out_f32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if out.dtype != odt or out.shape != (B, H, S, D) or not out.is_contiguous():
+        raise ValueError("out has the wrong dtype/shape/layout for this plan")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, S]")
+    with torch.cuda.device(q.device):
+        _check(load().bsattn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+                                 ctypes.c_void_p(v.data_ptr()), p.handle,
+                                 ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
+                                 B, H, S, D, float(scale), _stream_handle(stream)), "bsattn_fwd")
+    return out, lse
+
+
+def plan_status(p: Plan, stream=None) -> None:
+    """Wait for the stream; raise if a kernel reported a timeout or internal error."""
+    _check(load().bsattn_plan_status(p.handle, _stream_handle(stream)), "device status")
+
+
+def plan_csr(p: Plan):
+    """(row_ptr, col_idx) as fresh CUDA int32 tensors."""
+    rp, ci, nnz = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int64()
+    _check(load().bsattn_plan_csr(p.handle, ctypes.byref(rp), ctypes.byref(ci), ctypes.byref(nnz)),
+           "bsattn_plan_csr")
+    rows = p.B * p.H * (p.S // BLOCK)
+    return _view_i32(rp.value, rows + 1), _view_i32(ci.value, nnz.value)
+
+
+def plan_schedule(p: Plan):
+    """(tile_order, empty_tiles) as fresh CUDA int32 tensors."""
+    to, et = ctypes.c_void_p(), ctypes.c_void_p()
+    nl, ne = ctypes.c_int64(), ctypes.c_int64()
+    _check(load().bsattn_plan_schedule(p.handle, ctypes.byref(to), ctypes.byref(nl),
+                                       ctypes.byref(et), ctypes.byref(ne)), "bsattn_plan_schedule")
+    return _view_i32(to.value, nl.value), _view_i32(et.value, ne.value)
+
+
+def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> int:
+    """Run the bounded-wait self test; returns the status (ERR_TIMEOUT is the expected one)."""
+    return int(load().bsattn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)))
+
+
+def attention(q, k, v, mask, causal: bool = False, scale: float | None = None,
+              out_f32: bool = False):
+    """Convenience: plan + fwd for a one-off call."""
+    p = plan(mask, causal=causal, out_f32=out_f32)
+    try:
+        return fwd(q, k, v, p, scale)
+    finally:
+        torch.cuda.current_stream().synchronize()
+        p.close()

@@ -1,0 +1,295 @@
+// C ABI (include/bsattn.h): argument checks, plan ownership, TMA tensor-map
+// encoding and kernel launches.  All checks run before anything is launched;
+// no function aborts the process.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include <cudaTypedefs.h>
+
+#include "internal.h"
+
+using namespace bsattn;
+
+struct bsattn_plan_s {
+  uint32_t magic = 0;
+  int B = 0, H = 0, S = 0, nb = 0;
+  unsigned flags = 0;
+  int device = 0;
+  int64_t nnz = 0, n_live = 0, n_empty = 0;
+  PlanDevice dev;
+};
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+int sm_count(int dev) {
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bsattn_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return BSATTN_OK;
+  return e == cudaErrorMemoryAllocation ? BSATTN_ERR_OOM : BSATTN_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D view (rows = B*H*S, cols = D) of a bf16 tensor; box 64 columns x 128
+// rows (one 128-byte swizzle span), 128B swizzle.
+bsattn_status encode_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+bool plan_ok(const bsattn_plan_s* p) { return p != nullptr && p->magic == kPlanMagic; }
+
+void free_plan_memory(bsattn_plan_s* p) {
+  cudaFree(p->dev.row_ptr);
+  cudaFree(p->dev.col_idx);
+  cudaFree(p->dev.tile_order);
+  cudaFree(p->dev.empty_tiles);
+  cudaFree(p->dev.work);
+  p->dev = PlanDevice{};
+}
+
+}  // namespace
+
+extern "C" {
+
+int bsattn_version(void) { return 100; }
+
+const char* bsattn_status_string(bsattn_status s) {
+  switch (s) {
+    case BSATTN_OK: return "ok";
+    case BSATTN_ERR_INVALID_ARG: return "invalid argument";
+    case BSATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case BSATTN_ERR_CUDA: return "CUDA error";
+    case BSATTN_ERR_OOM: return "out of memory";
+    case BSATTN_ERR_TIMEOUT: return "device wait timed out";
+    case BSATTN_ERR_INTERNAL: return "internal error detected on device";
+  }
+  return "unknown status";
+}
+
+bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned flags,
+                          void* stream, bsattn_plan_t* out_plan) {
+  if (!d_mask || !out_plan) return BSATTN_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || S <= 0 || (S % kBlock) != 0) return BSATTN_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(BSATTN_CAUSAL | BSATTN_OUT_F32)) return BSATTN_ERR_INVALID_ARG;
+  const int nb = S / kBlock;
+  if (nb > kMaxBlocksPerRow) return BSATTN_ERR_UNSUPPORTED;
+  if ((long long)B * H * S >= (1ll << 31)) return BSATTN_ERR_UNSUPPORTED;
+  const int BH = B * H;
+  const int rows = BH * nb;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  bsattn_plan_s* p = new (std::nothrow) bsattn_plan_s();
+  if (!p) return BSATTN_ERR_OOM;
+  p->B = B;
+  p->H = H;
+  p->S = S;
+  p->nb = nb;
+  p->flags = flags;
+  cudaGetDevice(&p->device);
+  const int causal = (flags & BSATTN_CAUSAL) ? 1 : 0;
+
+  int* tmp = nullptr;  // counts[rows] | live_per_head[BH] | live_off[BH+1] | totals (2 x int64)
+  const size_t tmp_ints = (size_t)rows + BH + (BH + 1) + 1 + 4;
+  long long h_tot[2] = {0, 0};
+  auto fail = [&](bsattn_status s) {
+    cudaFree(tmp);
+    free_plan_memory(p);
+    delete p;
+    return s;
+  };
+  cudaError_t e;
+  if ((e = cudaMalloc(&p->dev.row_ptr, sizeof(int) * ((size_t)rows + 1))) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&p->dev.work, sizeof(int) * kWorkWords)) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&tmp, sizeof(int) * tmp_ints)) != cudaSuccess) return fail(from_cuda(e));
+  int* d_counts = tmp;
+  int* d_live_off = tmp + rows + BH;
+  // 8-byte aligned slot for the two int64 totals
+  size_t tot_off = (size_t)rows + BH + BH + 1;
+  tot_off = (tot_off + 1) & ~(size_t)1;
+  int* d_totals = tmp + tot_off;
+  if ((e = cudaMemsetAsync(p->dev.work, 0, sizeof(int) * kWorkWords, st)) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = plan_count_and_scan(d_mask, BH, nb, causal, d_counts, p->dev.row_ptr, d_live_off,
+                               d_totals, st)) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMemcpyAsync(h_tot, d_totals, sizeof(h_tot), cudaMemcpyDeviceToHost, st)) !=
+      cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
+  p->nnz = h_tot[0];
+  p->n_live = h_tot[1];
+  p->n_empty = (int64_t)rows - p->n_live;
+  if (p->nnz < 0 || p->nnz >= (1ll << 31) || p->n_live < 0 || p->n_live > rows)
+    return fail(BSATTN_ERR_UNSUPPORTED);
+  if ((e = cudaMalloc(&p->dev.col_idx, sizeof(int) * (size_t)(p->nnz > 0 ? p->nnz : 1))) !=
+      cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&p->dev.tile_order,
+                      sizeof(int) * (size_t)(p->n_live > 0 ? p->n_live : 1))) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&p->dev.empty_tiles,
+                      sizeof(int) * (size_t)(p->n_empty > 0 ? p->n_empty : 1))) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = plan_fill_and_order(d_mask, BH, nb, causal, p->dev.row_ptr, d_live_off,
+                               p->dev.col_idx, p->dev.tile_order, p->dev.empty_tiles, st)) !=
+      cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
+  cudaFree(tmp);
+  tmp = nullptr;
+  p->magic = kPlanMagic;
+  *out_plan = p;
+  return BSATTN_OK;
+}
+
+bsattn_status bsattn_plan_csr(bsattn_plan_t plan, const int32_t** d_row_ptr,
+                              const int32_t** d_col_idx, int64_t* nnz) {
+  if (!plan_ok(plan) || !d_row_ptr || !d_col_idx || !nnz) return BSATTN_ERR_INVALID_ARG;
+  *d_row_ptr = plan->dev.row_ptr;
+  *d_col_idx = plan->dev.col_idx;
+  *nnz = plan->nnz;
+  return BSATTN_OK;
+}
+
+bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_order,
+                                   int64_t* n_live, const int32_t** d_empty_tiles,
+                                   int64_t* n_empty) {
+  if (!plan_ok(plan) || !d_tile_order || !n_live || !d_empty_tiles || !n_empty)
+    return BSATTN_ERR_INVALID_ARG;
+  *d_tile_order = plan->dev.tile_order;
+  *n_live = plan->n_live;
+  *d_empty_tiles = plan->dev.empty_tiles;
+  *n_empty = plan->n_empty;
+  return BSATTN_OK;
+}
+
+bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                         void* out, float* lse, int B, int H, int S, int D, float scale,
+                         void* stream) {
+  if (!plan_ok(plan)) return BSATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return BSATTN_ERR_INVALID_ARG;
+  if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
+  if (!get_encoder()) return BSATTN_ERR_CUDA;
+
+  const long long rows = (long long)B * H * S;
+  CUtensorMap tq, tk, tv;
+  bsattn_status rc;
+  if ((rc = encode_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
+
+  FwdParams prm{};
+  prm.row_ptr = plan->dev.row_ptr;
+  prm.col_idx = plan->dev.col_idx;
+  prm.tile_order = plan->dev.tile_order;
+  prm.empty_tiles = plan->dev.empty_tiles;
+  prm.out = out;
+  prm.lse = lse;
+  prm.counter = plan->dev.work + kWorkCounter;
+  prm.done = plan->dev.work + kWorkDone;
+  prm.status = plan->dev.work + kWorkStatus;
+  prm.n_live = (int)plan->n_live;
+  prm.n_empty = (int)plan->n_empty;
+  prm.nb = plan->nb;
+  prm.S = S;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
+  prm.timeout_ns = kDefaultTimeoutNs;
+
+  const int grid = sm_count(dev);
+  const bool out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
+  return from_cuda(launch_fwd(D, out_f32, tq, tk, tv, prm, grid,
+                              static_cast<cudaStream_t>(stream)));
+}
+
+bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {
+  if (!plan_ok(plan)) return BSATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return BSATTN_ERR_CUDA;
+  int words[kWorkWords] = {0};
+  if (cudaMemcpy(words, plan->dev.work, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return BSATTN_ERR_CUDA;
+  // Clear the status and rewind the scheduler so the plan is usable again.
+  if (cudaMemset(plan->dev.work, 0, sizeof(words)) != cudaSuccess) return BSATTN_ERR_CUDA;
+  const int s = words[kWorkStatus];
+  if (s & kStatusInternal) return BSATTN_ERR_INTERNAL;
+  if (s & kStatusTimeout) return BSATTN_ERR_TIMEOUT;
+  return BSATTN_OK;
+}
+
+void bsattn_plan_free(bsattn_plan_t plan) {
+  if (!plan_ok(plan)) return;
+  cudaDeviceSynchronize();
+  free_plan_memory(plan);
+  plan->magic = 0;
+  delete plan;
+}
+
+bsattn_status bsattn_selftest_wait_timeout(int64_t timeout_ns, void* stream) {
+  if (timeout_ns < 1000 || timeout_ns > 5000000000ll) return BSATTN_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* d_status = nullptr;
+  cudaError_t e = cudaMalloc(&d_status, sizeof(int));
+  if (e != cudaSuccess) return from_cuda(e);
+  int h = 0;
+  bsattn_status rc = BSATTN_OK;
+  if ((e = cudaMemsetAsync(d_status, 0, sizeof(int), st)) != cudaSuccess ||
+      (e = launch_selftest_wait((unsigned long long)timeout_ns, d_status, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(&h, d_status, sizeof(int), cudaMemcpyDeviceToHost, st)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess) {
+    rc = BSATTN_ERR_CUDA;
+  } else {
+    rc = (h & kStatusTimeout) ? BSATTN_ERR_TIMEOUT : BSATTN_OK;
+  }
+  cudaFree(d_status);
+  return rc;
+}
+
+}  // extern "C"

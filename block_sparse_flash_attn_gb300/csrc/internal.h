@@ -1,0 +1,66 @@
+// Internal declarations shared by the host API (api.cu), the plan kernels
+// (plan.cu) and the forward kernel (fwd_sm103.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "bsattn.h"
+
+namespace bsattn {
+
+constexpr int kBlock = 128;           // query tile rows = key block rows = mask granularity
+constexpr int kMaxBlocksPerRow = 4096;
+constexpr uint32_t kPlanMagic = 0x42535041u;  // "BSPA"
+
+// Status bits written by kernels into the caller's status word.
+enum : int { kStatusTimeout = 1, kStatusInternal = 2 };
+
+// Device workspace words owned by a plan.
+enum : int { kWorkCounter = 0, kWorkStatus = 1, kWorkDone = 2, kWorkWords = 4 };
+
+struct PlanDevice {
+  int* row_ptr = nullptr;      // [R + 1]
+  int* col_idx = nullptr;      // [nnz]
+  int* tile_order = nullptr;   // [n_live] non-empty tiles, head-major, longest first
+  int* empty_tiles = nullptr;  // [n_empty]
+  int* work = nullptr;         // [kWorkWords] tile counter, status word
+};
+
+// Everything the forward kernel needs besides the three tensor maps.
+struct FwdParams {
+  const int* row_ptr;
+  const int* col_idx;
+  const int* tile_order;
+  const int* empty_tiles;
+  void* out;
+  float* lse;
+  int* counter;  // tile counter, zero at launch; rewound by the last CTA
+  int* done;     // CTAs finished
+  int* status;
+  int n_live;
+  int n_empty;
+  int nb;            // S / 128
+  int S;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  unsigned long long timeout_ns;
+};
+
+// plan.cu
+cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
+                                int* d_row_ptr, int* d_live_off, int* d_totals,
+                                cudaStream_t stream);
+cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
+                                const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
+                                int* d_tile_order, int* d_empty_tiles, cudaStream_t stream);
+
+// fwd_sm103.cu
+cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream);
+size_t fwd_smem_bytes(int D);
+cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
+                                 cudaStream_t stream);
+
+}  // namespace bsattn

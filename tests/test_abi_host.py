@@ -1,0 +1,97 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads,
+exports every symbol include/bsattn.h declares, and rejects bad arguments
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "bsattn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_flash_attn_gb300 import _build
+    _build.build()
+    import block_sparse_flash_attn_gb300 as bs
+    return bs.load()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bsattn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["bsattn_plan", "bsattn_plan_csr", "bsattn_fwd", "bsattn_plan_free",
+              "bsattn_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    import block_sparse_flash_attn_gb300 as bs
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert set(_declared()) == set(bs.EXPORTS)
+
+
+def test_status_strings_and_version(lib):
+    import block_sparse_flash_attn_gb300 as bs
+    assert lib.bsattn_version() == 100
+    for s in range(7):
+        assert bs.status_string(s)
+    assert bs.status_string(99) == "unknown status"
+
+
+def test_plan_rejects_bad_arguments_without_a_device(lib):
+    import block_sparse_flash_attn_gb300 as bs
+    vp = ctypes.c_void_p
+    out = vp()
+    fake = vp(0x10000)
+    assert lib.bsattn_plan(vp(0), 1, 1, 128, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 1, 128, 0, vp(0), None) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 1, 100, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 0, 1, 128, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, -2, 128, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 1, 128, 8, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 1, 128 * 4097, 0, vp(0), ctypes.byref(out)) == bs.ERR_UNSUPPORTED
+    assert lib.bsattn_plan(fake, 1024, 1024, 4096, 0, vp(0), ctypes.byref(out)) == bs.ERR_UNSUPPORTED
+    assert out.value is None
+
+
+def test_fwd_and_status_reject_missing_plan(lib):
+    import block_sparse_flash_attn_gb300 as bs
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    assert lib.bsattn_fwd(fake, fake, fake, vp(0), fake, fake, 1, 1, 128, 128,
+                          ctypes.c_float(0.1), vp(0)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan_status(vp(0), vp(0)) == bs.ERR_INVALID_ARG
+    rp, ci, n = vp(), vp(), ctypes.c_int64()
+    assert lib.bsattn_plan_csr(vp(0), ctypes.byref(rp), ctypes.byref(ci), ctypes.byref(n)) == \
+        bs.ERR_INVALID_ARG
+    lib.bsattn_plan_free(vp(0))  # ignored
+    assert lib.bsattn_selftest_wait_timeout(10, vp(0)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_selftest_wait_timeout(10 ** 10, vp(0)) == bs.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch):
+    import block_sparse_flash_attn_gb300 as bs
+    from block_sparse_flash_attn_gb300 import _build
+    monkeypatch.setattr(_build, "LIB", os.path.join(ROOT, "does-not-exist", "libbsattn.so"))
+    monkeypatch.setattr(bs, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        bs.load()
+
+
+def test_kernel_source_is_tcgen05_tma():
+    """The forward kernel is written with tcgen05 + TMA inline PTX for sm_103a."""
+    src = open(os.path.join(ROOT, "block_sparse_flash_attn_gb300", "csrc", "ptx.cuh")).read()
+    for needle in ["tcgen05.mma.cta_group::1.kind::f16", "tcgen05.alloc", "tcgen05.ld",
+                   "tcgen05.st", "cp.async.bulk.tensor.2d", "mbarrier.try_wait"]:
+        assert needle in src
+    from block_sparse_flash_attn_gb300 import _build
+    assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)

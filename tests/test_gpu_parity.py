@@ -1,0 +1,235 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Element-by-element comparison on seeded inputs at sizes the oracle finishes
+in seconds (several tiles, rows of different lengths, empty tiles), and at
+the five workloads' full sizes on sampled rows (whole tiles plus random rows)
+in the launch configuration the bench times.  The plan's CSR must match the
+oracle's bit for bit; the schedule must be a valid ordering.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from _util import compare, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bs():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import block_sparse_flash_attn_gb300 as bs
+    bs.load()
+    return bs
+
+
+def _run(bs, qb, kb, vb, mask, scale, causal, out_f32):
+    import torch
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    p = bs.plan(torch.from_numpy(np.ascontiguousarray(mask)).cuda(), causal=causal, out_f32=out_f32)
+    o, lse = bs.fwd(q, k, v, p, scale)
+    bs.plan_status(p)
+    return o.float().cpu().numpy(), lse.cpu().numpy(), p
+
+
+# ----------------------------------------------------------------------------
+# device-side timeout path
+# ----------------------------------------------------------------------------
+
+def test_bounded_wait_times_out(bs):
+    """A wait on a barrier nothing completes ends by its limit and reports it."""
+    assert bs.selftest_wait_timeout(2_000_000) == bs.ERR_TIMEOUT
+    assert bs.selftest_wait_timeout(200_000) == bs.ERR_TIMEOUT
+
+
+# ----------------------------------------------------------------------------
+# plan: CSR bit-exact, schedule valid
+# ----------------------------------------------------------------------------
+
+def _check_plan(bs, mask, causal):
+    import torch
+    p = bs.plan(torch.from_numpy(np.ascontiguousarray(mask)).cuda(), causal=causal)
+    rp, ci = bs.plan_csr(p)
+    rp_ref, ci_ref = oracle.csr(mask, causal)
+    assert np.array_equal(rp.cpu().numpy(), rp_ref)
+    assert np.array_equal(ci.cpu().numpy(), ci_ref)
+    order, empty = (x.cpu().numpy() for x in bs.plan_schedule(p))
+    counts = np.diff(rp_ref)
+    B, H, nb, _ = mask.shape
+    live = np.flatnonzero(counts > 0)
+    assert np.array_equal(np.sort(order), live)
+    assert np.array_equal(np.sort(empty), np.flatnonzero(counts == 0))
+    heads = order // nb
+    assert np.all(np.diff(heads) >= 0), "schedule must be head-major"
+    for h in np.unique(heads):
+        c = counts[order[heads == h]]
+        assert np.all(np.diff(c) <= 0), "longest tiles first inside a head"
+    p.close()
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_plan_csr_bit_exact(bs, wid):
+    w = workloads.WORKLOADS[wid]
+    _check_plan(bs, workloads.make_mask(w), w.causal)
+
+
+def test_plan_edge_masks(bs):
+    rng = np.random.default_rng(0)
+    m = (rng.random((2, 3, 9, 9)) < 0.3).astype(np.uint8)
+    m[0, 1] = 0                       # a fully dead head
+    m[1, 2, 4] = 0                    # one empty row
+    for causal in (False, True):
+        _check_plan(bs, m, causal)
+    _check_plan(bs, np.zeros((1, 1, 1, 1), np.uint8), False)
+    _check_plan(bs, np.ones((1, 1, 1, 1), np.uint8), True)
+
+
+# ----------------------------------------------------------------------------
+# small cases, every row compared
+# ----------------------------------------------------------------------------
+
+def _mask_iid(seed, B, H, nb, p, diag=False):
+    rng = np.random.default_rng(seed)
+    m = (rng.random((B, H, nb, nb)) < p).astype(np.uint8)
+    if diag:
+        m[:, :, np.arange(nb), np.arange(nb)] = 1
+    return m
+
+
+CASES = {
+    # name: (B, H, S, D, mask builder, causal, scale, mult)
+    "w1": (1, 2, 512, 64, lambda: workloads.make_mask(workloads.WORKLOADS[1]), False, 0.125, 1.0),
+    "s1024_d128_causal": (1, 2, 1024, 128, lambda: _mask_iid(1, 1, 2, 8, 0.4, diag=True), True, 128 ** -0.5, 1.0),
+    "s1024_d64_sparse": (1, 2, 1024, 64, lambda: _mask_iid(2, 1, 2, 8, 0.3), False, 0.125, 1.0),
+    "one_tile_d128": (1, 1, 128, 128, lambda: np.ones((1, 1, 1, 1), np.uint8), False, 128 ** -0.5, 1.0),
+    "one_tile_d64_causal": (2, 1, 128, 64, lambda: np.ones((2, 1, 1, 1), np.uint8), True, 0.125, 1.0),
+    "all_dead": (1, 2, 256, 128, lambda: np.zeros((1, 2, 2, 2), np.uint8), False, 0.1, 1.0),
+    "empty_rows": (1, 2, 512, 128, lambda: np.array([[[[1, 0, 0, 1], [0, 0, 0, 0], [0, 1, 1, 0], [0, 0, 0, 0]],
+                                                      [[0, 0, 0, 0], [1, 1, 1, 1], [0, 0, 0, 0], [0, 0, 0, 1]]]], np.uint8),
+                   False, 0.09, 1.0),
+    "one_block_per_row": (1, 2, 1024, 64, lambda: np.eye(8, dtype=np.uint8)[np.random.default_rng(3).permutation(8)][None, None].repeat(2, 1), False, 0.125, 1.0),
+    "causal_dead_diag": (1, 1, 512, 128, lambda: np.tril(np.ones((4, 4), np.uint8), -1)[None, None], True, 0.09, 1.0),
+    "scale_zero": (1, 1, 512, 128, lambda: _mask_iid(4, 1, 1, 4, 0.6, diag=True), True, 0.0, 1.0),
+    "scale_tiny": (1, 1, 512, 64, lambda: _mask_iid(5, 1, 1, 4, 0.6, diag=True), False, 1e-6, 1.0),
+    "scale_large": (1, 1, 512, 64, lambda: _mask_iid(6, 1, 1, 4, 0.6, diag=True), False, 2.0, 1.0),
+    "scale_negative": (1, 1, 512, 128, lambda: _mask_iid(7, 1, 1, 4, 0.6, diag=True), True, -0.2, 1.0),
+    "wide_logits_d64": (1, 2, 1024, 64, lambda: np.ones((1, 2, 8, 8), np.uint8), False, 0.125, 2.0),
+    "many_tiles": (4, 16, 1024, 128, lambda: _mask_iid(8, 4, 16, 8, 0.35, diag=True), False, 128 ** -0.5, 1.0),
+    "many_tiles_causal_d64": (2, 16, 2048, 64, lambda: _mask_iid(9, 2, 16, 16, 0.5, diag=True), True, 0.125, 1.0),
+}
+
+
+@pytest.mark.parametrize("out_f32", [True, False], ids=["o_f32", "o_bf16"])
+@pytest.mark.parametrize("name", list(CASES))
+def test_small_every_row(bs, name, out_f32):
+    B, H, S, D, mk, causal, scale, mult = CASES[name]
+    qb, kb, vb = workloads.custom(100 + len(name), B, H, S, D, mult)
+    mask = mk()
+    o, lse, p = _run(bs, qb, kb, vb, mask, scale, causal, out_f32)
+    p.close()
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(scale), causal)
+    ok, rep = compare(o, lse, O_ref, L_ref, out_bf16=not out_f32)
+    assert ok, rep
+
+
+def test_repeated_calls_same_plan(bs):
+    """The plan's workspace (tile counter) rewinds itself between launches."""
+    import torch
+    B, H, S, D = 2, 8, 1024, 128
+    qb, kb, vb = workloads.custom(77, B, H, S, D)
+    mask = _mask_iid(10, B, H, 8, 0.5, diag=True)
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    p = bs.plan(torch.from_numpy(mask).cuda(), out_f32=True)
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(D ** -0.5), False)
+    for _ in range(5):
+        o, lse = bs.fwd(q, k, v, p, D ** -0.5)
+    bs.plan_status(p)
+    ok, rep = compare(o.cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref)
+    assert ok, rep
+    p.close()
+
+
+# ----------------------------------------------------------------------------
+# full-size workloads, sampled rows
+# ----------------------------------------------------------------------------
+
+def _sample_rows(order, nb, S, n_random, seed):
+    """Whole tiles (first, middle and last of the schedule) plus random rows."""
+    rng = np.random.default_rng(seed)
+    tiles = [order[0], order[len(order) // 2], order[-1]]
+    rows = []
+    for t in tiles:
+        bh, qb = divmod(int(t), nb)
+        rows.extend(bh * S + qb * 128 + np.arange(128))
+    total = (order.max() // nb + 1) * S
+    rows.extend(rng.integers(0, total, n_random))
+    return np.unique(np.asarray(rows, dtype=np.int64))
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4, 5])
+def test_full_size_sampled_rows(bs, wid):
+    import torch
+    w = workloads.WORKLOADS[wid]
+    qb, kb, vb = workloads.make_qkv(w)
+    mask = workloads.make_mask(w)
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    mask_d = torch.from_numpy(mask).cuda()
+    B, H, S, D = qb.shape
+    results = {}
+    for out_f32 in (False, True):
+        p = bs.plan(mask_d, causal=w.causal, out_f32=out_f32)
+        o, lse = bs.fwd(q, k, v, p, w.scale)
+        bs.plan_status(p)
+        order, _ = bs.plan_schedule(p)
+        results[out_f32] = (o, lse)
+        p.close()
+    order = order.cpu().numpy()
+    rows = _sample_rows(order, w.nb, S, 384, wid)
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, w.scale, w.causal, rows=rows)
+    for out_f32, (o, lse) in results.items():
+        o_rows = o.reshape(-1, D)[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+        l_rows = lse.reshape(-1)[torch.from_numpy(rows).cuda()].cpu().numpy()
+        ok, rep = compare(o_rows, l_rows, O_ref, L_ref, out_bf16=not out_f32)
+        assert ok, (out_f32, rep)
+        # properties over every row: finite, and LSE finite exactly where a row has a live key
+        assert bool(torch.isfinite(o).all())
+        assert bool(torch.isfinite(lse).all())  # every workload row has at least one live key
+
+
+# ----------------------------------------------------------------------------
+# argument checks with a real plan (nothing is launched on error)
+# ----------------------------------------------------------------------------
+
+def test_fwd_argument_errors(bs):
+    import torch
+    lib = bs.load()
+    mask = torch.ones((1, 1, 2, 2), dtype=torch.uint8, device="cuda")
+    p = bs.plan(mask)
+    buf = torch.zeros(1 * 1 * 256 * 128 + 8, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(256, dtype=torch.float32, device="cuda")
+    ptr = buf.data_ptr()
+    vp = ctypes.c_void_p
+    st = vp(torch.cuda.current_stream().cuda_stream)
+
+    def call(q=ptr, k=ptr, v=ptr, out=ptr, l=lse.data_ptr(), B=1, H=1, S=256, D=128, scale=0.1):
+        return lib.bsattn_fwd(vp(q), vp(k), vp(v), p.handle, vp(out), vp(l), B, H, S, D,
+                              ctypes.c_float(scale), st)
+
+    assert call(q=ptr + 2) == bs.ERR_INVALID_ARG            # misaligned
+    assert call(out=0) == bs.ERR_INVALID_ARG                # null
+    assert call(S=512) == bs.ERR_INVALID_ARG                # differs from the plan
+    assert call(H=2) == bs.ERR_INVALID_ARG
+    assert call(D=96) == bs.ERR_UNSUPPORTED
+    assert call(scale=float("inf")) == bs.ERR_INVALID_ARG
+    assert call(scale=float("nan")) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_fwd(vp(ptr), vp(ptr), vp(ptr), vp(0), vp(ptr), vp(lse.data_ptr()), 1, 1, 256,
+                          128, ctypes.c_float(0.1), st) == bs.ERR_INVALID_ARG  # no plan
+    bs.plan_status(p)
+    p.close()
