@@ -27,11 +27,12 @@ from . import _build
 BLOCK = 128
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_INTERNAL = range(7)
+ERR_SCRATCH_LIMIT = 7
 CAUSAL, OUT_F32 = 1, 2
 
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
-           "bsattn_selftest_wait_timeout"]
+           "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc"]
 
 
 class BsattnError(RuntimeError):
@@ -76,6 +77,9 @@ def load():
     lib.bsattn_version.restype = i32
     lib.bsattn_selftest_wait_timeout.argtypes = [i64, vp]
     lib.bsattn_selftest_wait_timeout.restype = i32
+    lib.bsattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                       u32, vp]
+    lib.bsattn_fwd_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -207,6 +211,33 @@ def plan_schedule(p: Plan):
 def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> int:
     """Run the bounded-wait self test; returns the status (ERR_TIMEOUT is the expected one)."""
     return int(load().bsattn_selftest_wait_timeout(int(timeout_ns), _stream_handle(stream)))
+
+
+def fwd_noalloc(q, k, v, mask, causal: bool = False, scale: float | None = None,
+                out_f32: bool = False, out=None, lse=None, stream=None):
+    """Forward pass that allocates no device memory inside the library.
+
+    For callers that cannot call cudaMalloc: the plan and the kernel's scratch
+    live in the library's fixed 16 MiB device array (see bsattn_fwd_noalloc in
+    include/bsattn.h for the limit and the sharing rules).  Output tensors are
+    allocated here by torch only when not passed in.
+    """
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    odt = torch.float32 if out_f32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=odt, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0)
+    with torch.cuda.device(q.device):
+        _check(load().bsattn_fwd_noalloc(
+            ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+            ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(mask.data_ptr()),
+            ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()), B, H, S, D,
+            float(scale), flags, _stream_handle(stream)), "bsattn_fwd_noalloc")
+    return out, lse
 
 
 def attention(q, k, v, mask, causal: bool = False, scale: float | None = None,

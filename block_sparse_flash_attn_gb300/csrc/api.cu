@@ -23,14 +23,12 @@ struct bsattn_plan_s {
   PlanDevice dev;
 };
 
-namespace {
-
-constexpr unsigned long long kDefaultTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
+namespace bsattn {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-bool get_encoder() {
+bool get_tensor_map_encoder() {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q{};
@@ -42,7 +40,7 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-int sm_count(int dev) {
+int device_sm_count(int dev) {
   static int cache[64] = {0};
   if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
   int n = 0;
@@ -61,7 +59,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // 2-D view (rows = B*H*S, cols = D) of a bf16 tensor; box 64 columns x 128
 // rows (one 128-byte swizzle span), 128B swizzle.
-bsattn_status encode_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
+bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
@@ -72,6 +70,10 @@ bsattn_status encode_map(CUtensorMap* m, const void* ptr, int D, long long rows)
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? BSATTN_OK : BSATTN_ERR_CUDA;
 }
+
+}  // namespace bsattn
+
+namespace {
 
 bool plan_ok(const bsattn_plan_s* p) { return p != nullptr && p->magic == kPlanMagic; }
 
@@ -99,6 +101,7 @@ const char* bsattn_status_string(bsattn_status s) {
     case BSATTN_ERR_OOM: return "out of memory";
     case BSATTN_ERR_TIMEOUT: return "device wait timed out";
     case BSATTN_ERR_INTERNAL: return "internal error detected on device";
+    case BSATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the no-allocation scratch size";
   }
   return "unknown status";
 }
@@ -214,14 +217,14 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
   if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
-  if (!get_encoder()) return BSATTN_ERR_CUDA;
+  if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
 
   const long long rows = (long long)B * H * S;
   CUtensorMap tq, tk, tv;
   bsattn_status rc;
-  if ((rc = encode_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
 
   FwdParams prm{};
   prm.row_ptr = plan->dev.row_ptr;
@@ -239,9 +242,9 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
   prm.S = S;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
-  prm.timeout_ns = kDefaultTimeoutNs;
+  prm.timeout_ns = kDefaultWaitTimeoutNs;
 
-  const int grid = sm_count(dev);
+  const int grid = device_sm_count(dev);
   const bool out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
   return from_cuda(launch_fwd(D, out_f32, tq, tk, tv, prm, grid,
                               static_cast<cudaStream_t>(stream)));

@@ -48,6 +48,15 @@ struct FwdParams {
   unsigned long long timeout_ns;
 };
 
+constexpr unsigned long long kDefaultWaitTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
+
+// api.cu helpers
+bool get_tensor_map_encoder();
+int device_sm_count(int dev);
+bool aligned16(const void* p);
+bsattn_status from_cuda(cudaError_t e);
+bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows);
+
 // plan.cu
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,

@@ -53,7 +53,8 @@ typedef enum {
   BSATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
   BSATTN_ERR_OOM = 4,          /* device or host allocation failed */
   BSATTN_ERR_TIMEOUT = 5,      /* a kernel gave up waiting (bounded wait ran out) */
-  BSATTN_ERR_INTERNAL = 6      /* a kernel detected an inconsistent state */
+  BSATTN_ERR_INTERNAL = 6,     /* a kernel detected an inconsistent state */
+  BSATTN_ERR_SCRATCH_LIMIT = 7 /* problem too large for bsattn_fwd_noalloc's fixed scratch */
 } bsattn_status;
 
 /* Opaque plan: the per-query-tile list of live key blocks and the tile order. */
@@ -131,6 +132,40 @@ const char* bsattn_status_string(bsattn_status status);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int bsattn_version(void);
+
+/*
+ * bsattn_fwd_noalloc -- the same forward pass for callers that cannot
+ * allocate device memory.  No counterpart on the pages.
+ *
+ * bsattn_plan allocates its arrays with cudaMalloc.  Some callers cannot:
+ * a host framework that owns all GPU memory through its own pool, a plug-in
+ * that may not allocate once running, or a latency-critical loop that cannot
+ * absorb cudaMalloc's device-wide synchronisation.  This call builds the plan
+ * and runs the forward kernel with every piece of scratch (the plan's CSR and
+ * schedule, the tile counter and the status word) inside one fixed device
+ * array that is part of the library: 16 MiB, held by every GPU that loads the
+ * library until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *   q, k, v, out, lse, B, H, S, D, scale: as bsattn_fwd.
+ *   d_mask     device uint8 [B][H][S/128][S/128], as bsattn_plan.
+ *   flags      BSATTN_CAUSAL | BSATTN_OUT_F32.
+ *   stream     cudaStream_t; the call synchronises it twice (to size the
+ *              plan and to read the kernel's status) and returns the kernel's
+ *              TIMEOUT / INTERNAL status directly.
+ * Limit: with R = B*H*(S/128) query tiles and nb = S/128, the plan needs
+ * about R*(nb + 4) + 2*B*H + 16 int32 words; more than 16 MiB / 4 words is
+ * rejected with BSATTN_ERR_SCRATCH_LIMIT before anything is launched.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture begins.
+ * All calls share the array and it keeps the last call's contents; each call
+ * clears what must start at zero.  Calls that overlap on the GPU race on the
+ * array, so issue them one after another.
+ * Errors: as bsattn_plan and bsattn_fwd, plus SCRATCH_LIMIT.
+ */
+bsattn_status bsattn_fwd_noalloc(const void* q, const void* k, const void* v,
+                                 const uint8_t* d_mask, void* out, float* lse, int B, int H,
+                                 int S, int D, float scale, unsigned flags, void* stream);
 
 /*
  * bsattn_selftest_wait_timeout -- checks that the library's bounded device
