@@ -95,6 +95,22 @@ def row_live_blocks(mask: np.ndarray, causal: bool, rows: np.ndarray, S: int) ->
     return m.sum(axis=1)
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank float over the process group (identity when single-process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank: float, world: int, ms_max: float) -> float:
+    """Units all ranks processed / the slowest rank's time (weak scaling)."""
+    return world * flop_per_rank / (ms_max * 1e-3) / 1e12
+
+
 def read_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -287,11 +303,8 @@ def run_ours(args):
     bsattn.plan_status(plan)
     ms = [s.elapsed_time(e) for s, e in ev]
     ms_mean = statistics.mean(ms)
-    t = torch.tensor([ms_mean], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * flop / (ms_max * 1e-3) / 1e12
+    ms_max = max_over_ranks(ms_mean, dev)
+    value = whole_job_tflops(flop, world, ms_max)
 
     # end to end through the public API with pinned host buffers
     hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -317,11 +330,8 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-    e2e_value = world * flop / (float(te.item()) * 1e-3) / 1e12
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
+    e2e_value = whole_job_tflops(flop, world, e2e_ms)
 
     peaks = read_peaks()
     achieved = flop / (ms_mean * 1e-3) / 1e12
@@ -349,7 +359,7 @@ def run_ours(args):
                        "l2": "flushed (512 MB write) before every timed step",
                        "parallelism": f"replicas x{world} (independent problems, no collective)"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": float(te.item())},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "gpu_launches": args.steps,
             "roofline": roofline,
             "cpu_baseline": cpu,
