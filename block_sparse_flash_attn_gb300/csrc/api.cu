@@ -57,6 +57,16 @@ bsattn_status from_cuda(cudaError_t e) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The softmax works with a strictly positive multiplier sl = |scale| log2(e):
+// a negative scale is folded into the S MMA (-Q K^T), and scale = 0 becomes
+// sl = 1e-30, for which every exponent 2^(s*sl - m) of an allowed key is 1.0
+// in fp32 (|s*sl| < 1e-26), i.e. exactly the uniform weights of scale 0.
+void set_scale_params(FwdParams& p, float scale) {
+  const double a = std::fabs((double)scale) * 1.4426950408889634074;
+  p.scale_log2 = (scale == 0.0f) ? 1e-30f : (float)a;
+  p.neg_scale = scale < 0.0f ? 1 : 0;
+}
+
 // 2-D view (rows = B*H*S, cols = D) of a bf16 tensor; box 64 columns x 128
 // rows (one 128-byte swizzle span), 128B swizzle.
 bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
@@ -240,7 +250,7 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
   prm.n_empty = (int)plan->n_empty;
   prm.nb = plan->nb;
   prm.S = S;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  set_scale_params(prm, scale);
   prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
   prm.timeout_ns = kDefaultWaitTimeoutNs;
 

@@ -11,11 +11,13 @@
 // Dead key blocks are never loaded (the mask's purpose in "Writing the Kernel
 // Logic": only the small 128x128 block is ever materialised).
 //
-// GB300 design (one persistent CTA per SM, 320 threads, 10 warps):
+// GB300 design (one persistent CTA per SM, 384 threads = 3 warpgroups):
 //   warps 0-3  softmax + epilogue for query slot 0 (TMEM lanes 0..127)
 //   warps 4-7  softmax + epilogue for query slot 1
 //   warp  8    TMA producer and tile scheduler (one elected lane)
 //   warp  9    tcgen05 MMA issuer (one elected lane), TMEM owner
+//   warps 10-11 idle (they complete warpgroup 2 so it can hand its
+//              registers to the softmax warpgroups with setmaxnreg)
 // Two query tiles are in flight per CTA so the tensor core works on one slot
 // while the other slot's softmax runs.  Tensor memory (512 columns):
 //   S0 = [0,128), S1 = [128,256): fp32 scores, overwritten in place by the
@@ -45,10 +47,18 @@
 namespace bsattn {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kRegsSoftmax = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168 (launch budget)
+constexpr int kRegsOther = 88;
 constexpr float kTau = 8.0f;
+// Every kPolyEvery-th pair of probabilities in a block without causal masking
+// is computed by the FMA-pipe polynomial instead of the MUFU ex2 (0 = never).
+#ifndef BSATTN_POLY_EVERY
+#define BSATTN_POLY_EVERY 0
+#endif
+constexpr int kPolyEvery = BSATTN_POLY_EVERY;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 200ull * 1000 * 1000;
 
@@ -66,7 +76,15 @@ struct Cfg {
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, true);
 };
 
-struct __align__(8) Bars {
+// One scheduled tile as the producer publishes it to the MMA and softmax roles.
+struct TileInfo {
+  int t;     // tile id (b*H + h)*nb + qb, or -1 when no tiles are left
+  int r0;    // first CSR entry of the tile
+  int n;     // live key blocks
+  int diag;  // causal and the last live block is the diagonal one
+};
+
+struct __align__(16) Bars {
   uint64_t full[8];
   uint64_t empty[8];
   uint64_t q_full[2];
@@ -77,7 +95,7 @@ struct __align__(8) Bars {
   uint64_t tq_full[2][2];
   uint64_t tq_empty[2][2];
   uint64_t drain;
-  int tq[2][2];
+  TileInfo tq[2][2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -140,21 +158,29 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         }
         const int idx = atomicAdd(p.counter, 1);
         const int t = idx < p.n_live ? p.tile_order[idx] : -1;
-        reinterpret_cast<volatile int*>(&bars->tq[s][e])[0] = t;
+        int r0 = 0, cnt = 0, bh = 0, qb = 0, diag = 0;
+        if (t >= 0) {
+          r0 = p.row_ptr[t];
+          cnt = p.row_ptr[t + 1] - r0;
+          bh = t / p.nb;
+          qb = t - bh * p.nb;
+          if (cnt <= 0 || cnt > p.nb) {
+            raise_internal(abort_flag, p.status);
+            ok = false;
+            break;
+          }
+          diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
+        }
+        volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[s][e]);
+        slot[0] = t;
+        slot[1] = r0;
+        slot[2] = cnt;
+        slot[3] = diag;
         mbar_arrive(smem_u32(&bars->tq_full[s][e]));
         ++tq_cnt[s];
         if (t < 0) {
           active[s] = false;
           continue;
-        }
-        const int r0 = p.row_ptr[t];
-        const int cnt = p.row_ptr[t + 1] - r0;
-        const int bh = t / p.nb;
-        const int qb = t - bh * p.nb;
-        if (cnt <= 0 || cnt > p.nb) {
-          raise_internal(abort_flag, p.status);
-          ok = false;
-          break;
         }
         rp[s] = r0;
         n[s] = cnt;
@@ -227,7 +253,10 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
   };
 
   // S[s] = Q[s] K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a
-  // 128-byte swizzle row; a new 64-column box every 4 steps).
+  // 128-byte swizzle row; a new 64-column box every 4 steps).  A negative
+  // scale is applied as -Q (instruction-descriptor negate bit) so the
+  // softmax always sees a non-negative multiplier.
+  const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
   auto issue_s = [&](int s, uint32_t kaddr) {
     const uint32_t qaddr = q_base + s * C::kTileBytes;
 #pragma unroll
@@ -235,7 +264,7 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
       const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
       const uint64_t ad = smem_desc_sw128(qaddr + off, 16, 1024);
       const uint64_t bd = smem_desc_sw128(kaddr + off, 16, 1024);
-      mma_ss(tmem + s * 128, ad, bd, C::kIdescS, kk > 0 ? 1u : 0u);
+      mma_ss(tmem + s * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
     }
   };
   // O[s] (+)= P[s] V : M=128, N=D, K=128 keys in steps of 16.  P is read from
@@ -260,14 +289,16 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
           ok = false;
           break;
         }
-        const int t = reinterpret_cast<volatile int*>(&bars->tq[s][e])[0];
+        const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
+        const int t = slot[0];
+        const int cnt = slot[2];
         mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
         ++tq_cnt[s];
         if (t < 0) {
           active[s] = false;
           continue;
         }
-        n[s] = p.row_ptr[t + 1] - p.row_ptr[t];
+        n[s] = cnt;
         if (!wait_bounded(smem_u32(&bars->q_full[s]), (uint32_t)q_cnt[s] & 1u, abort_flag,
                           p.status, lim)) {
           ok = false;
@@ -351,6 +382,45 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// Probabilities of one 128-column row slice: p = 2^(s*sl - m), rounded to
+// bf16 pairs into pr[]; returns the running sums of the unrounded (a32) and of
+// the rounded (ar) values in four independent pairs of accumulators.
+template <bool POLY>
+__device__ __forceinline__ void softmax_exp(const uint32_t* sr, uint32_t* pr, float sl, float nm,
+                                            float (&a32)[8], float (&ar)[8]) {
+#pragma unroll
+  for (int q = 0; q < 64; ++q) {
+    float x0, x1;
+    fma2(x0, x1, __uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1]), sl, sl, nm, nm);
+    float p0, p1;
+    if (POLY && kPolyEvery > 0 && (q % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
+      exp2_poly2(p0, p1, x0, x1);
+    } else {
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    }
+    const uint32_t pk = pack_bf16x2(p0, p1);
+    pr[q] = pk;
+    const int k = (q & 3) * 2;
+    add2(a32[k], a32[k + 1], a32[k], a32[k + 1], p0, p1);
+    add2(ar[k], ar[k + 1], ar[k], ar[k + 1], __uint_as_float(pk << 16),
+         __uint_as_float(pk & 0xFFFF0000u));
+  }
+}
+
+__device__ __forceinline__ float row_max128(const uint32_t* sr) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
+#pragma unroll
+  for (int c = 16; c < 128; c += 16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      a[i] = max3(a[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]));
+  }
+  return fmaxf(max3(a[0], a[1], a[2]), max3(max3(a[3], a[4], a[5]), a[6], a[7]));
+}
+
 template <int D, bool OUT_F32>
 __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
@@ -362,8 +432,8 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
   const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
   const uint32_t tS = tmem + s * 128 + lane_off;
   const uint32_t tO = tmem + 256 + s * 128 + lane_off;
-  const float sl = p.scale_log2;
-  const float kInf = __int_as_float(0x7f800000);
+  const float sl = p.scale_log2;       // > 0 (see FwdParams)
+  const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
 
   write_empty_tiles<D, OUT_F32>(p);
@@ -373,18 +443,20 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
     if (!wait_warp(smem_u32(&bars->tq_full[s][e]), ph, abort_flag, p.status, lim)) return;
-    const int t = reinterpret_cast<volatile int*>(&bars->tq[s][e])[0];
+    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
+    const int t = slot[0];
+    const int n = slot[2];
+    const int diag_last = slot[3];
     mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
     ++tq_cnt;
     if (t < 0) return;
-    const int r0 = p.row_ptr[t];
-    const int n = p.row_ptr[t + 1] - r0;
     const int bh = t / p.nb;
     const int qb = t - bh * p.nb;
 
-    float m = -kInf;   // running max of scale*log2(e)*score (lazy)
-    float l = 0.f;     // sum of the bf16-rounded probabilities fed to PV (O's denominator)
-    float l32 = 0.f;   // sum of the unrounded probabilities (LSE)
+    float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
+    float a32[8], ar[8];                 // unrounded (LSE) and rounded (O) row sums
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a32[i] = ar[i] = 0.f;
     for (int jb = 0; jb < n; ++jb) {
       if (!wait_warp(smem_u32(&bars->s_full[s]), (uint32_t)s_cnt & 1u, abort_flag, p.status,
                      lim))
@@ -398,62 +470,26 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       tmem_ld32(tS + 96, sr + 96);
       tmem_wait_ld();
       reg_fence(sr, 128);
-      const bool diag = p.causal && (p.col_idx[r0 + jb] == qb);
-
-      // block maximum of the scaled scores (masked entries excluded)
-      float mx0, mx1, mx2, mx3;
-      if (sl >= 0.f) {
-        mx0 = mx1 = mx2 = mx3 = -kInf;
+      const bool diag = diag_last && jb == n - 1;
+      if (diag) {  // causal diagonal tile: key c is allowed for query row r iff c <= r
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          mx0 = fmaxf(mx0, (diag && c + 0 > r) ? -kInf : __uint_as_float(sr[c + 0]));
-          mx1 = fmaxf(mx1, (diag && c + 1 > r) ? -kInf : __uint_as_float(sr[c + 1]));
-          mx2 = fmaxf(mx2, (diag && c + 2 > r) ? -kInf : __uint_as_float(sr[c + 2]));
-          mx3 = fmaxf(mx3, (diag && c + 3 > r) ? -kInf : __uint_as_float(sr[c + 3]));
-        }
-        mx0 = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-      } else {
-        mx0 = mx1 = mx2 = mx3 = kInf;
-#pragma unroll
-        for (int c = 0; c < 128; c += 4) {
-          mx0 = fminf(mx0, (diag && c + 0 > r) ? kInf : __uint_as_float(sr[c + 0]));
-          mx1 = fminf(mx1, (diag && c + 1 > r) ? kInf : __uint_as_float(sr[c + 1]));
-          mx2 = fminf(mx2, (diag && c + 2 > r) ? kInf : __uint_as_float(sr[c + 2]));
-          mx3 = fminf(mx3, (diag && c + 3 > r) ? kInf : __uint_as_float(sr[c + 3]));
-        }
-        mx0 = fminf(fminf(mx0, mx1), fminf(mx2, mx3));
+        for (int c = 0; c < 128; ++c) sr[c] = (c > r) ? kNegInf : sr[c];
       }
-      const float xm = mx0 * sl;
+      const float xm = row_max128(sr) * sl;
       const bool need = xm > m + kTau;  // always true on the first block (m = -inf)
       float f = 1.f;
       if (need) {
         f = ex2_approx(m - xm);  // 0 when m = -inf
         m = xm;
-        l *= f;
-        l32 *= f;
-      }
-      const float neg_m = -m;
-
-      // probabilities, rounded to bf16 pairs in place of the scores
-      float la0 = 0.f, la1 = 0.f, lb0 = 0.f, lb1 = 0.f;
-      uint32_t pr[64];
 #pragma unroll
-      for (int c = 0; c < 128; c += 2) {
-        float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl, neg_m));
-        float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl, neg_m));
-        if (diag) {
-          p0 = (c > r) ? 0.f : p0;
-          p1 = (c + 1 > r) ? 0.f : p1;
+        for (int i = 0; i < 8; ++i) {
+          a32[i] *= f;
+          ar[i] *= f;
         }
-        const uint32_t pk = pack_bf16x2(p0, p1);
-        pr[c >> 1] = pk;
-        la0 += p0;
-        la1 += p1;
-        lb0 += __uint_as_float(pk << 16);
-        lb1 += __uint_as_float(pk & 0xFFFF0000u);
       }
-      l32 += la0 + la1;
-      l += lb0 + lb1;
+      uint32_t pr[64];
+      if (diag) softmax_exp<false>(sr, pr, sl, -m, a32, ar);
+      else softmax_exp<true>(sr, pr, sl, -m, a32, ar);
       tmem_st32(tS + 0, pr);
       tmem_st32(tS + 32, pr + 32);
 
@@ -477,11 +513,13 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     }
 
     // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32)
-    if (!wait_warp(smem_u32(&bars->o_full[s]), (uint32_t)o_cnt & 1u, abort_flag, p.status,
-                   lim))
+    if (!wait_warp(smem_u32(&bars->o_full[s]), (uint32_t)o_cnt & 1u, abort_flag, p.status, lim))
       return;
     ++o_cnt;
     tc_fence_after();
+    const float l = ((ar[0] + ar[1]) + (ar[2] + ar[3])) + ((ar[4] + ar[5]) + (ar[6] + ar[7]));
+    const float l32 =
+        ((a32[0] + a32[1]) + (a32[2] + a32[3])) + ((a32[4] + a32[5]) + (a32[6] + a32[7]));
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
     const float inv_l = 1.0f / l;
     p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
@@ -564,11 +602,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
-  if (warp == kWarpLoad) {
-    if (lane == 0) run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, q_base, ring_base, abort_flag);
-  } else if (warp == kWarpMma) {
-    if (lane == 0) run_mma<D>(p, bars, tmem, q_base, ring_base, abort_flag);
+  if (warp >= 8) {
+    regs_dec<kRegsOther>();
+    if (warp == kWarpLoad && lane == 0)
+      run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, q_base, ring_base, abort_flag);
+    else if (warp == kWarpMma && lane == 0)
+      run_mma<D>(p, bars, tmem, q_base, ring_base, abort_flag);
   } else {
+    regs_inc<kRegsSoftmax>();
     run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);
   }
   __syncwarp();  // reconverge each warp before the CTA-wide barrier

@@ -43,7 +43,8 @@ struct FwdParams {
   int n_empty;
   int nb;            // S / 128
   int S;
-  float scale_log2;  // scale * log2(e)
+  float scale_log2;  // |scale| * log2(e) (> 0; a tiny positive value stands in for scale = 0)
+  int neg_scale;     // scale < 0: the S MMA computes -Q K^T
   int causal;
   unsigned long long timeout_ns;
 };
@@ -51,6 +52,7 @@ struct FwdParams {
 constexpr unsigned long long kDefaultWaitTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
 
 // api.cu helpers
+void set_scale_params(FwdParams& p, float scale);
 bool get_tensor_map_encoder();
 int device_sm_count(int dev);
 bool aligned16(const void* p);

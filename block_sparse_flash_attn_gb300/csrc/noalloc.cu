@@ -162,7 +162,7 @@ extern "C" bsattn_status bsattn_fwd_noalloc(const void* q, const void* k, const 
   prm.n_empty = (int)(rows - n_live);
   prm.nb = nb;
   prm.S = S;
-  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  set_scale_params(prm, scale);
   prm.causal = causal;
   prm.timeout_ns = kDefaultWaitTimeoutNs;
   e = launch_fwd(D, (flags & BSATTN_OUT_F32) != 0, tq, tk, tv, prm, device_sm_count(dev), st);

@@ -226,6 +226,64 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// 3-input maximum (sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Packed fp32 pair arithmetic (sm_100+): one instruction for two lanes of work.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Register budget of the executing warpgroup (all four warps execute it).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// 2^x for a pair, on the FMA pipe instead of the MUFU unit (x <= 126).
+// Range reduction x = n + f with n = rint(x), |f| <= 1/2, then a cubic for
+// 2^f (coefficients fitted here for minimum relative error on [-1/2, 1/2]:
+// max relative error 7.6e-5, far below bf16's 2^-9 half-ulp), then 2^n is
+// applied by adding n to the exponent field.  x is clamped at -125 so the
+// exponent field never underflows (2^-125 stands in for smaller values).
+__device__ __forceinline__ void exp2_poly2(float& y0, float& y1, float x0, float x1) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer
+  constexpr float c0 = 0.99992847f, c1 = 0.69326085f, c2 = 0.24260531f, c3 = 0.05516921f;
+  x0 = fmaxf(x0, -125.f);
+  x1 = fmaxf(x1, -125.f);
+  float t0, t1, n0, n1, f0, f1, q0, q1;
+  add2(t0, t1, x0, x1, kRound, kRound);       // low mantissa bits of t hold rint(x)
+  add2(n0, n1, t0, t1, -kRound, -kRound);     // rint(x) as a float
+  fma2(f0, f1, n0, n1, -1.f, -1.f, x0, x1);  // f = x - rint(x) in [-1/2, 1/2]
+  fma2(q0, q1, f0, f1, c3, c3, c2, c2);
+  fma2(q0, q1, q0, q1, f0, f1, c1, c1);
+  fma2(q0, q1, q0, q1, f0, f1, c0, c0);
+  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
+}
+
 // Pack two floats to bf16x2 with round-to-nearest-even: `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
