@@ -11,26 +11,36 @@
 // Dead key blocks are never loaded (the mask's purpose in "Writing the Kernel
 // Logic": only the small 128x128 block is ever materialised).
 //
-// GB300 design (one persistent CTA per SM, 384 threads = 3 warpgroups):
-//   warps 0-3  softmax + epilogue for query slot 0 (TMEM lanes 0..127)
-//   warps 4-7  softmax + epilogue for query slot 1
-//   warp  8    TMA producer and tile scheduler (one elected lane)
-//   warp  9    tcgen05 MMA issuer (one elected lane), TMEM owner
-//   warps 10-11 idle (they complete warpgroup 2 so it can hand its
-//              registers to the softmax warpgroups with setmaxnreg)
+// GB300 design (one persistent CTA per SM, 640 threads = 5 warpgroups):
+//   warps 0-7   softmax + epilogue for query slot 0: warpgroup 0 owns key
+//               columns 0..63 of every block (and O columns [0, D/2)),
+//               warpgroup 1 columns 64..127 (O columns [D/2, D)); thread =
+//               one query row (TMEM lane) x one half of the columns
+//   warps 8-15  the same for query slot 1
+//   warp  16/19 TMA producer and tile scheduler of slot 0 / slot 1
+//   warp  17/18 tcgen05 MMA issuer of slot 0 / slot 1 (warp 17 owns TMEM)
+// Each slot is an independent pipeline with its own Q, K and V buffers in
+// shared memory, so one slot's MMA warp can feed the tensor core while the
+// other waits for its softmax or its data (tcgen05.mma issue is close to
+// synchronous: the hardware queue holds only a few instructions).
 // Two query tiles are in flight per CTA so the tensor core works on one slot
 // while the other slot's softmax runs.  Tensor memory (512 columns):
 //   S0 = [0,128), S1 = [128,256): fp32 scores, overwritten in place by the
-//   bf16 probabilities P (columns 0..63 of the slot's S region);
+//   bf16 probabilities P: keys 0..63 in columns 0..31, keys 64..127 in
+//   columns 64..95 of the slot's S region (each half writes only over
+//   scores it has already read);
 //   O0 = [256,384), O1 = [384,512): fp32 output accumulators.
-// Shared memory: Q tile per slot, a ring of K/V tiles (each 128 x D bf16,
-// 128-byte swizzled by TMA, read by tcgen05.mma through matrix descriptors).
+// Shared memory per slot: Q tile, a ring of K tiles and a ring of V tiles
+// (each 128 x D bf16, 128-byte swizzled by TMA, read by tcgen05.mma through
+// matrix descriptors).
 //
-// Per slot and tile with n live key blocks the MMA warp runs
+// Per slot and tile with n live key blocks the slot's MMA warp runs
 //   S(0); then for j = 1..n-1: [wait P(j-1)] O += P(j-1) V(j-1); S(j);
 //   finally [wait P(n-1)] O += P(n-1) V(n-1); signal O ready.
-// Because tcgen05 ops of one thread complete in order, "S(j) done" also
-// means "PV(j-1) done", so the softmax may rescale O right after seeing S(j).
+// The commit after S(j) frees K(j)'s buffer and is also the softmax's "S(j)
+// ready" signal.  Because tcgen05 ops of one thread complete in order,
+// "S(j) done" also means "PV(j-1) done", so the softmax may rescale O right
+// after seeing S(j).
 // Online softmax in base 2 with lazy rescale: the running max m only moves
 // when a block's max exceeds it by more than 8 (log2 units), so P <= 256 and
 // the O rescale (a TMEM round trip) is rare after the first block.
@@ -47,11 +57,16 @@
 namespace bsattn {
 namespace {
 
-constexpr int kThreads = 384;
-constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
-constexpr int kRegsSoftmax = 208;  // 2 x 128 x 208 + 128 x 88 = 384 x 168 (launch budget)
-constexpr int kRegsOther = 88;
+constexpr int kThreads = 640;
+constexpr int kSoftmaxThreads = 512;
+constexpr int kWarpLoad0 = 16;
+constexpr int kWarpMma0 = 17;
+constexpr int kWarpMma1 = 18;
+constexpr int kWarpLoad1 = 19;
+// Launch budget 640 x 96 registers; the producer/MMA warpgroup gives part of
+// its share to the four softmax warpgroups: 512 x 104 + 128 x 64 = 640 x 96.
+constexpr int kRegsSoftmax = 104;
+constexpr int kRegsOther = 64;
 constexpr float kTau = 8.0f;
 // Every kPolyEvery-th pair of probabilities in a block without causal masking
 // is computed by the FMA-pipe polynomial instead of the MUFU ex2 (0 = never).
@@ -67,11 +82,13 @@ struct Cfg {
   static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
   static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
-  static constexpr int kStages = (D == 128) ? 4 : 8;
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kBarOff = kRingOff + kStages * kTileBytes;
-  static constexpr int kSmem = kBarOff + 1024;
+  static constexpr int kKStages = (D == 128) ? 1 : 2;  // K buffers per slot
+  static constexpr int kVStages = (D == 128) ? 1 : 2;  // V buffers per slot
+  static constexpr int kQOff = 0;                                    // Q[slot]
+  static constexpr int kKOff = 2 * kTileBytes;                       // K[slot][stage]
+  static constexpr int kVOff = kKOff + 2 * kKStages * kTileBytes;    // V[slot][stage]
+  static constexpr int kBarOff = kVOff + 2 * kVStages * kTileBytes;
+  static constexpr int kSmem = kBarOff + 10240;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, true);
 };
@@ -85,19 +102,23 @@ struct TileInfo {
 };
 
 struct __align__(16) Bars {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t k_full[2][2];   // [slot][stage]
+  uint64_t k_empty[2][2];  // completes when S(j) is done: K(j) free, S(j) ready
+  uint64_t v_full[2][2];
+  uint64_t v_empty[2][2];
   uint64_t q_full[2];
   uint64_t q_empty[2];
-  uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t tq_full[2][2];
   uint64_t tq_empty[2][2];
-  uint64_t drain;
+  uint64_t drain[2];
+  uint64_t xchg[2];  // per slot: the two column halves exchange row maxima / sums
   TileInfo tq[2][2];
   uint32_t tmem_base;
   int abort_flag;
+  float xmax[2][2][2][128];  // [slot][use parity][half][row] block row maxima
+  float2 xsum[2][2][128];    // [slot][half][row] partial row sums at the end of a tile
 };
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
@@ -112,246 +133,224 @@ __device__ __forceinline__ void raise_internal(volatile int* abort_flag, int* st
   atomicOr(status, kStatusInternal);
 }
 
+// Every role runs with its whole warp converged (warp-collective tcgen05.ld/st
+// in the softmax; uniform bookkeeping in the producer and MMA roles, which
+// issue their single-thread instructions from an elected lane), so every
+// lane must take the same path after a wait: the outcome is made uniform.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status, uint64_t limit_ns) {
+  const bool ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------
-// warp 8: tile scheduler + TMA producer
+// producer warp of slot s: tile scheduler + TMA loads
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+__device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, Bars* bars,
-                             uint32_t q_base, uint32_t ring_base, volatile int* abort_flag) {
+                             uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D>;
   const uint64_t lim = p.timeout_ns;
-  int it = 0;
-  int tq_cnt[2] = {0, 0}, q_cnt[2] = {0, 0};
-  int jn[2] = {0, 0}, n[2] = {0, 0}, rp[2] = {0, 0}, hrow[2] = {0, 0};
-  bool active[2] = {true, true};
+  int kc = 0, vc = 0, qc = 0, tqc = 0;  // K / V / Q tiles loaded, tiles claimed
   bool ok = true;
 
-  auto push = [&](const CUtensorMap* tm, int kb, int s) -> bool {
+  // One TMA tile (128 rows x D) into a buffer, completion on `full`, after
+  // `empty` says the buffer's previous contents were consumed.
+  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, uint32_t empty,
+                       uint32_t empty_parity, int row) -> bool {
+    if (!wait_warp(empty, empty_parity, abort_flag, p.status, lim)) return false;
+    if (elect_one()) {
+      mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, full, c * 64, row);
+    }
+    __syncwarp();
+    return true;
+  };
+  auto load_k = [&](int kb, int hrow) -> bool {
     if (kb < 0 || kb >= p.nb) {
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int st = it % C::kStages;
-    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-    if (!wait_bounded(smem_u32(&bars->empty[st]), ph ^ 1u, abort_flag, p.status, lim))
+    const int st = kc % C::kKStages;
+    const uint32_t ph = ((uint32_t)(kc / C::kKStages) & 1u) ^ 1u;
+    ++kc;
+    return load_tile(tm_k, smem_base + C::kKOff + (s * C::kKStages + st) * C::kTileBytes,
+                     smem_u32(&bars->k_full[s][st]), smem_u32(&bars->k_empty[s][st]), ph,
+                     hrow + kb * kBlock);
+  };
+  auto load_v = [&](int kb, int hrow) -> bool {
+    if (kb < 0 || kb >= p.nb) {
+      raise_internal(abort_flag, p.status);
       return false;
-    const uint32_t fb = smem_u32(&bars->full[st]);
-    mbar_arrive_expect_tx(fb, C::kTileBytes);
-    const uint32_t dst = ring_base + st * C::kTileBytes;
-#pragma unroll
-    for (int c = 0; c < C::kBoxes; ++c)
-      tma_load_2d(dst + c * C::kBoxBytes, tm, fb, c * 64, hrow[s] + kb * kBlock);
-    ++it;
-    return true;
+    }
+    const int st = vc % C::kVStages;
+    const uint32_t ph = ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u;
+    ++vc;
+    return load_tile(tm_v, smem_base + C::kVOff + (s * C::kVStages + st) * C::kTileBytes,
+                     smem_u32(&bars->v_full[s][st]), smem_u32(&bars->v_empty[s][st]), ph,
+                     hrow + kb * kBlock);
   };
 
-  while (ok && (active[0] || active[1])) {
-    for (int s = 0; s < 2 && ok; ++s) {
-      if (!active[s]) continue;
-      if (jn[s] == 0) {
-        const int e = tq_cnt[s] & 1;
-        const uint32_t ph = (uint32_t)(tq_cnt[s] >> 1) & 1u;
-        if (!wait_bounded(smem_u32(&bars->tq_empty[s][e]), ph ^ 1u, abort_flag, p.status, lim)) {
-          ok = false;
-          break;
-        }
-        const int idx = atomicAdd(p.counter, 1);
-        const int t = idx < p.n_live ? p.tile_order[idx] : -1;
-        int r0 = 0, cnt = 0, bh = 0, qb = 0, diag = 0;
-        if (t >= 0) {
-          r0 = p.row_ptr[t];
-          cnt = p.row_ptr[t + 1] - r0;
-          bh = t / p.nb;
-          qb = t - bh * p.nb;
-          if (cnt <= 0 || cnt > p.nb) {
-            raise_internal(abort_flag, p.status);
-            ok = false;
-            break;
-          }
-          diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
-        }
-        volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[s][e]);
-        slot[0] = t;
-        slot[1] = r0;
-        slot[2] = cnt;
-        slot[3] = diag;
-        mbar_arrive(smem_u32(&bars->tq_full[s][e]));
-        ++tq_cnt[s];
-        if (t < 0) {
-          active[s] = false;
-          continue;
-        }
-        rp[s] = r0;
-        n[s] = cnt;
-        hrow[s] = bh * p.S;
-        const uint32_t qph = ((uint32_t)q_cnt[s] & 1u) ^ 1u;
-        if (!wait_bounded(smem_u32(&bars->q_empty[s]), qph, abort_flag, p.status, lim)) {
-          ok = false;
-          break;
-        }
-        ++q_cnt[s];
-        const uint32_t qbar = smem_u32(&bars->q_full[s]);
-        mbar_arrive_expect_tx(qbar, C::kTileBytes);
-#pragma unroll
-        for (int c = 0; c < C::kBoxes; ++c)
-          tma_load_2d(q_base + s * C::kTileBytes + c * C::kBoxBytes, tm_q, qbar, c * 64,
-                      hrow[s] + qb * kBlock);
-        if (!push(tm_k, p.col_idx[r0], s)) {
-          ok = false;
-          break;
-        }
-        jn[s] = 1;
-      } else {
-        if (!push(tm_v, p.col_idx[rp[s] + jn[s] - 1], s)) {
-          ok = false;
-          break;
-        }
-        if (jn[s] < n[s]) {
-          if (!push(tm_k, p.col_idx[rp[s] + jn[s]], s)) {
-            ok = false;
-            break;
-          }
-          ++jn[s];
-        } else {
-          jn[s] = 0;
-        }
+  while (ok) {
+    // claim a tile and publish it to this slot's MMA and softmax warps
+    const int e = tqc & 1;
+    const uint32_t ph = (uint32_t)(tqc >> 1) & 1u;
+    if (!wait_warp(smem_u32(&bars->tq_empty[s][e]), ph ^ 1u, abort_flag, p.status, lim)) break;
+    int idx = 0;
+    if (elect_one()) idx = atomicAdd(p.counter, 1);
+    idx = __reduce_max_sync(0xffffffffu, idx);  // the elected lane's claim, to every lane
+    const int t = idx < p.n_live ? p.tile_order[idx] : -1;
+    int r0 = 0, cnt = 0, bh = 0, qb = 0, diag = 0;
+    if (t >= 0) {
+      r0 = p.row_ptr[t];
+      cnt = p.row_ptr[t + 1] - r0;
+      bh = t / p.nb;
+      qb = t - bh * p.nb;
+      if (cnt <= 0 || cnt > p.nb) {
+        raise_internal(abort_flag, p.status);
+        break;
       }
+      diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
     }
+    if (elect_one()) {
+      volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[s][e]);
+      slot[0] = t;
+      slot[1] = r0;
+      slot[2] = cnt;
+      slot[3] = diag;
+      mbar_arrive(smem_u32(&bars->tq_full[s][e]));
+    }
+    __syncwarp();
+    ++tqc;
+    if (t < 0) break;
+    const int hrow = bh * p.S;
+    // Q, once its buffer is free (the previous tile's last S is done)
+    ok = load_tile(tm_q, smem_base + C::kQOff + s * C::kTileBytes, smem_u32(&bars->q_full[s]),
+                   smem_u32(&bars->q_empty[s]), ((uint32_t)qc & 1u) ^ 1u, hrow + qb * kBlock);
+    ++qc;
+    if (ok) ok = load_k(p.col_idx[r0], hrow);
+    for (int j = 1; ok && j < cnt; ++j) {
+      ok = load_v(p.col_idx[r0 + j - 1], hrow);  // V(j-1) frees up before K(j)
+      if (ok) ok = load_k(p.col_idx[r0 + j], hrow);
+    }
+    if (ok) ok = load_v(p.col_idx[r0 + cnt - 1], hrow);
   }
   if (!ok) {
     // Let every TMA load this warp issued land before the CTA exits.
-    for (int i = (it > C::kStages ? it - C::kStages : 0); i < it; ++i)
-      wait_drain(smem_u32(&bars->full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u);
-    for (int s = 0; s < 2; ++s)
-      if (q_cnt[s] > 0) wait_drain(smem_u32(&bars->q_full[s]), (uint32_t)(q_cnt[s] - 1) & 1u);
+    for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
+      wait_drain(smem_u32(&bars->k_full[s][i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
+    for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
+      wait_drain(smem_u32(&bars->v_full[s][i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
+    if (qc > 0) wait_drain(smem_u32(&bars->q_full[s]), (uint32_t)(qc - 1) & 1u);
   }
 }
 
 // ---------------------------------------------------------------------------
-// warp 9: tcgen05 MMA issuer
+// MMA warp of slot s: tcgen05 issue from one elected lane
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t q_base,
-                        uint32_t ring_base, volatile int* abort_flag) {
+__device__ void run_mma(int s, const FwdParams& p, Bars* bars, uint32_t tmem,
+                        uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D>;
   const uint64_t lim = p.timeout_ns;
-  int it = 0;
-  int tq_cnt[2] = {0, 0}, q_cnt[2] = {0, 0}, p_cnt[2] = {0, 0};
-  int jn[2] = {0, 0}, n[2] = {0, 0};
-  bool active[2] = {true, true};
+  int kc = 0, vc = 0, qc = 0, pc = 0, tqc = 0;
   bool ok = true;
+  const uint32_t qaddr = smem_base + C::kQOff + s * C::kTileBytes;
+  const uint32_t tS = tmem + s * 128;
+  const uint32_t tO = tmem + 256 + s * 128;
+  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
+  // swizzle row; a new 64-column box every 4 steps).  A negative scale is
+  // applied as -Q (instruction-descriptor negate bit) so the softmax always
+  // sees a non-negative multiplier.
+  const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
 
-  auto pop = [&](uint32_t& addr, uint32_t& empty_bar) -> bool {
-    const int st = it % C::kStages;
-    const uint32_t ph = (uint32_t)(it / C::kStages) & 1u;
-    if (!wait_bounded(smem_u32(&bars->full[st]), ph, abort_flag, p.status, lim)) return false;
-    addr = ring_base + st * C::kTileBytes;
-    empty_bar = smem_u32(&bars->empty[st]);
-    ++it;
+  auto commit = [&](uint32_t bar) {
+    if (elect_one()) mma_commit(bar);
+    __syncwarp();
+  };
+  // issue S(j) from the next K buffer; its commit frees the buffer and tells
+  // the softmax that S(j) is ready
+  auto do_s = [&]() -> bool {
+    const int st = kc % C::kKStages;
+    if (!wait_warp(smem_u32(&bars->k_full[s][st]), (uint32_t)(kc / C::kKStages) & 1u,
+                   abort_flag, p.status, lim))
+      return false;
+    const uint32_t kaddr = smem_base + C::kKOff + (s * C::kKStages + st) * C::kTileBytes;
+    if (elect_one()) {
+      // descriptors advance by adding the byte offset >> 4 to the start-address field
+      const uint64_t qd = smem_desc_sw128(qaddr, 16, 1024);
+      const uint64_t kd = smem_desc_sw128(kaddr, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+        mma_ss(tS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars->k_empty[s][st]));
+    }
+    __syncwarp();
+    ++kc;
+    return true;
+  };
+  // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P is read from TMEM
+  // (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31, keys
+  // 64..127 at columns 64..95); V is MN-major (D contiguous): 8-key groups
+  // 1024 bytes apart, 64-column boxes 16 KB apart.
+  auto do_pv = [&](bool accumulate) -> bool {
+    if (!wait_warp(smem_u32(&bars->p_full[s]), (uint32_t)pc & 1u, abort_flag, p.status, lim))
+      return false;
+    ++pc;
+    const int st = vc % C::kVStages;
+    if (!wait_warp(smem_u32(&bars->v_full[s][st]), (uint32_t)(vc / C::kVStages) & 1u,
+                   abort_flag, p.status, lim))
+      return false;
+    tc_fence_after();
+    const uint32_t vaddr = smem_base + C::kVOff + (s * C::kVStages + st) * C::kTileBytes;
+    if (elect_one()) {
+      const uint64_t vd = smem_desc_sw128(vaddr, C::kBoxBytes, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
+        mma_ts(tO, tS + pcol, vd + (uint32_t)(kk * 2048 >> 4), C::kIdescO,
+               (accumulate || kk > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(&bars->v_empty[s][st]));
+    }
+    __syncwarp();
+    ++vc;
     return true;
   };
 
-  // S[s] = Q[s] K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a
-  // 128-byte swizzle row; a new 64-column box every 4 steps).  A negative
-  // scale is applied as -Q (instruction-descriptor negate bit) so the
-  // softmax always sees a non-negative multiplier.
-  const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
-  auto issue_s = [&](int s, uint32_t kaddr) {
-    const uint32_t qaddr = q_base + s * C::kTileBytes;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-      const uint64_t ad = smem_desc_sw128(qaddr + off, 16, 1024);
-      const uint64_t bd = smem_desc_sw128(kaddr + off, 16, 1024);
-      mma_ss(tmem + s * 128, ad, bd, idesc_s, kk > 0 ? 1u : 0u);
+  while (ok) {
+    const int e = tqc & 1;
+    if (!wait_warp(smem_u32(&bars->tq_full[s][e]), (uint32_t)(tqc >> 1) & 1u, abort_flag,
+                   p.status, lim))
+      break;
+    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
+    const int t = slot[0];
+    const int n = slot[2];
+    if (elect_one()) mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
+    __syncwarp();
+    ++tqc;
+    if (t < 0) break;
+    if (!wait_warp(smem_u32(&bars->q_full[s]), (uint32_t)qc & 1u, abort_flag, p.status, lim))
+      break;
+    ++qc;
+    tc_fence_after();
+    ok = do_s();
+    if (ok && n == 1) commit(smem_u32(&bars->q_empty[s]));
+    for (int j = 1; ok && j < n; ++j) {
+      ok = do_pv(j > 1);
+      if (ok) ok = do_s();
+      if (ok && j == n - 1) commit(smem_u32(&bars->q_empty[s]));
     }
-  };
-  // O[s] (+)= P[s] V : M=128, N=D, K=128 keys in steps of 16.  P is read from
-  // TMEM (bf16 pairs, 8 columns per step); V is MN-major (D contiguous):
-  // 8-key groups 1024 bytes apart, 64-column boxes 16 KB apart.
-  auto issue_pv = [&](int s, uint32_t vaddr, bool accumulate) {
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint64_t bd = smem_desc_sw128(vaddr + kk * 2048, C::kBoxBytes, 1024);
-      mma_ts(tmem + 256 + s * 128, tmem + s * 128 + kk * 8, bd, C::kIdescO,
-             (accumulate || kk > 0) ? 1u : 0u);
-    }
-  };
-
-  while (ok && (active[0] || active[1])) {
-    for (int s = 0; s < 2 && ok; ++s) {
-      if (!active[s]) continue;
-      if (jn[s] == 0) {
-        const int e = tq_cnt[s] & 1;
-        const uint32_t ph = (uint32_t)(tq_cnt[s] >> 1) & 1u;
-        if (!wait_bounded(smem_u32(&bars->tq_full[s][e]), ph, abort_flag, p.status, lim)) {
-          ok = false;
-          break;
-        }
-        const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
-        const int t = slot[0];
-        const int cnt = slot[2];
-        mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
-        ++tq_cnt[s];
-        if (t < 0) {
-          active[s] = false;
-          continue;
-        }
-        n[s] = cnt;
-        if (!wait_bounded(smem_u32(&bars->q_full[s]), (uint32_t)q_cnt[s] & 1u, abort_flag,
-                          p.status, lim)) {
-          ok = false;
-          break;
-        }
-        ++q_cnt[s];
-        uint32_t kaddr, eb;
-        if (!pop(kaddr, eb)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_s(s, kaddr);
-        mma_commit(eb);
-        if (n[s] == 1) mma_commit(smem_u32(&bars->q_empty[s]));
-        mma_commit(smem_u32(&bars->s_full[s]));
-        jn[s] = 1;
-      } else {
-        if (!wait_bounded(smem_u32(&bars->p_full[s]), (uint32_t)p_cnt[s] & 1u, abort_flag,
-                          p.status, lim)) {
-          ok = false;
-          break;
-        }
-        ++p_cnt[s];
-        uint32_t vaddr, eb;
-        if (!pop(vaddr, eb)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(s, vaddr, jn[s] > 1);
-        mma_commit(eb);
-        if (jn[s] < n[s]) {
-          uint32_t kaddr, eb2;
-          if (!pop(kaddr, eb2)) {
-            ok = false;
-            break;
-          }
-          issue_s(s, kaddr);
-          mma_commit(eb2);
-          if (jn[s] == n[s] - 1) mma_commit(smem_u32(&bars->q_empty[s]));
-          mma_commit(smem_u32(&bars->s_full[s]));
-          ++jn[s];
-        } else {
-          mma_commit(smem_u32(&bars->o_full[s]));
-          jn[s] = 0;
-        }
-      }
-    }
+    if (ok) ok = do_pv(n > 1);
+    if (ok) commit(smem_u32(&bars->o_full[s]));
   }
   // Every MMA issued so far must finish before TMEM is released.
-  mma_commit(smem_u32(&bars->drain));
-  wait_drain(smem_u32(&bars->drain), 0);
+  commit(smem_u32(&bars->drain[s]));
+  wait_drain(smem_u32(&bars->drain[s]), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -360,7 +359,7 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
 template <int D, bool OUT_F32>
 __device__ void write_empty_tiles(const FwdParams& p) {
   using OutT = typename std::conditional<OUT_F32, float, uint16_t>::type;
-  const int tid = threadIdx.x;  // 0..255
+  const int tid = threadIdx.x;  // 0..kSoftmaxThreads-1
   constexpr int kVec = 16 / sizeof(OutT);
   for (int e = blockIdx.x; e < p.n_empty; e += gridDim.x) {
     const int t = p.empty_tiles[e];
@@ -369,27 +368,19 @@ __device__ void write_empty_tiles(const FwdParams& p) {
     const size_t row0 = (size_t)bh * p.S + (size_t)qb * kBlock;
     uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<OutT*>(p.out) + row0 * D);
     const int nvec = kBlock * D / kVec;
-    for (int i = tid; i < nvec; i += 256) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = tid; i < nvec; i += kSoftmaxThreads) dst[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid < kBlock) p.lse[row0 + tid] = -__int_as_float(0x7f800000);
   }
 }
 
-// The softmax warps execute warp-collective tcgen05.ld/st, so every lane of a
-// warp must take the same path after a wait: the outcome is made uniform.
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status, uint64_t limit_ns) {
-  const bool ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
-  return __all_sync(0xffffffffu, ok);
-}
-
-// Probabilities of one 128-column row slice: p = 2^(s*sl - m), rounded to
-// bf16 pairs into pr[]; returns the running sums of the unrounded (a32) and of
-// the rounded (ar) values in four independent pairs of accumulators.
+// Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
+// pairs into pr[]; accumulates the unrounded (a32, for LSE) and the rounded
+// (ar, the O denominator) row sums in two independent accumulators each.
 template <bool POLY>
-__device__ __forceinline__ void softmax_exp(const uint32_t* sr, uint32_t* pr, float sl, float nm,
-                                            float (&a32)[8], float (&ar)[8]) {
+__device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
+                                              float nm, float (&a32)[2], float (&ar)[2]) {
 #pragma unroll
-  for (int q = 0; q < 64; ++q) {
+  for (int q = 0; q < 32; ++q) {
     float x0, x1;
     fma2(x0, x1, __uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1]), sl, sl, nm, nm);
     float p0, p1;
@@ -401,19 +392,18 @@ __device__ __forceinline__ void softmax_exp(const uint32_t* sr, uint32_t* pr, fl
     }
     const uint32_t pk = pack_bf16x2(p0, p1);
     pr[q] = pk;
-    const int k = (q & 3) * 2;
-    add2(a32[k], a32[k + 1], a32[k], a32[k + 1], p0, p1);
-    add2(ar[k], ar[k + 1], ar[k], ar[k + 1], __uint_as_float(pk << 16),
+    add2(a32[0], a32[1], a32[0], a32[1], p0, p1);
+    add2(ar[0], ar[1], ar[0], ar[1], __uint_as_float(pk << 16),
          __uint_as_float(pk & 0xFFFF0000u));
   }
 }
 
-__device__ __forceinline__ float row_max128(const uint32_t* sr) {
+__device__ __forceinline__ float row_max64(const uint32_t* sr) {
   float a[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) a[i] = fmaxf(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1]));
 #pragma unroll
-  for (int c = 16; c < 128; c += 16) {
+  for (int c = 16; c < 64; c += 16) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
       a[i] = max3(a[i], __uint_as_float(sr[c + 2 * i]), __uint_as_float(sr[c + 2 * i + 1]));
@@ -424,21 +414,31 @@ __device__ __forceinline__ float row_max128(const uint32_t* sr) {
 template <int D, bool OUT_F32>
 __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
+  constexpr int DH = D / 2;            // O columns owned by this thread
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int s = warp >> 2;             // query slot
+  const int s = warp >> 3;             // query slot
+  const int h = (warp >> 2) & 1;       // column half: keys [64h, 64h+64), O cols [DH h, DH h+DH)
   const int sub = warp & 3;            // TMEM sub-partition: lanes 32*sub .. 32*sub+31
   const int r = sub * 32 + lane;       // row of the query tile owned by this thread
   const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-  const uint32_t tS = tmem + s * 128 + lane_off;
-  const uint32_t tO = tmem + 256 + s * 128 + lane_off;
+  const uint32_t tS = tmem + s * 128 + h * 64 + lane_off;  // my 64 score columns (P over the first 32)
+  const uint32_t tO = tmem + 256 + s * 128 + h * DH + lane_off;
   const float sl = p.scale_log2;       // > 0 (see FwdParams)
   const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
+  const uint32_t xbar = smem_u32(&bars->xchg[s]);
 
   write_empty_tiles<D, OUT_F32>(p);
 
-  int tq_cnt = 0, s_cnt = 0, o_cnt = 0;
+  int tq_cnt = 0, s_cnt = 0, o_cnt = 0, x_cnt = 0;
+  // exchange with the other half of this slot: arrive, then wait for all 256
+  auto exchange = [&]() -> bool {
+    mbar_arrive(xbar);
+    const bool ok = wait_warp(xbar, (uint32_t)x_cnt & 1u, abort_flag, p.status, lim);
+    ++x_cnt;
+    return ok;
+  };
   for (;;) {
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
@@ -454,50 +454,53 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
-    float a32[8], ar[8];                 // unrounded (LSE) and rounded (O) row sums
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a32[i] = ar[i] = 0.f;
+    float a32[2] = {0.f, 0.f}, ar[2] = {0.f, 0.f};  // unrounded (LSE) / rounded (O) partial sums
     for (int jb = 0; jb < n; ++jb) {
-      if (!wait_warp(smem_u32(&bars->s_full[s]), (uint32_t)s_cnt & 1u, abort_flag, p.status,
-                     lim))
-        return;
+      // S(jb) ready = the slot's K buffer of this block was released by its S MMA
+      {
+        constexpr int NK = (D == 128) ? 1 : 2;  // Cfg<D>::kKStages
+        if (!wait_warp(smem_u32(&bars->k_empty[s][s_cnt % NK]), (uint32_t)(s_cnt / NK) & 1u,
+                       abort_flag, p.status, lim))
+          return;
+      }
+      const int par = s_cnt & 1;
       ++s_cnt;
       tc_fence_after();
-      uint32_t sr[128];
+      uint32_t sr[64];
       tmem_ld32(tS + 0, sr + 0);
       tmem_ld32(tS + 32, sr + 32);
-      tmem_ld32(tS + 64, sr + 64);
-      tmem_ld32(tS + 96, sr + 96);
       tmem_wait_ld();
-      reg_fence(sr, 128);
+      reg_fence(sr, 64);
       const bool diag = diag_last && jb == n - 1;
       if (diag) {  // causal diagonal tile: key c is allowed for query row r iff c <= r
 #pragma unroll
-        for (int c = 0; c < 128; ++c) sr[c] = (c > r) ? kNegInf : sr[c];
+        for (int c = 0; c < 64; ++c) sr[c] = (h * 64 + c > r) ? kNegInf : sr[c];
       }
-      const float xm = row_max128(sr) * sl;
+      float mx = row_max64(sr);
+      bars->xmax[s][par][h][r] = mx;
+      if (!exchange()) return;
+      mx = fmaxf(mx, bars->xmax[s][par][h ^ 1][r]);
+      const float xm = mx * sl;
       const bool need = xm > m + kTau;  // always true on the first block (m = -inf)
       float f = 1.f;
       if (need) {
         f = ex2_approx(m - xm);  // 0 when m = -inf
         m = xm;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          a32[i] *= f;
-          ar[i] *= f;
-        }
+        a32[0] *= f;
+        a32[1] *= f;
+        ar[0] *= f;
+        ar[1] *= f;
       }
-      uint32_t pr[64];
-      if (diag) softmax_exp<false>(sr, pr, sl, -m, a32, ar);
-      else softmax_exp<true>(sr, pr, sl, -m, a32, ar);
-      tmem_st32(tS + 0, pr);
-      tmem_st32(tS + 32, pr + 32);
+      uint32_t pr[32];
+      if (diag) softmax_exp64<false>(sr, pr, sl, -m, a32, ar);
+      else softmax_exp64<true>(sr, pr, sl, -m, a32, ar);
+      tmem_st32(tS, pr);
 
-      // O rescale when this row's max moved (PV(jb-1) is complete: S(jb) was
-      // committed after it).
+      // O rescale (this half's columns) when a row's max moved; PV(jb-1) is
+      // complete because S(jb) was committed after it.
       if (jb > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < DH; c0 += 32) {
           uint32_t orr[32];
           tmem_ld32(tO + c0, orr);
           tmem_wait_ld();
@@ -512,25 +515,29 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       mbar_arrive(smem_u32(&bars->p_full[s]));
     }
 
-    // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32)
+    // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
     if (!wait_warp(smem_u32(&bars->o_full[s]), (uint32_t)o_cnt & 1u, abort_flag, p.status, lim))
       return;
     ++o_cnt;
     tc_fence_after();
-    const float l = ((ar[0] + ar[1]) + (ar[2] + ar[3])) + ((ar[4] + ar[5]) + (ar[6] + ar[7]));
-    const float l32 =
-        ((a32[0] + a32[1]) + (a32[2] + a32[3])) + ((a32[4] + a32[5]) + (a32[6] + a32[7]));
+    const float my_l = ar[0] + ar[1];
+    const float my_l32 = a32[0] + a32[1];
+    bars->xsum[s][h][r] = make_float2(my_l, my_l32);
+    if (!exchange()) return;
+    const float2 other = bars->xsum[s][h ^ 1][r];
+    const float l = my_l + other.x;
+    const float l32 = my_l32 + other.y;
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
     const float inv_l = 1.0f / l;
-    p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
+    if (h == 0) p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 0; c0 < DH; c0 += 32) {
       uint32_t orr[32];
       tmem_ld32(tO + c0, orr);
       tmem_wait_ld();
       reg_fence(orr, 32);
       if constexpr (OUT_F32) {
-        float* dst = reinterpret_cast<float*>(p.out) + row * D + c0;
+        float* dst = reinterpret_cast<float*>(p.out) + row * D + h * DH + c0;
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           st_global_v4(dst + i, __float_as_uint(__uint_as_float(orr[i]) * inv_l),
@@ -538,7 +545,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                        __float_as_uint(__uint_as_float(orr[i + 2]) * inv_l),
                        __float_as_uint(__uint_as_float(orr[i + 3]) * inv_l));
       } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + c0;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + h * DH + c0;
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -562,36 +569,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles want 1024-byte alignment
   Bars* bars = reinterpret_cast<Bars*>(smem_raw + (base - raw) + C::kBarOff);
-  const uint32_t q_base = base + C::kQOff;
-  const uint32_t ring_base = base + C::kRingOff;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(smem_u32(&bars->full[i]), 1);
-      mbar_init(smem_u32(&bars->empty[i]), 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(&bars->q_full[s]), 1);
-      mbar_init(smem_u32(&bars->q_empty[s]), 1);
-      mbar_init(smem_u32(&bars->s_full[s]), 1);
-      mbar_init(smem_u32(&bars->p_full[s]), 128);
-      mbar_init(smem_u32(&bars->o_full[s]), 1);
+    for (int sl = 0; sl < 2; ++sl) {
+      for (int i = 0; i < C::kKStages; ++i) {
+        mbar_init(smem_u32(&bars->k_full[sl][i]), 1);
+        mbar_init(smem_u32(&bars->k_empty[sl][i]), 1);
+      }
+      for (int i = 0; i < C::kVStages; ++i) {
+        mbar_init(smem_u32(&bars->v_full[sl][i]), 1);
+        mbar_init(smem_u32(&bars->v_empty[sl][i]), 1);
+      }
+      mbar_init(smem_u32(&bars->q_full[sl]), 1);
+      mbar_init(smem_u32(&bars->q_empty[sl]), 1);
+      mbar_init(smem_u32(&bars->p_full[sl]), kSoftmaxThreads / 2);
+      mbar_init(smem_u32(&bars->xchg[sl]), kSoftmaxThreads / 2);
+      mbar_init(smem_u32(&bars->o_full[sl]), 1);
+      mbar_init(smem_u32(&bars->drain[sl]), 1);
       for (int e = 0; e < 2; ++e) {
-        mbar_init(smem_u32(&bars->tq_full[s][e]), 1);
-        mbar_init(smem_u32(&bars->tq_empty[s][e]), 1 + 128);
+        mbar_init(smem_u32(&bars->tq_full[sl][e]), 1);
+        mbar_init(smem_u32(&bars->tq_empty[sl][e]), 1 + kSoftmaxThreads / 2);
       }
     }
-    mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpLoad && lane == 0) {
+  if (warp == kWarpLoad0 && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -602,12 +611,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort_flag = &bars->abort_flag;
 
-  if (warp >= 8) {
+  if (warp >= kSoftmaxThreads / 32) {
     regs_dec<kRegsOther>();
-    if (warp == kWarpLoad && lane == 0)
-      run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, q_base, ring_base, abort_flag);
-    else if (warp == kWarpMma && lane == 0)
-      run_mma<D>(p, bars, tmem, q_base, ring_base, abort_flag);
+    if (warp == kWarpLoad0 || warp == kWarpLoad1)
+      run_producer<D>(warp == kWarpLoad0 ? 0 : 1, &tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
+    else
+      run_mma<D>(warp == kWarpMma0 ? 0 : 1, p, bars, tmem, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
     run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);
@@ -616,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMma0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -23,6 +23,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// One lane of a converged warp (elect.sync): the issuing lane for
+// single-thread instructions (TMA, tcgen05.mma, tcgen05.commit) while the
+// rest of the role's bookkeeping stays warp-uniform.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n\t.reg .b32 lane_id;\n\t.reg .pred p;\n\t"
+      "elect.sync lane_id|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------
