@@ -12,10 +12,11 @@
 // Logic": only the small 128x128 block is ever materialised).
 //
 // GB300 design (one persistent CTA per SM, 640 threads = 5 warpgroups):
-//   warps 0-7   softmax + epilogue for query slot 0: warpgroup 0 owns key
-//               columns 0..63 of every block (and O columns [0, D/2)),
-//               warpgroup 1 columns 64..127 (O columns [D/2, D)); thread =
-//               one query row (TMEM lane) x one half of the columns
+//   warps 0-7   softmax + epilogue for query slot 0: each warp covers 16
+//               query rows (TMEM lanes); lanes 0..15 of the warp own key
+//               columns 0..63 of every block (O columns [0, D/2)), lanes
+//               16..31 the same rows' columns 64..127 (O columns [D/2, D)),
+//               so the two halves of a row meet in one warp (shuffles)
 //   warps 8-15  the same for query slot 1
 //   warp  16/19 TMA producer and tile scheduler of slot 0 / slot 1
 //   warp  17/18 tcgen05 MMA issuer of slot 0 / slot 1 (warp 17 owns TMEM)
@@ -88,7 +89,7 @@ struct Cfg {
   static constexpr int kKOff = 2 * kTileBytes;                       // K[slot][stage]
   static constexpr int kVOff = kKOff + 2 * kKStages * kTileBytes;    // V[slot][stage]
   static constexpr int kBarOff = kVOff + 2 * kVStages * kTileBytes;
-  static constexpr int kSmem = kBarOff + 10240;
+  static constexpr int kSmem = kBarOff + 1024;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, true);
 };
@@ -113,12 +114,9 @@ struct __align__(16) Bars {
   uint64_t tq_full[2][2];
   uint64_t tq_empty[2][2];
   uint64_t drain[2];
-  uint64_t xchg[2];  // per slot: the two column halves exchange row maxima / sums
   TileInfo tq[2][2];
   uint32_t tmem_base;
   int abort_flag;
-  float xmax[2][2][2][128];  // [slot][use parity][half][row] block row maxima
-  float2 xsum[2][2][128];    // [slot][half][row] partial row sums at the end of a tile
 };
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
@@ -418,27 +416,22 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int s = warp >> 3;             // query slot
-  const int h = (warp >> 2) & 1;       // column half: keys [64h, 64h+64), O cols [DH h, DH h+DH)
   const int sub = warp & 3;            // TMEM sub-partition: lanes 32*sub .. 32*sub+31
-  const int r = sub * 32 + lane;       // row of the query tile owned by this thread
-  const uint32_t lane_off = (uint32_t)(sub * 32) << 16;
-  const uint32_t tS = tmem + s * 128 + h * 64 + lane_off;  // my 64 score columns (P over the first 32)
-  const uint32_t tO = tmem + 256 + s * 128 + h * DH + lane_off;
+  const int lh = (warp >> 2) & 1;      // which 16 lanes of the sub-partition this warp covers
+  const int ch = lane >> 4;            // column half: keys [64ch, 64ch+64), O cols [DH ch, DH ch+DH)
+  const int r = sub * 32 + lh * 16 + (lane & 15);  // query row (TMEM lane) of this thread
+  // 16x32bx2 accesses: lanes 0..15 of the warp take the address's columns,
+  // lanes 16..31 the same rows 64 (or DH) columns further on.
+  const uint32_t lane_off = (uint32_t)(sub * 32 + lh * 16) << 16;
+  const uint32_t tS = tmem + s * 128 + lane_off;
+  const uint32_t tO = tmem + 256 + s * 128 + lane_off;
   const float sl = p.scale_log2;       // > 0 (see FwdParams)
   const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
-  const uint32_t xbar = smem_u32(&bars->xchg[s]);
 
   write_empty_tiles<D, OUT_F32>(p);
 
-  int tq_cnt = 0, s_cnt = 0, o_cnt = 0, x_cnt = 0;
-  // exchange with the other half of this slot: arrive, then wait for all 256
-  auto exchange = [&]() -> bool {
-    mbar_arrive(xbar);
-    const bool ok = wait_warp(xbar, (uint32_t)x_cnt & 1u, abort_flag, p.status, lim);
-    ++x_cnt;
-    return ok;
-  };
+  int tq_cnt = 0, s_cnt = 0, o_cnt = 0;
   for (;;) {
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
@@ -463,23 +456,20 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                        abort_flag, p.status, lim))
           return;
       }
-      const int par = s_cnt & 1;
       ++s_cnt;
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld32(tS + 0, sr + 0);
-      tmem_ld32(tS + 32, sr + 32);
+      tmem_ld16x2_32<64>(tS + 0, sr + 0);
+      tmem_ld16x2_32<64>(tS + 32, sr + 32);
       tmem_wait_ld();
       reg_fence(sr, 64);
       const bool diag = diag_last && jb == n - 1;
       if (diag) {  // causal diagonal tile: key c is allowed for query row r iff c <= r
 #pragma unroll
-        for (int c = 0; c < 64; ++c) sr[c] = (h * 64 + c > r) ? kNegInf : sr[c];
+        for (int c = 0; c < 64; ++c) sr[c] = (ch * 64 + c > r) ? kNegInf : sr[c];
       }
       float mx = row_max64(sr);
-      bars->xmax[s][par][h][r] = mx;
-      if (!exchange()) return;
-      mx = fmaxf(mx, bars->xmax[s][par][h ^ 1][r]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
       const float xm = mx * sl;
       const bool need = xm > m + kTau;  // always true on the first block (m = -inf)
       float f = 1.f;
@@ -494,20 +484,20 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       uint32_t pr[32];
       if (diag) softmax_exp64<false>(sr, pr, sl, -m, a32, ar);
       else softmax_exp64<true>(sr, pr, sl, -m, a32, ar);
-      tmem_st32(tS, pr);
+      tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
 
-      // O rescale (this half's columns) when a row's max moved; PV(jb-1) is
+      // O rescale (this thread's columns) when a row's max moved; PV(jb-1) is
       // complete because S(jb) was committed after it.
       if (jb > 0 && __any_sync(0xffffffffu, need)) {
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
           uint32_t orr[32];
-          tmem_ld32(tO + c0, orr);
+          tmem_ld16x2_32<DH>(tO + c0, orr);
           tmem_wait_ld();
           reg_fence(orr, 32);
 #pragma unroll
           for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
-          tmem_st32(tO + c0, orr);
+          tmem_st16x2_32<DH>(tO + c0, orr);
         }
       }
       tmem_wait_st();
@@ -520,24 +510,21 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       return;
     ++o_cnt;
     tc_fence_after();
-    const float my_l = ar[0] + ar[1];
-    const float my_l32 = a32[0] + a32[1];
-    bars->xsum[s][h][r] = make_float2(my_l, my_l32);
-    if (!exchange()) return;
-    const float2 other = bars->xsum[s][h ^ 1][r];
-    const float l = my_l + other.x;
-    const float l32 = my_l32 + other.y;
+    float l = ar[0] + ar[1];
+    float l32 = a32[0] + a32[1];
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    l32 += __shfl_xor_sync(0xffffffffu, l32, 16);
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
     const float inv_l = 1.0f / l;
-    if (h == 0) p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
+    if (ch == 0) p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
 #pragma unroll
     for (int c0 = 0; c0 < DH; c0 += 32) {
       uint32_t orr[32];
-      tmem_ld32(tO + c0, orr);
+      tmem_ld16x2_32<DH>(tO + c0, orr);
       tmem_wait_ld();
       reg_fence(orr, 32);
       if constexpr (OUT_F32) {
-        float* dst = reinterpret_cast<float*>(p.out) + row * D + h * DH + c0;
+        float* dst = reinterpret_cast<float*>(p.out) + row * D + ch * DH + c0;
 #pragma unroll
         for (int i = 0; i < 32; i += 4)
           st_global_v4(dst + i, __float_as_uint(__uint_as_float(orr[i]) * inv_l),
@@ -545,7 +532,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                        __float_as_uint(__uint_as_float(orr[i + 2]) * inv_l),
                        __float_as_uint(__uint_as_float(orr[i + 3]) * inv_l));
       } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + h * DH + c0;
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + ch * DH + c0;
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
@@ -585,7 +572,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->q_full[sl]), 1);
       mbar_init(smem_u32(&bars->q_empty[sl]), 1);
       mbar_init(smem_u32(&bars->p_full[sl]), kSoftmaxThreads / 2);
-      mbar_init(smem_u32(&bars->xchg[sl]), kSoftmaxThreads / 2);
       mbar_init(smem_u32(&bars->o_full[sl]), 1);
       mbar_init(smem_u32(&bars->drain[sl]), 1);
       for (int e = 0; e < 2; ++e) {
