@@ -19,11 +19,11 @@
 //               so the two halves of a row meet in one warp (shuffles)
 //   warps 8-15  the same for query slot 1
 //   warp  16/19 TMA producer and tile scheduler of slot 0 / slot 1
-//   warp  17/18 tcgen05 MMA issuer of slot 0 / slot 1 (warp 17 owns TMEM)
+//   warp  17    tensor-memory owner (alloc/free); warp 18 idle
+// The first softmax warp of each slot (warps 0 and 8) also issues that
+// slot's tcgen05 MMAs from an elected lane, right after the slot's P is in.
 // Each slot is an independent pipeline with its own Q, K and V buffers in
-// shared memory, so one slot's MMA warp can feed the tensor core while the
-// other waits for its softmax or its data (tcgen05.mma issue is close to
-// synchronous: the hardware queue holds only a few instructions).
+// shared memory.
 // Two query tiles are in flight per CTA so the tensor core works on one slot
 // while the other slot's softmax runs.  Tensor memory (512 columns):
 //   S0 = [0,128), S1 = [128,256): fp32 scores, overwritten in place by the
@@ -61,8 +61,7 @@ namespace {
 constexpr int kThreads = 640;
 constexpr int kSoftmaxThreads = 512;
 constexpr int kWarpLoad0 = 16;
-constexpr int kWarpMma0 = 17;
-constexpr int kWarpMma1 = 18;
+constexpr int kWarpTmem = 17;  // allocates and frees tensor memory
 constexpr int kWarpLoad1 = 19;
 // Launch budget 640 x 96 registers; the producer/MMA warpgroup gives part of
 // its share to the four softmax warpgroups: 512 x 104 + 128 x 64 = 640 x 96.
@@ -246,35 +245,31 @@ __device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* 
 }
 
 // ---------------------------------------------------------------------------
-// MMA warp of slot s: tcgen05 issue from one elected lane
+// MMA issue for slot s, done by the slot's first softmax warp (elected lane)
 // ---------------------------------------------------------------------------
+// Per tile with n live key blocks:  S(0) at tile start; after P(j) is in
+// TMEM: O (+)= P(j) V(j) and, for j < n-1, S(j+1).  The commit after S(j)
+// frees K(j)'s buffer and is the softmax's "S(j) ready" signal; the commit
+// after the last PV is "O ready".  Issuing from the softmax warpgroup that
+// produced P removes a cross-warp handoff per block.
 template <int D>
-__device__ void run_mma(int s, const FwdParams& p, Bars* bars, uint32_t tmem,
-                        uint32_t smem_base, volatile int* abort_flag) {
+struct MmaIssuer {
   using C = Cfg<D>;
-  const uint64_t lim = p.timeout_ns;
-  int kc = 0, vc = 0, qc = 0, pc = 0, tqc = 0;
-  bool ok = true;
-  const uint32_t qaddr = smem_base + C::kQOff + s * C::kTileBytes;
-  const uint32_t tS = tmem + s * 128;
-  const uint32_t tO = tmem + 256 + s * 128;
-  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
-  // swizzle row; a new 64-column box every 4 steps).  A negative scale is
-  // applied as -Q (instruction-descriptor negate bit) so the softmax always
-  // sees a non-negative multiplier.
-  const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
+  int s;
+  Bars* bars;
+  uint32_t tmem, smem_base;
+  uint32_t idesc_s;
+  int kc = 0, vc = 0, qc = 0;
 
-  auto commit = [&](uint32_t bar) {
+  __device__ void commit(uint32_t bar) {
     if (elect_one()) mma_commit(bar);
     __syncwarp();
-  };
-  // issue S(j) from the next K buffer; its commit frees the buffer and tells
-  // the softmax that S(j) is ready
-  auto do_s = [&]() -> bool {
+  }
+  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
+  // swizzle row; a new 64-column box every 4 steps).
+  __device__ void issue_s() {
     const int st = kc % C::kKStages;
-    if (!wait_warp(smem_u32(&bars->k_full[s][st]), (uint32_t)(kc / C::kKStages) & 1u,
-                   abort_flag, p.status, lim))
-      return false;
+    const uint32_t qaddr = smem_base + C::kQOff + s * C::kTileBytes;
     const uint32_t kaddr = smem_base + C::kKOff + (s * C::kKStages + st) * C::kTileBytes;
     if (elect_one()) {
       // descriptors advance by adding the byte offset >> 4 to the start-address field
@@ -283,73 +278,44 @@ __device__ void run_mma(int s, const FwdParams& p, Bars* bars, uint32_t tmem,
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tS, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + s * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars->k_empty[s][st]));
     }
     __syncwarp();
     ++kc;
-    return true;
-  };
+  }
   // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P is read from TMEM
   // (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31, keys
   // 64..127 at columns 64..95); V is MN-major (D contiguous): 8-key groups
   // 1024 bytes apart, 64-column boxes 16 KB apart.
-  auto do_pv = [&](bool accumulate) -> bool {
-    if (!wait_warp(smem_u32(&bars->p_full[s]), (uint32_t)pc & 1u, abort_flag, p.status, lim))
-      return false;
-    ++pc;
+  __device__ void issue_pv(bool accumulate) {
     const int st = vc % C::kVStages;
-    if (!wait_warp(smem_u32(&bars->v_full[s][st]), (uint32_t)(vc / C::kVStages) & 1u,
-                   abort_flag, p.status, lim))
-      return false;
-    tc_fence_after();
     const uint32_t vaddr = smem_base + C::kVOff + (s * C::kVStages + st) * C::kTileBytes;
     if (elect_one()) {
       const uint64_t vd = smem_desc_sw128(vaddr, C::kBoxBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
-        mma_ts(tO, tS + pcol, vd + (uint32_t)(kk * 2048 >> 4), C::kIdescO,
-               (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts(tmem + 256 + s * 128, tmem + s * 128 + pcol, vd + (uint32_t)(kk * 2048 >> 4),
+               C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars->v_empty[s][st]));
     }
     __syncwarp();
     ++vc;
-    return true;
-  };
-
-  while (ok) {
-    const int e = tqc & 1;
-    if (!wait_warp(smem_u32(&bars->tq_full[s][e]), (uint32_t)(tqc >> 1) & 1u, abort_flag,
-                   p.status, lim))
-      break;
-    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
-    const int t = slot[0];
-    const int n = slot[2];
-    if (elect_one()) mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
-    __syncwarp();
-    ++tqc;
-    if (t < 0) break;
-    if (!wait_warp(smem_u32(&bars->q_full[s]), (uint32_t)qc & 1u, abort_flag, p.status, lim))
-      break;
-    ++qc;
-    tc_fence_after();
-    ok = do_s();
-    if (ok && n == 1) commit(smem_u32(&bars->q_empty[s]));
-    for (int j = 1; ok && j < n; ++j) {
-      ok = do_pv(j > 1);
-      if (ok) ok = do_s();
-      if (ok && j == n - 1) commit(smem_u32(&bars->q_empty[s]));
-    }
-    if (ok) ok = do_pv(n > 1);
-    if (ok) commit(smem_u32(&bars->o_full[s]));
   }
-  // Every MMA issued so far must finish before TMEM is released.
-  commit(smem_u32(&bars->drain[s]));
-  wait_drain(smem_u32(&bars->drain[s]), 0);
-}
+  __device__ bool wait_k(volatile int* abort_flag, int* status, uint64_t lim) {
+    const int st = kc % C::kKStages;
+    return wait_warp(smem_u32(&bars->k_full[s][st]), (uint32_t)(kc / C::kKStages) & 1u,
+                     abort_flag, status, lim);
+  }
+  __device__ bool wait_v(volatile int* abort_flag, int* status, uint64_t lim) {
+    const int st = vc % C::kVStages;
+    return wait_warp(smem_u32(&bars->v_full[s][st]), (uint32_t)(vc / C::kVStages) & 1u,
+                     abort_flag, status, lim);
+  }
+};
 
 // ---------------------------------------------------------------------------
 // warps 0-7: softmax + epilogue (one thread per query row of the slot)
@@ -410,7 +376,7 @@ __device__ __forceinline__ float row_max64(const uint32_t* sr) {
 }
 
 template <int D, bool OUT_F32>
-__device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
+__device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
                             volatile int* abort_flag) {
   constexpr int DH = D / 2;            // O columns owned by this thread
   const int warp = threadIdx.x >> 5;
@@ -431,7 +397,13 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
 
   write_empty_tiles<D, OUT_F32>(p);
 
-  int tq_cnt = 0, s_cnt = 0, o_cnt = 0;
+  // The first warp of the slot issues the slot's MMAs.  A negative scale is
+  // applied as -Q (instruction-descriptor negate bit) so the softmax always
+  // sees a non-negative multiplier.
+  const bool issuer = (warp & 7) == 0;
+  MmaIssuer<D> mma{s, bars, tmem, smem_base,
+                   Cfg<D>::kIdescS | (p.neg_scale ? (1u << 13) : 0u)};
+  int tq_cnt = 0, s_cnt = 0, o_cnt = 0, p_cnt = 0;
   for (;;) {
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
@@ -445,6 +417,14 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     if (t < 0) return;
     const int bh = t / p.nb;
     const int qb = t - bh * p.nb;
+    if (issuer) {  // S(0) once Q and K(0) are in
+      if (!wait_warp(smem_u32(&bars->q_full[s]), (uint32_t)mma.qc & 1u, abort_flag, p.status, lim) ||
+          !mma.wait_k(abort_flag, p.status, lim))
+        return;
+      ++mma.qc;
+      mma.issue_s();
+      if (n == 1) mma.commit(smem_u32(&bars->q_empty[s]));
+    }
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
     float a32[2] = {0.f, 0.f}, ar[2] = {0.f, 0.f};  // unrounded (LSE) / rounded (O) partial sums
@@ -503,6 +483,22 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars->p_full[s]));
+      if (issuer) {  // once all 256 threads wrote P(jb): PV(jb), then S(jb+1)
+        if (!wait_warp(smem_u32(&bars->p_full[s]), (uint32_t)p_cnt & 1u, abort_flag, p.status,
+                       lim) ||
+            !mma.wait_v(abort_flag, p.status, lim))
+          return;
+        ++p_cnt;
+        tc_fence_after();
+        mma.issue_pv(jb > 0);
+        if (jb + 1 < n) {
+          if (!mma.wait_k(abort_flag, p.status, lim)) return;
+          mma.issue_s();
+          if (jb + 1 == n - 1) mma.commit(smem_u32(&bars->q_empty[s]));
+        } else {
+          mma.commit(smem_u32(&bars->o_full[s]));
+        }
+      }
     }
 
     // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
@@ -576,13 +572,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->drain[sl]), 1);
       for (int e = 0; e < 2; ++e) {
         mbar_init(smem_u32(&bars->tq_full[sl][e]), 1);
-        mbar_init(smem_u32(&bars->tq_empty[sl][e]), 1 + kSoftmaxThreads / 2);
+        mbar_init(smem_u32(&bars->tq_empty[sl][e]), kSoftmaxThreads / 2);
       }
     }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma0) {
+  if (warp == kWarpTmem) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
@@ -601,17 +597,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsOther>();
     if (warp == kWarpLoad0 || warp == kWarpLoad1)
       run_producer<D>(warp == kWarpLoad0 ? 0 : 1, &tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
-    else
-      run_mma<D>(warp == kWarpMma0 ? 0 : 1, p, bars, tmem, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);
+    run_softmax<D, OUT_F32>(p, bars, tmem, base, abort_flag);
+    if ((warp & 7) == 0) {  // the slot's MMA issuer: its MMAs finish before TMEM is freed
+      const int sl = warp >> 3;
+      if (elect_one()) mma_commit(smem_u32(&bars->drain[sl]));
+      __syncwarp();
+      wait_drain(smem_u32(&bars->drain[sl]), 0);
+    }
   }
   __syncwarp();  // reconverge each warp before the CTA-wide barrier
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma0) {
+  if (warp == kWarpTmem) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
