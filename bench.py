@@ -47,10 +47,10 @@ FALLBACK_BF16_TFLOPS = 1900.0   # profiling recipe's fallback (GB300, burst)
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
 
-# DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum),
-# from the ncu capture summarised under profiles/; None until captured for the
-# current kernel.
-TRAFFIC_BYTES = {}
+# DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
+# of the current forward kernel, from the ncu capture summarised in
+# profiles/bsattn_fwd_kernel-causal-s4096-d128.md; workloads not captured: None.
+TRAFFIC_BYTES = {"w2_bf16": 201_620_736 + 49_830_912}
 
 
 def parse_args(argv=None):
