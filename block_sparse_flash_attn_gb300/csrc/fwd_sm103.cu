@@ -11,40 +11,35 @@
 // Dead key blocks are never loaded (the mask's purpose in "Writing the Kernel
 // Logic": only the small 128x128 block is ever materialised).
 //
-// GB300 design (one persistent CTA per SM, 640 threads = 5 warpgroups):
-//   warps 0-7   softmax + epilogue for query slot 0: each warp covers 16
-//               query rows (TMEM lanes); lanes 0..15 of the warp own key
-//               columns 0..63 of every block (O columns [0, D/2)), lanes
-//               16..31 the same rows' columns 64..127 (O columns [D/2, D)),
-//               so the two halves of a row meet in one warp (shuffles)
-//   warps 8-15  the same for query slot 1
-//   warp  16/19 TMA producer and tile scheduler of slot 0 / slot 1
-//   warp  17    tensor-memory owner (alloc/free); warp 18 idle
-// The first softmax warp of each slot (warps 0 and 8) also issues that
-// slot's tcgen05 MMAs from an elected lane, right after the slot's P is in.
-// Each slot is an independent pipeline with its own Q, K and V buffers in
-// shared memory.
-// Two query tiles are in flight per CTA so the tensor core works on one slot
-// while the other slot's softmax runs.  Tensor memory (512 columns):
-//   S0 = [0,128), S1 = [128,256): fp32 scores, overwritten in place by the
-//   bf16 probabilities P: keys 0..63 in columns 0..31, keys 64..127 in
-//   columns 64..95 of the slot's S region (each half writes only over
-//   scores it has already read);
-//   O0 = [256,384), O1 = [384,512): fp32 output accumulators.
-// Shared memory per slot: Q tile, a ring of K tiles and a ring of V tiles
-// (each 128 x D bf16, 128-byte swizzled by TMA, read by tcgen05.mma through
-// matrix descriptors).
+// GB300 design (one persistent CTA per SM, 384 threads = 3 warpgroups, one
+// query tile in flight per CTA):
+//   warps 0-7  softmax + epilogue.  Each warp covers 16 query rows (TMEM
+//              lanes); lanes 0..15 own key columns 0..63 of every block (O
+//              columns [0, D/2)), lanes 16..31 the same rows' columns 64..127
+//              (O columns [D/2, D)); tcgen05 16x32bx2 accesses put both halves
+//              of a row in one warp, so row max and sums combine by shuffle.
+//   warp  8    tile scheduler + TMA producer (elected lane)
+//   warp  9    tcgen05 MMA issuer (elected lane) and tensor-memory owner
+//   warps 10-11 idle (complete warpgroup 2 for setmaxnreg)
+// Tensor memory (512 columns allocated): two score buffers S[0] = [0,128),
+// S[1] = [128,256) and the fp32 output accumulator O = [256, 256+D).  Block g
+// (counted over the CTA's whole run) uses S[g % 2]; its bf16 probabilities P
+// overwrite the scores already read (keys 0..63 -> columns 0..31, keys
+// 64..127 -> columns 64..95).  With two score buffers the MMA warp computes
+// S(j+1) while the softmax works on block j, and issues S(j+2) into block j's
+// buffer right after O += P(j) V(j), so neither side waits for the other in
+// steady state.  Shared memory: Q, a 2-stage ring of K tiles and a 2-stage
+// ring of V tiles (128 x D bf16 each, 128-byte swizzled by TMA, read by
+// tcgen05.mma through matrix descriptors).
 //
-// Per slot and tile with n live key blocks the slot's MMA warp runs
-//   S(0); then for j = 1..n-1: [wait P(j-1)] O += P(j-1) V(j-1); S(j);
-//   finally [wait P(n-1)] O += P(n-1) V(n-1); signal O ready.
-// The commit after S(j) frees K(j)'s buffer and is also the softmax's "S(j)
-// ready" signal.  Because tcgen05 ops of one thread complete in order,
-// "S(j) done" also means "PV(j-1) done", so the softmax may rescale O right
-// after seeing S(j).
-// Online softmax in base 2 with lazy rescale: the running max m only moves
-// when a block's max exceeds it by more than 8 (log2 units), so P <= 256 and
-// the O rescale (a TMEM round trip) is rare after the first block.
+// Per tile with n live key blocks the MMA warp issues
+//   S(0), S(1); then for j = 0..n-1: [P(j) in] O (+)= P(j) V(j); S(j+2).
+// The commit after S(g) frees K(g)'s ring stage and is the softmax's "S(g)
+// ready" signal; the commit after PV(g) frees V(g)'s stage and is "PV(g)
+// done", which the softmax waits for only before an O rescale and, for the
+// tile's last block, before the epilogue.  Online softmax in base 2 with lazy
+// rescale: the running max m only moves when a block's max exceeds it by more
+// than 8 (log2 units), so P <= 256 and the O rescale is rare.
 //
 // Every wait is bounded (globaltimer); on expiry the kernel records a timeout
 // in the status word, every role leaves its loop, outstanding TMA loads and
@@ -58,22 +53,15 @@
 namespace bsattn {
 namespace {
 
-constexpr int kThreads = 640;
-constexpr int kSoftmaxThreads = 512;
-constexpr int kWarpLoad0 = 16;
-constexpr int kWarpTmem = 17;  // allocates and frees tensor memory
-constexpr int kWarpLoad1 = 19;
-// Launch budget 640 x 96 registers; the producer/MMA warpgroup gives part of
-// its share to the four softmax warpgroups: 512 x 104 + 128 x 64 = 640 x 96.
-constexpr int kRegsSoftmax = 104;
-constexpr int kRegsOther = 64;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kWarpLoad = 8;
+constexpr int kWarpMma = 9;
+// Launch budget 384 x 168 registers; the producer/MMA warpgroup hands part of
+// its share to the two softmax warpgroups: 256 x 208 + 128 x 88 = 384 x 168.
+constexpr int kRegsSoftmax = 208;
+constexpr int kRegsOther = 88;
 constexpr float kTau = 8.0f;
-// Every kPolyEvery-th pair of probabilities in a block without causal masking
-// is computed by the FMA-pipe polynomial instead of the MUFU ex2 (0 = never).
-#ifndef BSATTN_POLY_EVERY
-#define BSATTN_POLY_EVERY 0
-#endif
-constexpr int kPolyEvery = BSATTN_POLY_EVERY;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 200ull * 1000 * 1000;
 
@@ -82,18 +70,17 @@ struct Cfg {
   static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
   static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
-  static constexpr int kKStages = (D == 128) ? 1 : 2;  // K buffers per slot
-  static constexpr int kVStages = (D == 128) ? 1 : 2;  // V buffers per slot
-  static constexpr int kQOff = 0;                                    // Q[slot]
-  static constexpr int kKOff = 2 * kTileBytes;                       // K[slot][stage]
-  static constexpr int kVOff = kKOff + 2 * kKStages * kTileBytes;    // V[slot][stage]
-  static constexpr int kBarOff = kVOff + 2 * kVStages * kTileBytes;
+  static constexpr int kStages = 2;                  // K ring and V ring depth
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
   static constexpr int kSmem = kBarOff + 1024;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, true);
 };
 
-// One scheduled tile as the producer publishes it to the MMA and softmax roles.
+// One scheduled tile as the producer publishes it to the MMA and softmax warps.
 struct TileInfo {
   int t;     // tile id (b*H + h)*nb + qb, or -1 when no tiles are left
   int r0;    // first CSR entry of the tile
@@ -102,18 +89,17 @@ struct TileInfo {
 };
 
 struct __align__(16) Bars {
-  uint64_t k_full[2][2];   // [slot][stage]
-  uint64_t k_empty[2][2];  // completes when S(j) is done: K(j) free, S(j) ready
-  uint64_t v_full[2][2];
-  uint64_t v_empty[2][2];
-  uint64_t q_full[2];
-  uint64_t q_empty[2];
-  uint64_t p_full[2];
-  uint64_t o_full[2];
-  uint64_t tq_full[2][2];
-  uint64_t tq_empty[2][2];
-  uint64_t drain[2];
-  TileInfo tq[2][2];
+  uint64_t k_full[2];   // K ring stage loaded
+  uint64_t k_empty[2];  // S(g) complete: K stage free, S(g) ready for the softmax
+  uint64_t v_full[2];   // V ring stage loaded
+  uint64_t v_empty[2];  // PV(g) complete: V stage free, O holds block g
+  uint64_t q_full;
+  uint64_t q_empty;     // the tile's last S complete: Q buffer free
+  uint64_t p_full[2];   // all softmax threads wrote P(g) (indexed by g % 2)
+  uint64_t tq_full[2];
+  uint64_t tq_empty[2];
+  uint64_t drain;
+  TileInfo tq[2];
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -131,9 +117,9 @@ __device__ __forceinline__ void raise_internal(volatile int* abort_flag, int* st
 }
 
 // Every role runs with its whole warp converged (warp-collective tcgen05.ld/st
-// in the softmax; uniform bookkeeping in the producer and MMA roles, which
-// issue their single-thread instructions from an elected lane), so every
-// lane must take the same path after a wait: the outcome is made uniform.
+// in the softmax; uniform bookkeeping in the producer and MMA warps, which
+// issue their single-thread instructions from an elected lane), so every lane
+// must take the same path after a wait: the outcome is made uniform.
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, uint64_t limit_ns) {
   const bool ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
@@ -141,10 +127,12 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------------------
-// producer warp of slot s: tile scheduler + TMA loads
+// warp 8: tile scheduler + TMA producer
 // ---------------------------------------------------------------------------
+// Load order per tile (matching the MMA warp's consumption order within each
+// ring): Q, K(0), K(1), then for j = 0..n-1: V(j), K(j+2).
 template <int D>
-__device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+__device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, Bars* bars,
                              uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D>;
@@ -170,11 +158,11 @@ __device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* 
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int st = kc % C::kKStages;
-    const uint32_t ph = ((uint32_t)(kc / C::kKStages) & 1u) ^ 1u;
+    const int st = kc % C::kStages;
+    const uint32_t ph = ((uint32_t)(kc / C::kStages) & 1u) ^ 1u;
     ++kc;
-    return load_tile(tm_k, smem_base + C::kKOff + (s * C::kKStages + st) * C::kTileBytes,
-                     smem_u32(&bars->k_full[s][st]), smem_u32(&bars->k_empty[s][st]), ph,
+    return load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes,
+                     smem_u32(&bars->k_full[st]), smem_u32(&bars->k_empty[st]), ph,
                      hrow + kb * kBlock);
   };
   auto load_v = [&](int kb, int hrow) -> bool {
@@ -182,19 +170,19 @@ __device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* 
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int st = vc % C::kVStages;
-    const uint32_t ph = ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u;
+    const int st = vc % C::kStages;
+    const uint32_t ph = ((uint32_t)(vc / C::kStages) & 1u) ^ 1u;
     ++vc;
-    return load_tile(tm_v, smem_base + C::kVOff + (s * C::kVStages + st) * C::kTileBytes,
-                     smem_u32(&bars->v_full[s][st]), smem_u32(&bars->v_empty[s][st]), ph,
+    return load_tile(tm_v, smem_base + C::kVOff + st * C::kTileBytes,
+                     smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]), ph,
                      hrow + kb * kBlock);
   };
 
   while (ok) {
-    // claim a tile and publish it to this slot's MMA and softmax warps
+    // claim a tile and publish it to the MMA and softmax warps
     const int e = tqc & 1;
     const uint32_t ph = (uint32_t)(tqc >> 1) & 1u;
-    if (!wait_warp(smem_u32(&bars->tq_empty[s][e]), ph ^ 1u, abort_flag, p.status, lim)) break;
+    if (!wait_warp(smem_u32(&bars->tq_empty[e]), ph ^ 1u, abort_flag, p.status, lim)) break;
     int idx = 0;
     if (elect_one()) idx = atomicAdd(p.counter, 1);
     idx = __reduce_max_sync(0xffffffffu, idx);  // the elected lane's claim, to every lane
@@ -212,65 +200,66 @@ __device__ void run_producer(int s, const CUtensorMap* tm_q, const CUtensorMap* 
       diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
     }
     if (elect_one()) {
-      volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[s][e]);
+      volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[e]);
       slot[0] = t;
       slot[1] = r0;
       slot[2] = cnt;
       slot[3] = diag;
-      mbar_arrive(smem_u32(&bars->tq_full[s][e]));
+      mbar_arrive(smem_u32(&bars->tq_full[e]));
     }
     __syncwarp();
     ++tqc;
     if (t < 0) break;
     const int hrow = bh * p.S;
     // Q, once its buffer is free (the previous tile's last S is done)
-    ok = load_tile(tm_q, smem_base + C::kQOff + s * C::kTileBytes, smem_u32(&bars->q_full[s]),
-                   smem_u32(&bars->q_empty[s]), ((uint32_t)qc & 1u) ^ 1u, hrow + qb * kBlock);
+    ok = load_tile(tm_q, smem_base + C::kQOff, smem_u32(&bars->q_full),
+                   smem_u32(&bars->q_empty), ((uint32_t)qc & 1u) ^ 1u, hrow + qb * kBlock);
     ++qc;
     if (ok) ok = load_k(p.col_idx[r0], hrow);
-    for (int j = 1; ok && j < cnt; ++j) {
-      ok = load_v(p.col_idx[r0 + j - 1], hrow);  // V(j-1) frees up before K(j)
-      if (ok) ok = load_k(p.col_idx[r0 + j], hrow);
+    if (ok && cnt > 1) ok = load_k(p.col_idx[r0 + 1], hrow);
+    for (int j = 0; ok && j < cnt; ++j) {
+      ok = load_v(p.col_idx[r0 + j], hrow);
+      if (ok && j + 2 < cnt) ok = load_k(p.col_idx[r0 + j + 2], hrow);
     }
-    if (ok) ok = load_v(p.col_idx[r0 + cnt - 1], hrow);
   }
   if (!ok) {
     // Let every TMA load this warp issued land before the CTA exits.
-    for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
-      wait_drain(smem_u32(&bars->k_full[s][i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
-    for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
-      wait_drain(smem_u32(&bars->v_full[s][i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
-    if (qc > 0) wait_drain(smem_u32(&bars->q_full[s]), (uint32_t)(qc - 1) & 1u);
+    for (int i = (kc > C::kStages ? kc - C::kStages : 0); i < kc; ++i)
+      wait_drain(smem_u32(&bars->k_full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u);
+    for (int i = (vc > C::kStages ? vc - C::kStages : 0); i < vc; ++i)
+      wait_drain(smem_u32(&bars->v_full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u);
+    if (qc > 0) wait_drain(smem_u32(&bars->q_full), (uint32_t)(qc - 1) & 1u);
   }
 }
 
 // ---------------------------------------------------------------------------
-// MMA issue for slot s, done by the slot's first softmax warp (elected lane)
+// warp 9: tcgen05 MMA issue (elected lane)
 // ---------------------------------------------------------------------------
-// Per tile with n live key blocks:  S(0) at tile start; after P(j) is in
-// TMEM: O (+)= P(j) V(j) and, for j < n-1, S(j+1).  The commit after S(j)
-// frees K(j)'s buffer and is the softmax's "S(j) ready" signal; the commit
-// after the last PV is "O ready".  Issuing from the softmax warpgroup that
-// produced P removes a cross-warp handoff per block.
 template <int D>
-struct MmaIssuer {
+__device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
+                        volatile int* abort_flag) {
   using C = Cfg<D>;
-  int s;
-  Bars* bars;
-  uint32_t tmem, smem_base;
-  uint32_t idesc_s;
-  int kc = 0, vc = 0, qc = 0;
+  const uint64_t lim = p.timeout_ns;
+  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
+  // swizzle row; a new 64-column box every 4 steps).  A negative scale is
+  // applied as -Q (instruction-descriptor negate bit) so the softmax always
+  // sees a non-negative multiplier.
+  const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
+  const uint32_t qaddr = smem_base + C::kQOff;
+  int kc = 0, vc = 0, qc = 0, tqc = 0;
 
-  __device__ void commit(uint32_t bar) {
+  auto commit = [&](uint32_t bar) {
     if (elect_one()) mma_commit(bar);
     __syncwarp();
-  }
-  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
-  // swizzle row; a new 64-column box every 4 steps).
-  __device__ void issue_s() {
-    const int st = kc % C::kKStages;
-    const uint32_t qaddr = smem_base + C::kQOff + s * C::kTileBytes;
-    const uint32_t kaddr = smem_base + C::kKOff + (s * C::kKStages + st) * C::kTileBytes;
+  };
+  // S(g) into S[g % 2] from K ring stage g % 2; its commit frees the stage and
+  // tells the softmax that S(g) is ready.
+  auto do_s = [&]() -> bool {
+    const int st = kc % C::kStages;
+    if (!wait_warp(smem_u32(&bars->k_full[st]), (uint32_t)(kc / C::kStages) & 1u, abort_flag,
+                   p.status, lim))
+      return false;
+    const uint32_t kaddr = smem_base + C::kKOff + st * C::kTileBytes;
     if (elect_one()) {
       // descriptors advance by adding the byte offset >> 4 to the start-address field
       const uint64_t qd = smem_desc_sw128(qaddr, 16, 1024);
@@ -278,47 +267,79 @@ struct MmaIssuer {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + s * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + st * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bars->k_empty[s][st]));
+      mma_commit(smem_u32(&bars->k_empty[st]));
     }
     __syncwarp();
     ++kc;
-  }
-  // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P is read from TMEM
-  // (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31, keys
-  // 64..127 at columns 64..95); V is MN-major (D contiguous): 8-key groups
-  // 1024 bytes apart, 64-column boxes 16 KB apart.
-  __device__ void issue_pv(bool accumulate) {
-    const int st = vc % C::kVStages;
-    const uint32_t vaddr = smem_base + C::kVOff + (s * C::kVStages + st) * C::kTileBytes;
+    return true;
+  };
+  // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P(g) is read from
+  // S[g % 2] (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31,
+  // keys 64..127 at columns 64..95); V is MN-major (D contiguous): 8-key
+  // groups 1024 bytes apart, 64-column boxes 16 KB apart.
+  auto do_pv = [&](bool accumulate) -> bool {
+    // P(g) in, g = vc: two barriers so that P(g+1) can never be mistaken for P(g)
+    if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
+                   p.status, lim))
+      return false;
+    const int st = vc % C::kStages;
+    if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kStages) & 1u, abort_flag,
+                   p.status, lim))
+      return false;
+    tc_fence_after();
+    const uint32_t vaddr = smem_base + C::kVOff + st * C::kTileBytes;
+    const uint32_t pbuf = tmem + (vc % 2) * 128;  // block g's score buffer (g = vc)
     if (elect_one()) {
       const uint64_t vd = smem_desc_sw128(vaddr, C::kBoxBytes, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
-        mma_ts(tmem + 256 + s * 128, tmem + s * 128 + pcol, vd + (uint32_t)(kk * 2048 >> 4),
-               C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+        mma_ts(tmem + 256, pbuf + pcol, vd + (uint32_t)(kk * 2048 >> 4), C::kIdescO,
+               (accumulate || kk > 0) ? 1u : 0u);
       }
-      mma_commit(smem_u32(&bars->v_empty[s][st]));
+      mma_commit(smem_u32(&bars->v_empty[st]));
     }
     __syncwarp();
     ++vc;
+    return true;
+  };
+
+  bool ok = true;
+  while (ok) {
+    const int e = tqc & 1;
+    if (!wait_warp(smem_u32(&bars->tq_full[e]), (uint32_t)(tqc >> 1) & 1u, abort_flag, p.status,
+                   lim))
+      break;
+    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[e]);
+    const int t = slot[0];
+    const int n = slot[2];
+    if (elect_one()) mbar_arrive(smem_u32(&bars->tq_empty[e]));
+    __syncwarp();
+    ++tqc;
+    if (t < 0) break;
+    if (!wait_warp(smem_u32(&bars->q_full), (uint32_t)qc & 1u, abort_flag, p.status, lim)) break;
+    ++qc;
+    // S(0), S(1)
+    ok = do_s();
+    if (ok && n > 1) ok = do_s();
+    if (ok && n <= 2) commit(smem_u32(&bars->q_empty));
+    for (int j = 0; ok && j < n; ++j) {
+      ok = do_pv(j > 0);
+      if (ok && j + 2 < n) {
+        ok = do_s();
+        if (ok && j + 2 == n - 1) commit(smem_u32(&bars->q_empty));
+      }
+    }
   }
-  __device__ bool wait_k(volatile int* abort_flag, int* status, uint64_t lim) {
-    const int st = kc % C::kKStages;
-    return wait_warp(smem_u32(&bars->k_full[s][st]), (uint32_t)(kc / C::kKStages) & 1u,
-                     abort_flag, status, lim);
-  }
-  __device__ bool wait_v(volatile int* abort_flag, int* status, uint64_t lim) {
-    const int st = vc % C::kVStages;
-    return wait_warp(smem_u32(&bars->v_full[s][st]), (uint32_t)(vc / C::kVStages) & 1u,
-                     abort_flag, status, lim);
-  }
-};
+  // Every MMA issued so far must finish before TMEM is released.
+  commit(smem_u32(&bars->drain));
+  wait_drain(smem_u32(&bars->drain), 0);
+}
 
 // ---------------------------------------------------------------------------
-// warps 0-7: softmax + epilogue (one thread per query row of the slot)
+// warps 0-7: softmax + epilogue
 // ---------------------------------------------------------------------------
 template <int D, bool OUT_F32>
 __device__ void write_empty_tiles(const FwdParams& p) {
@@ -340,20 +361,14 @@ __device__ void write_empty_tiles(const FwdParams& p) {
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
 // pairs into pr[]; accumulates the unrounded (a32, for LSE) and the rounded
 // (ar, the O denominator) row sums in two independent accumulators each.
-template <bool POLY>
 __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
                                               float nm, float (&a32)[2], float (&ar)[2]) {
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     float x0, x1;
     fma2(x0, x1, __uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1]), sl, sl, nm, nm);
-    float p0, p1;
-    if (POLY && kPolyEvery > 0 && (q % (kPolyEvery > 0 ? kPolyEvery : 1)) == kPolyEvery - 1) {
-      exp2_poly2(p0, p1, x0, x1);
-    } else {
-      p0 = ex2_approx(x0);
-      p1 = ex2_approx(x1);
-    }
+    const float p0 = ex2_approx(x0);
+    const float p1 = ex2_approx(x1);
     const uint32_t pk = pack_bf16x2(p0, p1);
     pr[q] = pk;
     add2(a32[0], a32[1], a32[0], a32[1], p0, p1);
@@ -376,12 +391,11 @@ __device__ __forceinline__ float row_max64(const uint32_t* sr) {
 }
 
 template <int D, bool OUT_F32>
-__device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
+__device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
   constexpr int DH = D / 2;            // O columns owned by this thread
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int s = warp >> 3;             // query slot
   const int sub = warp & 3;            // TMEM sub-partition: lanes 32*sub .. 32*sub+31
   const int lh = (warp >> 2) & 1;      // which 16 lanes of the sub-partition this warp covers
   const int ch = lane >> 4;            // column half: keys [64ch, 64ch+64), O cols [DH ch, DH ch+DH)
@@ -389,55 +403,38 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem, uint3
   // 16x32bx2 accesses: lanes 0..15 of the warp take the address's columns,
   // lanes 16..31 the same rows 64 (or DH) columns further on.
   const uint32_t lane_off = (uint32_t)(sub * 32 + lh * 16) << 16;
-  const uint32_t tS = tmem + s * 128 + lane_off;
-  const uint32_t tO = tmem + 256 + s * 128 + lane_off;
+  const uint32_t tO = tmem + 256 + lane_off;
   const float sl = p.scale_log2;       // > 0 (see FwdParams)
   const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
 
   write_empty_tiles<D, OUT_F32>(p);
 
-  // The first warp of the slot issues the slot's MMAs.  A negative scale is
-  // applied as -Q (instruction-descriptor negate bit) so the softmax always
-  // sees a non-negative multiplier.
-  const bool issuer = (warp & 7) == 0;
-  MmaIssuer<D> mma{s, bars, tmem, smem_base,
-                   Cfg<D>::kIdescS | (p.neg_scale ? (1u << 13) : 0u)};
-  int tq_cnt = 0, s_cnt = 0, o_cnt = 0, p_cnt = 0;
+  int tq_cnt = 0, g = 0;  // g: blocks processed by this CTA (selects S buffer / ring stages)
   for (;;) {
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
-    if (!wait_warp(smem_u32(&bars->tq_full[s][e]), ph, abort_flag, p.status, lim)) return;
-    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[s][e]);
+    if (!wait_warp(smem_u32(&bars->tq_full[e]), ph, abort_flag, p.status, lim)) return;
+    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[e]);
     const int t = slot[0];
     const int n = slot[2];
     const int diag_last = slot[3];
-    mbar_arrive(smem_u32(&bars->tq_empty[s][e]));
+    mbar_arrive(smem_u32(&bars->tq_empty[e]));
     ++tq_cnt;
     if (t < 0) return;
     const int bh = t / p.nb;
     const int qb = t - bh * p.nb;
-    if (issuer) {  // S(0) once Q and K(0) are in
-      if (!wait_warp(smem_u32(&bars->q_full[s]), (uint32_t)mma.qc & 1u, abort_flag, p.status, lim) ||
-          !mma.wait_k(abort_flag, p.status, lim))
-        return;
-      ++mma.qc;
-      mma.issue_s();
-      if (n == 1) mma.commit(smem_u32(&bars->q_empty[s]));
-    }
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
     float a32[2] = {0.f, 0.f}, ar[2] = {0.f, 0.f};  // unrounded (LSE) / rounded (O) partial sums
-    for (int jb = 0; jb < n; ++jb) {
-      // S(jb) ready = the slot's K buffer of this block was released by its S MMA
-      {
-        constexpr int NK = (D == 128) ? 1 : 2;  // Cfg<D>::kKStages
-        if (!wait_warp(smem_u32(&bars->k_empty[s][s_cnt % NK]), (uint32_t)(s_cnt / NK) & 1u,
-                       abort_flag, p.status, lim))
-          return;
-      }
-      ++s_cnt;
+    for (int jb = 0; jb < n; ++jb, ++g) {
+      const int b = g & 1;  // S buffer and ring stage of this block
+      // S(g) ready = its commit released K(g)'s stage
+      if (!wait_warp(smem_u32(&bars->k_empty[b]), (uint32_t)(g >> 1) & 1u, abort_flag, p.status,
+                     lim))
+        return;
       tc_fence_after();
+      const uint32_t tS = tmem + b * 128 + lane_off;
       uint32_t sr[64];
       tmem_ld16x2_32<64>(tS + 0, sr + 0);
       tmem_ld16x2_32<64>(tS + 32, sr + 32);
@@ -462,13 +459,16 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem, uint3
         ar[1] *= f;
       }
       uint32_t pr[32];
-      if (diag) softmax_exp64<false>(sr, pr, sl, -m, a32, ar);
-      else softmax_exp64<true>(sr, pr, sl, -m, a32, ar);
+      softmax_exp64(sr, pr, sl, -m, a32, ar);
       tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
 
-      // O rescale (this thread's columns) when a row's max moved; PV(jb-1) is
-      // complete because S(jb) was committed after it.
+      // O rescale (this thread's columns) when a row's max moved: first wait
+      // until PV(g-1) has landed in O (PV(g) is not issued before P(g)).
       if (jb > 0 && __any_sync(0xffffffffu, need)) {
+        if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u,
+                       abort_flag, p.status, lim))
+          return;
+        tc_fence_after();
 #pragma unroll
         for (int c0 = 0; c0 < DH; c0 += 32) {
           uint32_t orr[32];
@@ -482,29 +482,13 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem, uint3
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[s]));
-      if (issuer) {  // once all 256 threads wrote P(jb): PV(jb), then S(jb+1)
-        if (!wait_warp(smem_u32(&bars->p_full[s]), (uint32_t)p_cnt & 1u, abort_flag, p.status,
-                       lim) ||
-            !mma.wait_v(abort_flag, p.status, lim))
-          return;
-        ++p_cnt;
-        tc_fence_after();
-        mma.issue_pv(jb > 0);
-        if (jb + 1 < n) {
-          if (!mma.wait_k(abort_flag, p.status, lim)) return;
-          mma.issue_s();
-          if (jb + 1 == n - 1) mma.commit(smem_u32(&bars->q_empty[s]));
-        } else {
-          mma.commit(smem_u32(&bars->o_full[s]));
-        }
-      }
+      mbar_arrive(smem_u32(&bars->p_full[b]));
     }
 
     // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
-    if (!wait_warp(smem_u32(&bars->o_full[s]), (uint32_t)o_cnt & 1u, abort_flag, p.status, lim))
-      return;
-    ++o_cnt;
+    if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u,
+                   abort_flag, p.status, lim))
+      return;  // the tile's last PV has landed in O
     tc_fence_after();
     float l = ar[0] + ar[1];
     float l32 = a32[0] + a32[1];
@@ -556,33 +540,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int sl = 0; sl < 2; ++sl) {
-      for (int i = 0; i < C::kKStages; ++i) {
-        mbar_init(smem_u32(&bars->k_full[sl][i]), 1);
-        mbar_init(smem_u32(&bars->k_empty[sl][i]), 1);
-      }
-      for (int i = 0; i < C::kVStages; ++i) {
-        mbar_init(smem_u32(&bars->v_full[sl][i]), 1);
-        mbar_init(smem_u32(&bars->v_empty[sl][i]), 1);
-      }
-      mbar_init(smem_u32(&bars->q_full[sl]), 1);
-      mbar_init(smem_u32(&bars->q_empty[sl]), 1);
-      mbar_init(smem_u32(&bars->p_full[sl]), kSoftmaxThreads / 2);
-      mbar_init(smem_u32(&bars->o_full[sl]), 1);
-      mbar_init(smem_u32(&bars->drain[sl]), 1);
-      for (int e = 0; e < 2; ++e) {
-        mbar_init(smem_u32(&bars->tq_full[sl][e]), 1);
-        mbar_init(smem_u32(&bars->tq_empty[sl][e]), kSoftmaxThreads / 2);
-      }
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(smem_u32(&bars->k_full[i]), 1);
+      mbar_init(smem_u32(&bars->k_empty[i]), 1);
+      mbar_init(smem_u32(&bars->v_full[i]), 1);
+      mbar_init(smem_u32(&bars->v_empty[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q_empty), 1);
+    mbar_init(smem_u32(&bars->p_full[0]), kSoftmaxThreads);
+    mbar_init(smem_u32(&bars->p_full[1]), kSoftmaxThreads);
+    mbar_init(smem_u32(&bars->drain), 1);
+    for (int e = 0; e < 2; ++e) {
+      mbar_init(smem_u32(&bars->tq_full[e]), 1);
+      mbar_init(smem_u32(&bars->tq_empty[e]), 1 + kSoftmaxThreads);
     }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpTmem) {
+  if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if (warp == kWarpLoad0 && lane == 0) {
+  if (warp == kWarpLoad && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -595,23 +575,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp >= kSoftmaxThreads / 32) {
     regs_dec<kRegsOther>();
-    if (warp == kWarpLoad0 || warp == kWarpLoad1)
-      run_producer<D>(warp == kWarpLoad0 ? 0 : 1, &tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
+    if (warp == kWarpLoad)
+      run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
+    else if (warp == kWarpMma)
+      run_mma<D>(p, bars, tmem, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, OUT_F32>(p, bars, tmem, base, abort_flag);
-    if ((warp & 7) == 0) {  // the slot's MMA issuer: its MMAs finish before TMEM is freed
-      const int sl = warp >> 3;
-      if (elect_one()) mma_commit(smem_u32(&bars->drain[sl]));
-      __syncwarp();
-      wait_drain(smem_u32(&bars->drain[sl]), 0);
-    }
+    run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);
   }
   __syncwarp();  // reconverge each warp before the CTA-wide barrier
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpTmem) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
