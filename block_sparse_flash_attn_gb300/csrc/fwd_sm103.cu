@@ -22,7 +22,9 @@
 //   warp  9    tcgen05 MMA issuer (elected lane) and tensor-memory owner
 //   warps 10-11 idle (complete warpgroup 2 for setmaxnreg)
 // Tensor memory (512 columns allocated): two score buffers S[0] = [0,128),
-// S[1] = [128,256) and the fp32 output accumulator O = [256, 256+D).  Block g
+// S[1] = [128,256) and the fp32 output accumulator O = [256, 256+D) followed
+// by 16 columns holding the row sum of the rounded P (the PV MMA multiplies
+// P by [V | ones]).  Block g
 // (counted over the CTA's whole run) uses S[g % 2]; its bf16 probabilities P
 // overwrite the scores already read (keys 0..63 -> columns 0..31, keys
 // 64..127 -> columns 64..95).  With two score buffers the MMA warp computes
@@ -73,11 +75,19 @@ struct Cfg {
   static constexpr int kStages = 2;                  // K ring and V ring depth
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kTileBytes;
+  // V region: the PV MMA's B operand is [V | ones]: N = D + 16, its 64-wide
+  // column groups kVGroup bytes apart.  Group c of stage s sits at
+  // kVOff + c * kVGroup + s * kBoxBytes; the last group is a tile of bf16 ones,
+  // so the tensor core also accumulates the row sum of the rounded P into O
+  // columns D..D+15.
+  static constexpr int kVGroup = kStages * kBoxBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;  // ones tiles, one per stage
+  static constexpr int kBarOff = kOnesOff + kStages * kBoxBytes;
   static constexpr int kSmem = kBarOff + 1024;
+  static constexpr int kPvN = D + 16;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
-  static constexpr uint32_t kIdescO = idesc_bf16_f32(128, D, true);
+  static constexpr uint32_t kIdescO = idesc_bf16_f32(128, kPvN, true);
 };
 
 // One scheduled tile as the producer publishes it to the MMA and softmax warps.
@@ -142,13 +152,13 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 
   // One TMA tile (128 rows x D) into a buffer, completion on `full`, after
   // `empty` says the buffer's previous contents were consumed.
-  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t full, uint32_t empty,
-                       uint32_t empty_parity, int row) -> bool {
+  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t box_stride, uint32_t full,
+                       uint32_t empty, uint32_t empty_parity, int row) -> bool {
     if (!wait_warp(empty, empty_parity, abort_flag, p.status, lim)) return false;
     if (elect_one()) {
       mbar_arrive_expect_tx(full, C::kTileBytes);
 #pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, full, c * 64, row);
+      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * box_stride, tm, full, c * 64, row);
     }
     __syncwarp();
     return true;
@@ -161,7 +171,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     const int st = kc % C::kStages;
     const uint32_t ph = ((uint32_t)(kc / C::kStages) & 1u) ^ 1u;
     ++kc;
-    return load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes,
+    return load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes, C::kBoxBytes,
                      smem_u32(&bars->k_full[st]), smem_u32(&bars->k_empty[st]), ph,
                      hrow + kb * kBlock);
   };
@@ -173,7 +183,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     const int st = vc % C::kStages;
     const uint32_t ph = ((uint32_t)(vc / C::kStages) & 1u) ^ 1u;
     ++vc;
-    return load_tile(tm_v, smem_base + C::kVOff + st * C::kTileBytes,
+    return load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
                      smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]), ph,
                      hrow + kb * kBlock);
   };
@@ -212,7 +222,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     if (t < 0) break;
     const int hrow = bh * p.S;
     // Q, once its buffer is free (the previous tile's last S is done)
-    ok = load_tile(tm_q, smem_base + C::kQOff, smem_u32(&bars->q_full),
+    ok = load_tile(tm_q, smem_base + C::kQOff, C::kBoxBytes, smem_u32(&bars->q_full),
                    smem_u32(&bars->q_empty), ((uint32_t)qc & 1u) ^ 1u, hrow + qb * kBlock);
     ++qc;
     if (ok) ok = load_k(p.col_idx[r0], hrow);
@@ -275,10 +285,11 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
     ++kc;
     return true;
   };
-  // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P(g) is read from
-  // S[g % 2] (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31,
-  // keys 64..127 at columns 64..95); V is MN-major (D contiguous): 8-key
-  // groups 1024 bytes apart, 64-column boxes 16 KB apart.
+  // [O | l] (+)= P [V | 1] : M=128, N=D+16, K=128 keys in steps of 16.  P(g)
+  // is read from S[g % 2] (bf16 pairs, 8 columns per step; keys 0..63 at
+  // columns 0..31, keys 64..127 at columns 64..95); B is MN-major (D
+  // contiguous): 8-key groups 1024 bytes apart, 64-wide column groups
+  // kVGroup apart, the last group being the stage's ones tile.
   auto do_pv = [&](bool accumulate) -> bool {
     // P(g) in, g = vc: two barriers so that P(g+1) can never be mistaken for P(g)
     if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
@@ -289,10 +300,10 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
                    p.status, lim))
       return false;
     tc_fence_after();
-    const uint32_t vaddr = smem_base + C::kVOff + st * C::kTileBytes;
+    const uint32_t vaddr = smem_base + C::kVOff + st * C::kBoxBytes;
     const uint32_t pbuf = tmem + (vc % 2) * 128;  // block g's score buffer (g = vc)
     if (elect_one()) {
-      const uint64_t vd = smem_desc_sw128(vaddr, C::kBoxBytes, 1024);
+      const uint64_t vd = smem_desc_sw128(vaddr, C::kVGroup, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
@@ -359,21 +370,19 @@ __device__ void write_empty_tiles(const FwdParams& p) {
 }
 
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
-// pairs into pr[]; accumulates the unrounded (a32, for LSE) and the rounded
-// (ar, the O denominator) row sums in two independent accumulators each.
+// pairs into pr[]; accumulates the unrounded row sum (for LSE) in two
+// independent accumulators.  The sum of the rounded values (the O
+// denominator) is accumulated by the tensor core next to O.
 __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
-                                              float nm, float (&a32)[2], float (&ar)[2]) {
+                                              float nm, float (&a32)[2]) {
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     float x0, x1;
     fma2(x0, x1, __uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1]), sl, sl, nm, nm);
     const float p0 = ex2_approx(x0);
     const float p1 = ex2_approx(x1);
-    const uint32_t pk = pack_bf16x2(p0, p1);
-    pr[q] = pk;
+    pr[q] = pack_bf16x2(p0, p1);
     add2(a32[0], a32[1], a32[0], a32[1], p0, p1);
-    add2(ar[0], ar[1], ar[0], ar[1], __uint_as_float(pk << 16),
-         __uint_as_float(pk & 0xFFFF0000u));
   }
 }
 
@@ -426,7 +435,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
-    float a32[2] = {0.f, 0.f}, ar[2] = {0.f, 0.f};  // unrounded (LSE) / rounded (O) partial sums
+    float a32[2] = {0.f, 0.f};  // unrounded partial row sums (LSE)
     for (int jb = 0; jb < n; ++jb, ++g) {
       const int b = g & 1;  // S buffer and ring stage of this block
       // S(g) ready = its commit released K(g)'s stage
@@ -455,11 +464,9 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         m = xm;
         a32[0] *= f;
         a32[1] *= f;
-        ar[0] *= f;
-        ar[1] *= f;
       }
       uint32_t pr[32];
-      softmax_exp64(sr, pr, sl, -m, a32, ar);
+      softmax_exp64(sr, pr, sl, -m, a32);
       tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
 
       // O rescale (this thread's columns) when a row's max moved: first wait
@@ -479,6 +486,12 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
           for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
           tmem_st16x2_32<DH>(tO + c0, orr);
         }
+        uint32_t rs[1];  // the row-sum column this thread reads at the end scales with O
+        tmem_ld16x2_1<1>(tO + D, rs);
+        tmem_wait_ld();
+        reg_fence(rs, 1);
+        rs[0] = __float_as_uint(__uint_as_float(rs[0]) * f);
+        tmem_st16x2_1<1>(tO + D, rs);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -490,9 +503,14 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                    abort_flag, p.status, lim))
       return;  // the tile's last PV has landed in O
     tc_fence_after();
-    float l = ar[0] + ar[1];
+    // sum of the rounded P accumulated by the tensor core in O column D
+    // (lanes 16..31 read the identical column D+1)
+    uint32_t rs[1];
+    tmem_ld16x2_1<1>(tO + D, rs);
+    tmem_wait_ld();
+    reg_fence(rs, 1);
+    const float l = __uint_as_float(rs[0]);
     float l32 = a32[0] + a32[1];
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
     l32 += __shfl_xor_sync(0xffffffffu, l32, 16);
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
     const float inv_l = 1.0f / l;
@@ -561,6 +579,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
+  }
+  {  // bf16 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
+    uint4* ones = reinterpret_cast<uint4*>(smem_raw + (base - raw) + C::kOnesOff);
+    for (int i = threadIdx.x; i < C::kStages * C::kBoxBytes / 16; i += kThreads)
+      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == kWarpLoad && lane == 0) {
     tma_prefetch_desc(&tm_q);

@@ -258,6 +258,20 @@ __device__ __forceinline__ void tmem_st16x2_32(uint32_t taddr, const uint32_t* r
       : "memory");
 }
 
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld16x2_1(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x1.b32 {%0}, [%1], %2;"
+               : "=r"(r[0])
+               : "r"(taddr), "n"(kSplit));
+}
+
+template <int kSplit>
+__device__ __forceinline__ void tmem_st16x2_1(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x1.b32 [%0], %2, {%1};" ::"r"(taddr), "r"(r[0]),
+               "n"(kSplit)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
