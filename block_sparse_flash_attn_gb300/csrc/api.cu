@@ -183,7 +183,8 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
                       sizeof(int) * (size_t)(p->n_empty > 0 ? p->n_empty : 1))) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = plan_fill_and_order(d_mask, BH, nb, causal, p->dev.row_ptr, d_live_off,
-                               p->dev.col_idx, p->dev.tile_order, p->dev.empty_tiles, st)) !=
+                               p->dev.col_idx, p->dev.tile_order, p->dev.empty_tiles,
+                               device_sm_count(p->device), st)) !=
       cudaSuccess)
     return fail(from_cuda(e));
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));

@@ -12,15 +12,19 @@
 // Logic": only the small 128x128 block is ever materialised).
 //
 // GB300 design (one persistent CTA per SM, 384 threads = 3 warpgroups, one
-// query tile in flight per CTA):
+// query tile in the softmax at a time):
 //   warps 0-7  softmax + epilogue.  Each warp covers 16 query rows (TMEM
 //              lanes); lanes 0..15 own key columns 0..63 of every block (O
 //              columns [0, D/2)), lanes 16..31 the same rows' columns 64..127
 //              (O columns [D/2, D)); tcgen05 16x32bx2 accesses put both halves
 //              of a row in one warp, so row max and sums combine by shuffle.
-//   warp  8    tile scheduler + TMA producer (elected lane)
+//   warp  8    TMA producer (elected lane)
 //   warp  9    tcgen05 MMA issuer (elected lane) and tensor-memory owner
-//   warps 10-11 idle (complete warpgroup 2 for setmaxnreg)
+//   warp  10   tile scheduler: claims the next tile when the producer asks
+//              for it (a few blocks before the current tile's end),
+//              publishes it (CSR range and first key blocks) in a 2-slot
+//              queue and loads its Q (elected lane)
+//   warp  11   idle (completes warpgroup 2 for setmaxnreg)
 // Tensor memory (512 columns allocated): two score buffers S[0] = [0,128),
 // S[1] = [128,256) and the fp32 output accumulator O = [256, 256+D) followed
 // by 16 columns holding the row sum of the rounded P (the PV MMA multiplies
@@ -30,18 +34,32 @@
 // 64..127 -> columns 64..95).  With two score buffers the MMA warp computes
 // S(j+1) while the softmax works on block j, and issues S(j+2) into block j's
 // buffer right after O += P(j) V(j), so neither side waits for the other in
-// steady state.  Shared memory: Q, a 2-stage ring of K tiles and a 2-stage
-// ring of V tiles (128 x D bf16 each, 128-byte swizzled by TMA, read by
-// tcgen05.mma through matrix descriptors).
+// steady state.  Shared memory: Q buffers and rings of K and V tiles
+// (128 x D bf16 each, 128-byte swizzled by TMA, read by tcgen05.mma through
+// matrix descriptors) plus one 16 KB tile of bf16 ones per V stage: at
+// D = 128 one Q, three K and two V stages (224 KB), at D = 64 two Q and four
+// stages per ring.  A tile's TMA load takes about as long as one block's
+// MMAs, so a third K stage gives each K load a block's time of slack.
 //
-// Per tile with n live key blocks the MMA warp issues
-//   S(0), S(1); then for j = 0..n-1: [P(j) in] O (+)= P(j) V(j); S(j+2).
-// The commit after S(g) frees K(g)'s ring stage and is the softmax's "S(g)
-// ready" signal; the commit after PV(g) frees V(g)'s stage and is "PV(g)
-// done", which the softmax waits for only before an O rescale and, for the
-// tile's last block, before the epilogue.  Online softmax in base 2 with lazy
-// rescale: the running max m only moves when a block's max exceeds it by more
-// than 8 (log2 units), so P <= 256 and the O rescale is rare.
+// The producer sees the CTA's tiles as one stream of key blocks g = 0, 1,
+// 2, ... (every live block of every tile the CTA claimed, tile after tile)
+// and loads K two blocks ahead of V along it, so the next tile's first K
+// tiles arrive while the current tile runs; the scheduler warp loads the
+// next tile's Q as soon as the Q buffer is free.  Per tile with n live key
+// blocks the MMA warp issues
+//   S(0), S(1); then for j = 0..n-1: [P(j) in] O (+)= P(j) V(j); S(j+2)
+// (S(j+2) only while j+2 < n), and goes straight on to the next tile's
+// S(0), S(1) after the last PV.  The commit after S(g) frees K(g)'s ring
+// stage and is the softmax's "S(g) ready" signal; the commit after PV(g)
+// frees V(g)'s stage and is "PV(g) done", which the softmax waits for only
+// before an O rescale and, for the tile's last block, before the epilogue
+// (which therefore always precedes the next tile's first PV, the one that
+// overwrites O).  Online softmax in base 2 with lazy rescale: the running
+// max m only moves when a block's max exceeds it by more than 8 (log2
+// units), so P <= 256 and the O rescale is rare.  O is normalised by the
+// row sum of the bf16-rounded P that multiplied V (so the weights on V sum
+// to one even when a single key dominates a row); the LSE uses the fp32 sum
+// of the unrounded P.
 //
 // Every wait is bounded (globaltimer); on expiry the kernel records a timeout
 // in the status word, every role leaves its loop, outstanding TMA loads and
@@ -59,6 +77,11 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpSched = 10;
+// The producer asks for the next tile when its K cursor has this many blocks
+// of the current tile left: claiming a tile (four dependent global reads)
+// and loading its Q take about as long as this many blocks' MMAs.
+constexpr int kClaimAhead = 4;
 // Launch budget 384 x 168 registers; the producer/MMA warpgroup hands part of
 // its share to the two softmax warpgroups: 256 x 208 + 128 x 88 = 384 x 168.
 constexpr int kRegsSoftmax = 208;
@@ -72,47 +95,64 @@ struct Cfg {
   static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
   static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
-  static constexpr int kStages = 2;                  // K ring and V ring depth
+  // Ring depths and Q buffers, each filling 224 KB: D = 128 has one Q tile,
+  // three K stages and two V stages (each V stage with its ones tile);
+  // D = 64 two Q tiles and four stages of each ring.
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kQStages = D == 128 ? 1 : 2;
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kTileBytes;
+  static constexpr int kKOff = kQStages * kTileBytes;
   // V region: the PV MMA's B operand is [V | ones]: N = D + 16, its 64-wide
   // column groups kVGroup bytes apart.  Group c of stage s sits at
-  // kVOff + c * kVGroup + s * kBoxBytes; the last group is a tile of bf16 ones,
-  // so the tensor core also accumulates the row sum of the rounded P into O
-  // columns D..D+15.
-  static constexpr int kVGroup = kStages * kBoxBytes;
-  static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;  // ones tiles, one per stage
-  static constexpr int kBarOff = kOnesOff + kStages * kBoxBytes;
+  // kVOff + c * kVGroup + s * kBoxBytes; the last group is a tile of bf16
+  // ones, so the tensor core also accumulates the row sum of the rounded P
+  // into O columns D..D+15.
+  static constexpr int kVGroup = kVStages * kBoxBytes;
+  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;  // ones tiles, one per V stage
+  static constexpr int kBarOff = kOnesOff + kVStages * kBoxBytes;
   static constexpr int kSmem = kBarOff + 1024;
   static constexpr int kPvN = D + 16;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, kPvN, true);
 };
 
-// One scheduled tile as the producer publishes it to the MMA and softmax warps.
+constexpr int kSlotCols = 32;  // key blocks of a tile published with it
+constexpr int kMaxStages = 4;  // deepest K / V ring of any Cfg
+
+// One scheduled tile as the scheduler warp publishes it to the producer, MMA
+// and softmax warps.
 struct TileInfo {
   int t;     // tile id (b*H + h)*nb + qb, or -1 when no tiles are left
   int r0;    // first CSR entry of the tile
   int n;     // live key blocks
   int diag;  // causal and the last live block is the diagonal one
+  int cols[kSlotCols];  // its first min(n, 32) key blocks (CSR col_idx[r0 ..])
 };
 
 struct __align__(16) Bars {
-  uint64_t k_full[2];   // K ring stage loaded
-  uint64_t k_empty[2];  // S(g) complete: K stage free, S(g) ready for the softmax
-  uint64_t v_full[2];   // V ring stage loaded
-  uint64_t v_empty[2];  // PV(g) complete: V stage free, O holds block g
-  uint64_t q_full;
-  uint64_t q_empty;     // the tile's last S complete: Q buffer free
+  uint64_t k_full[kMaxStages];   // K ring stage loaded
+  uint64_t k_empty[kMaxStages];  // S(g) complete: K stage free, S(g) ready for the softmax
+  uint64_t v_full[kMaxStages];   // V ring stage loaded
+  uint64_t v_empty[kMaxStages];  // PV(g) complete: V stage free, O holds block g
+  uint64_t q_full[2];
+  uint64_t q_empty[2];  // the tile's last S complete: Q buffer free
   uint64_t p_full[2];   // all softmax threads wrote P(g) (indexed by g % 2)
-  uint64_t tq_full[2];
-  uint64_t tq_empty[2];
+  uint64_t tq_full[2];  // tile queue slot published
+  uint64_t tq_empty[2]; // slot read by producer, MMA warp and every softmax thread
   uint64_t drain;
+  uint64_t req;         // the producer asks for the next tile (once per tile)
   TileInfo tq[2];
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Bars) <= 1024, "barrier block must fit its 1 KB region");
+static_assert(Cfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
+static_assert(Cfg<64>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
+static_assert(Cfg<128>::kKStages <= kMaxStages && Cfg<64>::kKStages <= kMaxStages &&
+                  Cfg<128>::kVStages <= kMaxStages && Cfg<64>::kVStages <= kMaxStages,
+              "ring depth");
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -137,18 +177,143 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
 }
 
 // ---------------------------------------------------------------------------
-// warp 8: tile scheduler + TMA producer
+// warp 10: tile scheduler
 // ---------------------------------------------------------------------------
-// Load order per tile (matching the MMA warp's consumption order within each
-// ring): Q, K(0), K(1), then for j = 0..n-1: V(j), K(j+2).
+// Claims tiles from the global counter (in the plan's tile order).  The first
+// tile is claimed at once, every later one when the producer asks for it
+// (`req`, a few key blocks before the producer needs it), so a CTA never
+// holds a claimed tile long before it can start it: tiles stay with the SMs
+// that free up first, which keeps the end of the run balanced.  Each tile is
+// published in the 2-slot queue with its first key blocks, then its Q is
+// loaded into the tile's Q buffer; the claim's chain of dependent global
+// reads (counter, tile order, CSR row pointers, column indices) and the Q
+// load are thus off the producer's and the MMA warp's path.  Ends after
+// publishing the "no tiles left" entry.
+template <int D>
+__device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars* bars,
+                              uint32_t smem_base, volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int lane = threadIdx.x & 31;
+  const uint64_t lim = p.timeout_ns;
+  const int rows = p.n_live + p.n_empty;
+  int qc = 0;  // Q tiles loaded
+  bool ok = true;
+  for (int i = 0; ok; ++i) {
+    const int e = i & 1;
+    if (i > 0 && !wait_warp(smem_u32(&bars->req), (uint32_t)(i - 1) & 1u, abort_flag, p.status,
+                            lim)) {
+      ok = false;
+      break;
+    }
+    if (!wait_warp(smem_u32(&bars->tq_empty[e]), ((uint32_t)(i >> 1) & 1u) ^ 1u, abort_flag,
+                   p.status, lim)) {
+      ok = false;
+      break;
+    }
+    int idx = 0;
+    if (lane == 0) idx = atomicAdd(p.counter, 1);
+    idx = __shfl_sync(0xffffffffu, idx, 0);
+    const int t = idx < p.n_live ? p.tile_order[idx] : -1;
+    int r0 = 0, cnt = 0, diag = 0;
+    if (t >= 0) {
+      if (t >= rows) {
+        raise_internal(abort_flag, p.status);
+        ok = false;
+        break;
+      }
+      r0 = p.row_ptr[t];
+      cnt = p.row_ptr[t + 1] - r0;
+      if (cnt <= 0 || cnt > p.nb) {
+        raise_internal(abort_flag, p.status);
+        ok = false;
+        break;
+      }
+      diag = (p.causal && p.col_idx[r0 + cnt - 1] == t % p.nb) ? 1 : 0;
+      if (lane < cnt) bars->tq[e].cols[lane] = p.col_idx[r0 + lane];
+    }
+    if (lane == 0) {
+      volatile TileInfo* slot = &bars->tq[e];
+      slot->t = t;
+      slot->r0 = r0;
+      slot->n = cnt;
+      slot->diag = diag;
+    }
+    __syncwarp();  // every lane's writes to the slot precede the arrive
+    if (lane == 0) mbar_arrive(smem_u32(&bars->tq_full[e]));
+    __syncwarp();
+    if (t < 0) break;
+    // the tile's Q, once its buffer is free (the last S of the tile before
+    // the previous one is complete)
+    const int qs = qc % C::kQStages;
+    if (!wait_warp(smem_u32(&bars->q_empty[qs]), ((uint32_t)(qc / C::kQStages) & 1u) ^ 1u, abort_flag,
+                   p.status, lim)) {
+      ok = false;
+      break;
+    }
+    if (elect_one()) {
+      const int bh = t / p.nb;
+      const int row = bh * p.S + (t - bh * p.nb) * kBlock;
+      const uint32_t full = smem_u32(&bars->q_full[qs]);
+      const uint32_t dst = smem_base + C::kQOff + qs * C::kTileBytes;
+      mbar_arrive_expect_tx(full, C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_2d(dst + c * C::kBoxBytes, tm_q, full, c * 64, row);
+    }
+    __syncwarp();
+    ++qc;
+  }
+  if (!ok) {
+    // Let the Q loads this warp issued land before the CTA exits.
+    for (int i = (qc > C::kQStages ? qc - C::kQStages : 0); i < qc; ++i)
+      wait_drain(smem_u32(&bars->q_full[i % C::kQStages]), (uint32_t)(i / C::kQStages) & 1u);
+  }
+}
+
+// Reads tile-queue slot `tqc % 2` (waiting until it is published) and marks
+// it read.  Returns false when the wait failed.
+__device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& p,
+                                          volatile int* abort_flag, int& t, int& r0, int& n,
+                                          int& col) {
+  const int lane = threadIdx.x & 31;
+  const int e = tqc & 1;
+  if (!wait_warp(smem_u32(&bars->tq_full[e]), (uint32_t)(tqc >> 1) & 1u, abort_flag, p.status,
+                 p.timeout_ns))
+    return false;
+  const volatile TileInfo* slot = &bars->tq[e];
+  t = slot->t;
+  r0 = slot->r0;
+  n = slot->n;
+  col = (t >= 0 && lane < n && lane < kSlotCols) ? slot->cols[lane] : 0;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(smem_u32(&bars->tq_empty[e]));
+  __syncwarp();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// warp 8: TMA producer
+// ---------------------------------------------------------------------------
+// Two cursors over the CTA's block stream: the K cursor runs two blocks ahead
+// of the V cursor, matching the MMA warp's order S(g+2) after PV(g).  Each
+// ring is loaded in its consumption order.  When the K cursor has
+// kClaimAhead blocks of its tile left (or enters a shorter tile) it asks the
+// scheduler for the next tile.
 template <int D>
 __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, Bars* bars,
                              uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D>;
+  const int lane = threadIdx.x & 31;
   const uint64_t lim = p.timeout_ns;
-  int kc = 0, vc = 0, qc = 0, tqc = 0;  // K / V / Q tiles loaded, tiles claimed
-  bool ok = true;
+  int kc = 0, vc = 0, tqc = 0;  // K / V tiles loaded, tiles taken
+  bool ok = true, more = true;
+  int k_ask = 0;  // K cursor's remaining-block count at which to ask for the next tile
+  // K cursor: position in its tile; `k_col` holds, in lane i, the key block
+  // of the tile's entry 32 * (k_j / 32) + i.
+  int k_rem = 0, k_j = 0, k_r0 = 0, k_hrow = 0, k_col = 0;
+  // key rows of blocks whose K is loaded and V not yet (at most two)
+  int f0 = 0, f1 = 0, nf = 0;
 
   // One TMA tile (128 rows x D) into a buffer, completion on `full`, after
   // `empty` says the buffer's previous contents were consumed.
@@ -163,82 +328,70 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     __syncwarp();
     return true;
   };
-  auto load_k = [&](int kb, int hrow) -> bool {
+  auto next_k = [&]() -> bool {
+    if (k_rem == 0) {
+      if (!more) return true;
+      int t = 0;
+      if (!take_tile(bars, tqc, p, abort_flag, t, k_r0, k_rem, k_col)) return false;
+      ++tqc;
+      if (t < 0) {
+        more = false;
+        k_rem = 0;
+        return true;
+      }
+      k_hrow = (t / p.nb) * p.S;
+      k_j = 0;
+      k_ask = k_rem - 1 < kClaimAhead ? k_rem - 1 : kClaimAhead;
+    } else if ((k_j & 31) == 0) {  // next 32 entries of the tile's CSR list
+      k_col = (lane < k_rem) ? p.col_idx[k_r0 + k_j + lane] : 0;
+    }
+    const int kb = __shfl_sync(0xffffffffu, k_col, k_j & 31);
     if (kb < 0 || kb >= p.nb) {
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int st = kc % C::kStages;
-    const uint32_t ph = ((uint32_t)(kc / C::kStages) & 1u) ^ 1u;
+    const int row = k_hrow + kb * kBlock;
+    const int st = kc % C::kKStages;
+    if (!load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes, C::kBoxBytes,
+                   smem_u32(&bars->k_full[st]), smem_u32(&bars->k_empty[st]),
+                   ((uint32_t)(kc / C::kKStages) & 1u) ^ 1u, row))
+      return false;
     ++kc;
-    return load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes, C::kBoxBytes,
-                     smem_u32(&bars->k_full[st]), smem_u32(&bars->k_empty[st]), ph,
-                     hrow + kb * kBlock);
-  };
-  auto load_v = [&](int kb, int hrow) -> bool {
-    if (kb < 0 || kb >= p.nb) {
-      raise_internal(abort_flag, p.status);
-      return false;
+    ++k_j;
+    --k_rem;
+    if (k_rem == k_ask) {
+      if (elect_one()) mbar_arrive(smem_u32(&bars->req));
+      __syncwarp();
     }
-    const int st = vc % C::kStages;
-    const uint32_t ph = ((uint32_t)(vc / C::kStages) & 1u) ^ 1u;
+    if (nf == 0) f0 = row; else f1 = row;
+    ++nf;
+    return true;
+  };
+  auto load_v = [&](int row) -> bool {
+    const int st = vc % C::kVStages;
+    if (!load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
+                   smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]),
+                   ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u, row))
+      return false;
     ++vc;
-    return load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
-                     smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]), ph,
-                     hrow + kb * kBlock);
+    return true;
   };
 
-  while (ok) {
-    // claim a tile and publish it to the MMA and softmax warps
-    const int e = tqc & 1;
-    const uint32_t ph = (uint32_t)(tqc >> 1) & 1u;
-    if (!wait_warp(smem_u32(&bars->tq_empty[e]), ph ^ 1u, abort_flag, p.status, lim)) break;
-    int idx = 0;
-    if (elect_one()) idx = atomicAdd(p.counter, 1);
-    idx = __reduce_max_sync(0xffffffffu, idx);  // the elected lane's claim, to every lane
-    const int t = idx < p.n_live ? p.tile_order[idx] : -1;
-    int r0 = 0, cnt = 0, bh = 0, qb = 0, diag = 0;
-    if (t >= 0) {
-      r0 = p.row_ptr[t];
-      cnt = p.row_ptr[t + 1] - r0;
-      bh = t / p.nb;
-      qb = t - bh * p.nb;
-      if (cnt <= 0 || cnt > p.nb) {
-        raise_internal(abort_flag, p.status);
-        break;
-      }
-      diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
-    }
-    if (elect_one()) {
-      volatile int* slot = reinterpret_cast<volatile int*>(&bars->tq[e]);
-      slot[0] = t;
-      slot[1] = r0;
-      slot[2] = cnt;
-      slot[3] = diag;
-      mbar_arrive(smem_u32(&bars->tq_full[e]));
-    }
-    __syncwarp();
-    ++tqc;
-    if (t < 0) break;
-    const int hrow = bh * p.S;
-    // Q, once its buffer is free (the previous tile's last S is done)
-    ok = load_tile(tm_q, smem_base + C::kQOff, C::kBoxBytes, smem_u32(&bars->q_full),
-                   smem_u32(&bars->q_empty), ((uint32_t)qc & 1u) ^ 1u, hrow + qb * kBlock);
-    ++qc;
-    if (ok) ok = load_k(p.col_idx[r0], hrow);
-    if (ok && cnt > 1) ok = load_k(p.col_idx[r0 + 1], hrow);
-    for (int j = 0; ok && j < cnt; ++j) {
-      ok = load_v(p.col_idx[r0 + j], hrow);
-      if (ok && j + 2 < cnt) ok = load_k(p.col_idx[r0 + j + 2], hrow);
-    }
+  ok = next_k();
+  if (ok) ok = next_k();
+  while (ok && nf > 0) {
+    const int row = f0;
+    f0 = f1;
+    --nf;
+    ok = load_v(row);
+    if (ok) ok = next_k();
   }
   if (!ok) {
     // Let every TMA load this warp issued land before the CTA exits.
-    for (int i = (kc > C::kStages ? kc - C::kStages : 0); i < kc; ++i)
-      wait_drain(smem_u32(&bars->k_full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u);
-    for (int i = (vc > C::kStages ? vc - C::kStages : 0); i < vc; ++i)
-      wait_drain(smem_u32(&bars->v_full[i % C::kStages]), (uint32_t)(i / C::kStages) & 1u);
-    if (qc > 0) wait_drain(smem_u32(&bars->q_full), (uint32_t)(qc - 1) & 1u);
+    for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
+      wait_drain(smem_u32(&bars->k_full[i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
+    for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
+      wait_drain(smem_u32(&bars->v_full[i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
   }
 }
 
@@ -255,18 +408,17 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
   // applied as -Q (instruction-descriptor negate bit) so the softmax always
   // sees a non-negative multiplier.
   const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
-  const uint32_t qaddr = smem_base + C::kQOff;
-  int kc = 0, vc = 0, qc = 0, tqc = 0;
+  int kc = 0, vc = 0, qc = 0, tqc = 0;  // S issued, PV issued, tiles' Q used, tiles taken
 
   auto commit = [&](uint32_t bar) {
     if (elect_one()) mma_commit(bar);
     __syncwarp();
   };
-  // S(g) into S[g % 2] from K ring stage g % 2; its commit frees the stage and
-  // tells the softmax that S(g) is ready.
-  auto do_s = [&]() -> bool {
-    const int st = kc % C::kStages;
-    if (!wait_warp(smem_u32(&bars->k_full[st]), (uint32_t)(kc / C::kStages) & 1u, abort_flag,
+  // S(g) into S[g % 2] from K ring stage g % kKStages; its commit frees the
+  // stage and tells the softmax that S(g) is ready.
+  auto do_s = [&](uint32_t qaddr) -> bool {
+    const int st = kc % C::kKStages;
+    if (!wait_warp(smem_u32(&bars->k_full[st]), (uint32_t)(kc / C::kKStages) & 1u, abort_flag,
                    p.status, lim))
       return false;
     const uint32_t kaddr = smem_base + C::kKOff + st * C::kTileBytes;
@@ -277,7 +429,7 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + st * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
+        mma_ss(tmem + (kc & 1) * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
       }
       mma_commit(smem_u32(&bars->k_empty[st]));
     }
@@ -295,8 +447,8 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
     if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
                    p.status, lim))
       return false;
-    const int st = vc % C::kStages;
-    if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kStages) & 1u, abort_flag,
+    const int st = vc % C::kVStages;
+    if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kVStages) & 1u, abort_flag,
                    p.status, lim))
       return false;
     tc_fence_after();
@@ -316,31 +468,30 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
     ++vc;
     return true;
   };
-
+  // Per tile: S(0), S(1); then for j = 0..n-1: PV(j), S(j+2) while j+2 < n.
+  // The next tile's S(0) and S(1) follow the tile's last PV, so that PV (the
+  // one the softmax's epilogue waits for) never queues behind them; its Q
+  // and first K tiles are normally loaded long before.
   bool ok = true;
   while (ok) {
-    const int e = tqc & 1;
-    if (!wait_warp(smem_u32(&bars->tq_full[e]), (uint32_t)(tqc >> 1) & 1u, abort_flag, p.status,
-                   lim))
-      break;
-    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[e]);
-    const int t = slot[0];
-    const int n = slot[2];
-    if (elect_one()) mbar_arrive(smem_u32(&bars->tq_empty[e]));
-    __syncwarp();
+    int t = 0, r0 = 0, n = 0, col = 0;
+    if (!take_tile(bars, tqc, p, abort_flag, t, r0, n, col)) break;
     ++tqc;
     if (t < 0) break;
-    if (!wait_warp(smem_u32(&bars->q_full), (uint32_t)qc & 1u, abort_flag, p.status, lim)) break;
+    const int qs = qc % C::kQStages;
+    if (!wait_warp(smem_u32(&bars->q_full[qs]), (uint32_t)(qc / C::kQStages) & 1u, abort_flag, p.status,
+                   lim))
+      break;
     ++qc;
-    // S(0), S(1)
-    ok = do_s();
-    if (ok && n > 1) ok = do_s();
-    if (ok && n <= 2) commit(smem_u32(&bars->q_empty));
+    const uint32_t qaddr = smem_base + C::kQOff + qs * C::kTileBytes;
+    ok = do_s(qaddr);
+    if (ok && n > 1) ok = do_s(qaddr);
+    if (ok && n <= 2) commit(smem_u32(&bars->q_empty[qs]));  // the tile's last S: Q free
     for (int j = 0; ok && j < n; ++j) {
       ok = do_pv(j > 0);
       if (ok && j + 2 < n) {
-        ok = do_s();
-        if (ok && j + 2 == n - 1) commit(smem_u32(&bars->q_empty));
+        ok = do_s(qaddr);
+        if (ok && j + 2 == n - 1) commit(smem_u32(&bars->q_empty[qs]));
       }
     }
   }
@@ -370,9 +521,10 @@ __device__ void write_empty_tiles(const FwdParams& p) {
 }
 
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
-// pairs into pr[]; accumulates the unrounded row sum (for LSE) in two
-// independent accumulators.  The sum of the rounded values (the O
-// denominator) is accumulated by the tensor core next to O.
+// pairs into pr[] (the A operand of the PV product); accumulates the fp32
+// row sum of the unrounded p (for the LSE) in two independent accumulators.
+// The sum of the rounded values (the O denominator) is accumulated by the
+// tensor core next to O.
 __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
                                               float nm, float (&a32)[2]) {
 #pragma unroll
@@ -402,6 +554,7 @@ __device__ __forceinline__ float row_max64(const uint32_t* sr) {
 template <int D, bool OUT_F32>
 __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
+  using C = Cfg<D>;
   constexpr int DH = D / 2;            // O columns owned by this thread
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -435,12 +588,12 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
-    float a32[2] = {0.f, 0.f};  // unrounded partial row sums (LSE)
+    float a32[2] = {0.f, 0.f};  // partial fp32 row sums of this half row
     for (int jb = 0; jb < n; ++jb, ++g) {
-      const int b = g & 1;  // S buffer and ring stage of this block
+      const int b = g & 1;  // S buffer of this block
       // S(g) ready = its commit released K(g)'s stage
-      if (!wait_warp(smem_u32(&bars->k_empty[b]), (uint32_t)(g >> 1) & 1u, abort_flag, p.status,
-                     lim))
+      if (!wait_warp(smem_u32(&bars->k_empty[g % C::kKStages]), (uint32_t)(g / C::kKStages) & 1u,
+                     abort_flag, p.status, lim))
         return;
       tc_fence_after();
       const uint32_t tS = tmem + b * 128 + lane_off;
@@ -472,8 +625,8 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       // O rescale (this thread's columns) when a row's max moved: first wait
       // until PV(g-1) has landed in O (PV(g) is not issued before P(g)).
       if (jb > 0 && __any_sync(0xffffffffu, need)) {
-        if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u,
-                       abort_flag, p.status, lim))
+        if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) % C::kVStages]),
+                       (uint32_t)((g - 1) / C::kVStages) & 1u, abort_flag, p.status, lim))
           return;
         tc_fence_after();
 #pragma unroll
@@ -499,19 +652,20 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     }
 
     // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
-    if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) & 1]), (uint32_t)((g - 1) >> 1) & 1u,
-                   abort_flag, p.status, lim))
+    if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) % C::kVStages]),
+                   (uint32_t)((g - 1) / C::kVStages) & 1u, abort_flag, p.status, lim))
       return;  // the tile's last PV has landed in O
     tc_fence_after();
     // sum of the rounded P accumulated by the tensor core in O column D
-    // (lanes 16..31 read the identical column D+1)
+    // (lanes 16..31 read the identical column D+1): the O denominator, so
+    // that the weights applied to V sum to one
     uint32_t rs[1];
     tmem_ld16x2_1<1>(tO + D, rs);
     tmem_wait_ld();
     reg_fence(rs, 1);
     const float l = __uint_as_float(rs[0]);
-    float l32 = a32[0] + a32[1];
-    l32 += __shfl_xor_sync(0xffffffffu, l32, 16);
+    float l32 = a32[0] + a32[1];  // fp32 sum of the unrounded P: the LSE
+    l32 += __shfl_xor_sync(0xffffffffu, l32, 16);  // the other half of the row
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
     const float inv_l = 1.0f / l;
     if (ch == 0) p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
@@ -558,20 +712,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
+    for (int i = 0; i < C::kKStages; ++i) {
       mbar_init(smem_u32(&bars->k_full[i]), 1);
       mbar_init(smem_u32(&bars->k_empty[i]), 1);
+    }
+    for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(smem_u32(&bars->v_full[i]), 1);
       mbar_init(smem_u32(&bars->v_empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->q_full), 1);
-    mbar_init(smem_u32(&bars->q_empty), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->q_full[i]), 1);
+      mbar_init(smem_u32(&bars->q_empty[i]), 1);
+    }
     mbar_init(smem_u32(&bars->p_full[0]), kSoftmaxThreads);
     mbar_init(smem_u32(&bars->p_full[1]), kSoftmaxThreads);
     mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->req), 1);
     for (int e = 0; e < 2; ++e) {
       mbar_init(smem_u32(&bars->tq_full[e]), 1);
-      mbar_init(smem_u32(&bars->tq_empty[e]), 1 + kSoftmaxThreads);
+      mbar_init(smem_u32(&bars->tq_empty[e]), 2 + kSoftmaxThreads);
     }
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -582,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   {  // bf16 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
     uint4* ones = reinterpret_cast<uint4*>(smem_raw + (base - raw) + C::kOnesOff);
-    for (int i = threadIdx.x; i < C::kStages * C::kBoxBytes / 16; i += kThreads)
+    for (int i = threadIdx.x; i < C::kVStages * C::kBoxBytes / 16; i += kThreads)
       ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -603,6 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
     else if (warp == kWarpMma)
       run_mma<D>(p, bars, tmem, base, abort_flag);
+    else if (warp == kWarpSched)
+      run_scheduler<D>(&tm_q, p, bars, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
     run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);

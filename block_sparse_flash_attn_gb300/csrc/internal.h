@@ -65,7 +65,10 @@ cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causa
                                 cudaStream_t stream);
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
-                                int* d_tile_order, int* d_empty_tiles, cudaStream_t stream);
+                                int* d_tile_order, int* d_empty_tiles, int nsm,
+                                cudaStream_t stream);
+// Heads per schedule chunk for S/128 = nb key blocks per head.
+int schedule_chunk_heads(int nb);
 
 // fwd_sm103.cu
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,

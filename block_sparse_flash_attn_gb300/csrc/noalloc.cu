@@ -139,7 +139,7 @@ extern "C" bsattn_status bsattn_fwd_noalloc(const void* q, const void* k, const 
   if (h_tot[0] < 0 || h_tot[0] > (long long)rows * nb || n_live < 0 || n_live > rows)
     return BSATTN_ERR_INTERNAL;
   e = plan_fill_and_order(d_mask, BH, nb, causal, row_ptr, live_off, col_idx, tile_order, empty,
-                          st);
+                          device_sm_count(dev), st);
   if (e != cudaSuccess) return from_cuda(e);
 
   const long long nrows = (long long)B * H * S;

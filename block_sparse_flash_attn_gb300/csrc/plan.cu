@@ -10,9 +10,10 @@
 //
 // Layout: row r = (b*H + h)*nb + qb; row_ptr[r]..row_ptr[r+1] index col_idx,
 // which lists kb ascending with mask != 0 (and kb <= qb when causal).
-// Schedule: non-empty tiles grouped by head in head order (so one head's K/V
-// stay resident in L2 while its tiles run), inside a head sorted by live
-// count descending then qb ascending (longest-processing-time first); empty
+// Schedule: non-empty tiles in chunks of consecutive heads (so a chunk's K/V
+// stay resident in L2 while its tiles run), inside a chunk sorted by live
+// count descending (longest-processing-time first), with the few tiles that
+// are long for their chunk moved one chunk earlier (see order_kernel); empty
 // tiles listed separately (the forward kernel writes O = 0, LSE = -inf there).
 #include <cstdint>
 
@@ -22,6 +23,9 @@ namespace bsattn {
 namespace {
 
 constexpr int kScanThreads = 1024;
+// Key blocks of K/V per schedule chunk: 768 blocks of 128 keys x D=128 bf16
+// K and V = 48 MB, well inside the 126 MB L2.
+constexpr int kChunkKeyBlocks = 768;
 
 __device__ __forceinline__ bool block_live(const uint8_t* mask_row, int kb, int qb, int causal) {
   return mask_row[kb] != 0 && (!causal || kb <= qb);
@@ -105,32 +109,68 @@ __global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, 
   }
 }
 
-// One block per head: sort the head's tiles by (live count desc, qb asc) with
-// a shared-memory bitonic sort, then split into the live and empty lists.
+// One block per chunk of `kh` consecutive heads (the heads whose K/V fill
+// about kChunkKeyBlocks key blocks, so that a chunk's K/V stay resident in L2
+// while its tiles run).  The chunk's tiles are sorted by live count
+// descending, ties by (head, qb) ascending (longest-processing-time first).
+// A tile of chunk k > 0 whose count exceeds half of chunk k's blocks per SM
+// (`nsm` SMs) is moved into chunk k-1: such a tile alone is about as long as
+// the chunk's whole share per SM, and at the end of the schedule it would
+// run long after every other SM has finished.  Chunk k's slice of tile_order
+// therefore holds its own short enough tiles plus the long tiles of chunk
+// k+1, and starts at (live tiles of chunks < k) + (tiles moved out of chunk
+// k).  Empty tiles are listed head by head, qb ascending.
 __global__ void __launch_bounds__(1024)
-    order_kernel(const int* __restrict__ row_ptr, const int* __restrict__ live_off, int nb,
-                 int* __restrict__ tile_order, int* __restrict__ empty_tiles) {
+    order_kernel(const int* __restrict__ row_ptr, const int* __restrict__ live_off, int BH, int nb,
+                 int kh, int nsm, int* __restrict__ tile_order, int* __restrict__ empty_tiles) {
   extern __shared__ uint32_t keys[];
-  const int bh = blockIdx.x;
+  __shared__ int n_in, n_moved;
+  const int k = blockIdx.x;
+  const int h0 = k * kh;
+  const int h1 = min(BH, h0 + kh);  // own heads [h0, h1)
+  const int h2 = min(BH, h1 + kh);  // next chunk's heads [h1, h2)
+  // a count above thr is "long" in its chunk
+  const long long thr_own =
+      (long long)(row_ptr[h1 * nb] - row_ptr[h0 * nb]) / (2ll * nsm);
+  const long long thr_next =
+      (h2 > h1) ? (long long)(row_ptr[h2 * nb] - row_ptr[h1 * nb]) / (2ll * nsm) : (1ll << 40);
+  const int own = (h1 - h0) * nb;
+  const int pool = (h2 - h0) * nb;
   int n2 = 1;
-  while (n2 < nb) n2 <<= 1;
-  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
-    if (i < nb) {
-      const int r = bh * nb + i;
-      const uint32_t cnt = (uint32_t)(row_ptr[r + 1] - row_ptr[r]);
-      keys[i] = (((uint32_t)nb - cnt) << 12) | (uint32_t)i;
-    } else {
-      keys[i] = 0xFFFFFFFFu;
-    }
+  while (n2 < pool) n2 <<= 1;
+  if (threadIdx.x == 0) {
+    n_in = 0;
+    n_moved = 0;
   }
   __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    uint32_t key = 0xFFFFFFFFu;
+    if (i < pool) {
+      const int r = h0 * nb + i;
+      const int cnt = row_ptr[r + 1] - row_ptr[r];
+      bool in;
+      if (i < own) {
+        const bool moved = k > 0 && cnt > thr_own;
+        if (moved && cnt > 0) atomicAdd(&n_moved, 1);
+        in = cnt > 0 && !moved;
+      } else {
+        in = cnt > 0 && cnt > thr_next;
+      }
+      if (in) {
+        key = ((uint32_t)(nb - cnt) << 14) | (uint32_t)i;  // i < 2^14: pool <= 2 * 4096
+        atomicAdd(&n_in, 1);
+      }
+    }
+    keys[i] = key;
+  }
+  __syncthreads();
+  for (int kk = 2; kk <= n2; kk <<= 1) {
+    for (int j = kk >> 1; j > 0; j >>= 1) {
       for (int i = threadIdx.x; i < n2; i += blockDim.x) {
         const int p = i ^ j;
         if (p > i) {
           const uint32_t a = keys[i], b = keys[p];
-          const bool up = (i & k) == 0;
+          const bool up = (i & kk) == 0;
           if ((a > b) == up) {
             keys[i] = b;
             keys[p] = a;
@@ -140,14 +180,21 @@ __global__ void __launch_bounds__(1024)
       __syncthreads();
     }
   }
-  const int live0 = live_off[bh];
-  const int nlive = live_off[bh + 1] - live0;
-  const int empty0 = bh * nb - live0;
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-    const int qb = (int)(keys[i] & 0xFFFu);
-    const int tile = bh * nb + qb;
-    if (i < nlive) tile_order[live0 + i] = tile;
-    else empty_tiles[empty0 + (i - nlive)] = tile;
+  const int start = live_off[h0] + n_moved;
+  for (int i = threadIdx.x; i < n_in; i += blockDim.x)
+    tile_order[start + i] = h0 * nb + (int)(keys[i] & 0x3FFFu);
+  // empty tiles: one warp per own head, qb ascending
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int h = h0 + warp; h < h1; h += blockDim.x >> 5) {
+    int pos = h * nb - live_off[h];
+    for (int q0 = 0; q0 < nb; q0 += 32) {
+      const int qb = q0 + lane;
+      const int r = h * nb + qb;
+      const bool empty = qb < nb && row_ptr[r + 1] == row_ptr[r];
+      const unsigned bal = __ballot_sync(0xffffffffu, empty);
+      if (empty) empty_tiles[pos + __popc(bal & ((1u << lane) - 1u))] = r;
+      pos += __popc(bal);
+    }
   }
 }
 
@@ -169,18 +216,23 @@ cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causa
   return cudaGetLastError();
 }
 
+int schedule_chunk_heads(int nb) { return nb >= kChunkKeyBlocks ? 1 : kChunkKeyBlocks / nb; }
+
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
-                                int* d_tile_order, int* d_empty_tiles, cudaStream_t stream) {
+                                int* d_tile_order, int* d_empty_tiles, int nsm,
+                                cudaStream_t stream) {
   const int rows = BH * nb;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
   fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, d_row_ptr,
                                                          d_col_idx);
+  const int kh = schedule_chunk_heads(nb);
+  const int chunks = (BH + kh - 1) / kh;
   int n2 = 1;
-  while (n2 < nb) n2 <<= 1;
-  order_kernel<<<BH, 1024, sizeof(uint32_t) * n2, stream>>>(d_row_ptr, d_live_off, nb,
-                                                            d_tile_order, d_empty_tiles);
+  while (n2 < 2 * kh * nb) n2 <<= 1;
+  order_kernel<<<chunks, 1024, sizeof(uint32_t) * n2, stream>>>(
+      d_row_ptr, d_live_off, BH, nb, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles);
   return cudaGetLastError();
 }
 

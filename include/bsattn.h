@@ -72,8 +72,12 @@ enum {
  * The plan is the compressed-sparse-row list of live key blocks of every
  * query tile (row r = (b*H + h)*(S/128) + qb; col_idx ascending; under
  * BSATTN_CAUSAL only kb <= qb is kept) and a schedule: the non-empty tiles
- * ordered head-major, most live blocks first inside each head, and the list
- * of empty tiles.  Built on the device by kernels on `stream`.  This is the
+ * in chunks of C = max(1, 768 / (S/128)) consecutive heads (b*H + h order),
+ * most live blocks first inside a chunk (ties: head, then qb ascending),
+ * except that a tile of chunk k > 0 with more live blocks than
+ * (live blocks of chunk k) / (2 * number of SMs of the current device) is
+ * listed in chunk k-1; and the list of empty tiles (head by head, qb
+ * ascending).  Built on the device by kernels on `stream`.  This is the
  * only call that synchronises: it waits for `stream` once to learn the number
  * of live blocks before allocating.
  *

@@ -66,12 +66,31 @@ def _check_plan(bs, mask, causal):
     live = np.flatnonzero(counts > 0)
     assert np.array_equal(np.sort(order), live)
     assert np.array_equal(np.sort(empty), np.flatnonzero(counts == 0))
-    heads = order // nb
-    assert np.all(np.diff(heads) >= 0), "schedule must be head-major"
-    for h in np.unique(heads):
-        c = counts[order[heads == h]]
-        assert np.all(np.diff(c) <= 0), "longest tiles first inside a head"
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    assert np.array_equal(order, _expected_schedule(counts, B * H, nb, nsm))
+    assert np.array_equal(empty, np.flatnonzero(counts == 0)), "empty tiles head by head, qb asc"
     p.close()
+
+
+def _expected_schedule(counts, BH, nb, nsm):
+    """The documented tile order, restated with plain loops: chunks of
+    max(1, 768 // nb) heads, longest first inside a chunk (ties by tile id),
+    tiles long for their chunk (count > chunk blocks // (2 * nsm)) moved one
+    chunk earlier."""
+    kh = max(1, 768 // nb)
+    c = counts.reshape(BH, nb)
+    keys = []
+    for h in range(BH):
+        k = h // kh
+        thr = int(c[k * kh:(k + 1) * kh].sum()) // (2 * nsm)
+        for qb in range(nb):
+            n = int(c[h, qb])
+            if n == 0:
+                continue
+            kk = k - 1 if (k > 0 and n > thr) else k
+            keys.append((kk, -n, h * nb + qb))
+    keys.sort()
+    return np.asarray([t for _, _, t in keys], dtype=np.int64)
 
 
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
