@@ -50,7 +50,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the current forward kernel, from the ncu capture summarised in
 # profiles/bsattn_fwd_kernel-causal-s4096-d128.md; workloads not captured: None.
-TRAFFIC_BYTES = {"w2_bf16": 201_555_200 + 50_130_432}
+TRAFFIC_BYTES = {}
 
 
 def parse_args(argv=None):

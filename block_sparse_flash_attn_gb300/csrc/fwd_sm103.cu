@@ -11,55 +11,49 @@
 // Dead key blocks are never loaded (the mask's purpose in "Writing the Kernel
 // Logic": only the small 128x128 block is ever materialised).
 //
-// GB300 design (one persistent CTA per SM, 384 threads = 3 warpgroups, one
+// GB300 design (one persistent CTA per SM, 512 threads = 4 warpgroups, one
 // query tile in the softmax at a time):
 //   warps 0-7  softmax + epilogue.  Each warp covers 16 query rows (TMEM
 //              lanes); lanes 0..15 own key columns 0..63 of every block (O
 //              columns [0, D/2)), lanes 16..31 the same rows' columns 64..127
 //              (O columns [D/2, D)); tcgen05 16x32bx2 accesses put both halves
 //              of a row in one warp, so row max and sums combine by shuffle.
-//   warp  8    TMA producer (elected lane)
-//   warp  9    tcgen05 MMA issuer (elected lane) and tensor-memory owner
+//   warp  8    TMA producer of K and V (elected lane)
+//   warp  9    tcgen05 issuer of S = Q K^T (elected lane), tensor-memory owner
 //   warp  10   tile scheduler: claims the next tile when the producer asks
 //              for it (a few blocks before the current tile's end),
 //              publishes it (CSR range and first key blocks) in a 2-slot
 //              queue and loads its Q (elected lane)
-//   warp  11   idle (completes warpgroup 2 for setmaxnreg)
-// Tensor memory (512 columns allocated): two score buffers S[0] = [0,128),
-// S[1] = [128,256) and the fp32 output accumulator O = [256, 256+D) followed
-// by 16 columns holding the row sum of the rounded P (the PV MMA multiplies
-// P by [V | ones]).  Block g
-// (counted over the CTA's whole run) uses S[g % 2]; its bf16 probabilities P
-// overwrite the scores already read (keys 0..63 -> columns 0..31, keys
-// 64..127 -> columns 64..95).  With two score buffers the MMA warp computes
-// S(j+1) while the softmax works on block j, and issues S(j+2) into block j's
-// buffer right after O += P(j) V(j), so neither side waits for the other in
-// steady state.  Shared memory: Q buffers and rings of K and V tiles
-// (128 x D bf16 each, 128-byte swizzled by TMA, read by tcgen05.mma through
-// matrix descriptors) plus one 16 KB tile of bf16 ones per V stage: at
-// D = 128 one Q, three K and two V stages (224 KB), at D = 64 two Q and four
-// stages per ring.  A tile's TMA load takes about as long as one block's
-// MMAs, so a third K stage gives each K load a block's time of slack.
+//   warp  12   tcgen05 issuer of O += P V (elected lane)
+//   warps 11, 13-15 idle (complete warpgroups 2 and 3 for setmaxnreg)
+// Tensor memory (512 columns allocated): three score buffers S[0] = [0,128),
+// S[1] = [128,256), S[2] = [256,384) and the fp32 output accumulator
+// O = [384, 384+D) (at D = 64 followed by 16 columns of the rounded row sum,
+// see Cfg::kOnes).  Block g (counted over the CTA's whole run) uses
+// S[g % 3]; its bf16 probabilities P overwrite the scores already read
+// (keys 0..63 -> columns 0..31, keys 64..127 -> columns 64..95).  S(g+3) goes
+// into block g's buffer once O += P(g) V(g) is complete, so the scores of
+// the next blocks are computed while the softmax works on block g: the chain
+// softmax -> PV -> next S spans three blocks and hides behind the tensor
+// core's own work.  Shared memory: Q buffers and 3-stage rings of K and V
+// tiles (128 x D bf16 each, 128-byte swizzled by TMA, read by tcgen05.mma
+// through matrix descriptors): at D = 128 one Q (224 KB), at D = 64 two.
 //
-// The producer sees the CTA's tiles as one stream of key blocks g = 0, 1,
-// 2, ... (every live block of every tile the CTA claimed, tile after tile)
-// and loads K two blocks ahead of V along it, so the next tile's first K
-// tiles arrive while the current tile runs; the scheduler warp loads the
-// next tile's Q as soon as the Q buffer is free.  Per tile with n live key
-// blocks the MMA warp issues
-//   S(0), S(1); then for j = 0..n-1: [P(j) in] O (+)= P(j) V(j); S(j+2)
-// (S(j+2) only while j+2 < n), and goes straight on to the next tile's
-// S(0), S(1) after the last PV.  The commit after S(g) frees K(g)'s ring
-// stage and is the softmax's "S(g) ready" signal; the commit after PV(g)
-// frees V(g)'s stage and is "PV(g) done", which the softmax waits for only
-// before an O rescale and, for the tile's last block, before the epilogue
-// (which therefore always precedes the next tile's first PV, the one that
-// overwrites O).  Online softmax in base 2 with lazy rescale: the running
-// max m only moves when a block's max exceeds it by more than 8 (log2
-// units), so P <= 256 and the O rescale is rare.  O is normalised by the
-// row sum of the bf16-rounded P that multiplied V (so the weights on V sum
-// to one even when a single key dominates a row); the LSE uses the fp32 sum
-// of the unrounded P.
+// The producer sees the CTA's tiles as one stream of key blocks and loads K
+// two blocks ahead of V along it; the scheduler warp loads each tile's Q as
+// soon as the Q buffer is free.  Along the same stream one MMA warp issues
+// S(g) as soon as K(g) is loaded and PV(g-3) is complete, another issues
+// PV(g) as soon as P(g) is written and V(g) loaded; a tile's first PV starts
+// a fresh O.  The commit after S(g) frees K(g)'s ring stage and is the
+// softmax's "S(g) ready" signal; the commit after PV(g) frees V(g)'s stage
+// and is "PV(g) done", which the softmax waits for only before an O rescale
+// and, for the tile's last block, before the epilogue (which therefore
+// always precedes the next tile's first PV, the one that overwrites O).
+// Online softmax in base 2 with lazy rescale: the running max m only moves
+// when a block's max exceeds it by more than 8 (log2 units), so P <= 256 and
+// the O rescale is rare.  O is normalised by the row sum of the bf16-rounded
+// P that multiplied V (so the weights on V sum to one even when a single key
+// dominates a row); the LSE uses the fp32 sum of the unrounded P.
 //
 // Every wait is bounded (globaltimer); on expiry the kernel records a timeout
 // in the status word, every role leaves its loop, outstanding TMA loads and
@@ -73,21 +67,31 @@
 namespace bsattn {
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
 constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpMmaS = 9;  // also allocates and frees tensor memory
 constexpr int kWarpSched = 10;
+constexpr int kWarpMmaPV = 12;
 // The producer asks for the next tile when its K cursor has this many blocks
 // of the current tile left: claiming a tile (four dependent global reads)
 // and loading its Q take about as long as this many blocks' MMAs.
 constexpr int kClaimAhead = 4;
-// Launch budget 384 x 168 registers; the producer/MMA warpgroup hands part of
-// its share to the two softmax warpgroups: 256 x 208 + 128 x 88 = 384 x 168.
+// Launch budget 512 x 128 registers; the two role warpgroups hand part of
+// their share to the two softmax warpgroups: 256 x 208 + 256 x 48 = 512 x 128.
 constexpr int kRegsSoftmax = 208;
-constexpr int kRegsOther = 88;
+constexpr int kRegsOther = 48;
 constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 512;
+// Tensor-memory columns: three score buffers S[0..2] (128 each; the bf16 P
+// of a block overwrites its scores) and the output accumulator O (D).
+constexpr int kSBufs = 3;
+constexpr uint32_t kTmemS = 0;
+constexpr uint32_t kTmemO = 384;
+static_assert(kTmemS + kSBufs * 128 <= kTmemO && kTmemO + 128 <= kTmemCols &&
+                  kTmemO + 64 + 16 <= kTmemCols,
+              "tensor memory columns");
 constexpr unsigned long long kDrainNs = 200ull * 1000 * 1000;
 
 template <int D>
@@ -95,31 +99,34 @@ struct Cfg {
   static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
   static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
-  // Ring depths and Q buffers, each filling 224 KB: D = 128 has one Q tile,
-  // three K stages and two V stages (each V stage with its ones tile);
-  // D = 64 two Q tiles and four stages of each ring.
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
+  // Ring depths and Q buffers: D = 128 fills 224 KB with one Q tile and
+  // three stages of each ring; D = 64 has two Q tiles and three stages.
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 3;
   static constexpr int kQStages = D == 128 ? 1 : 2;
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQStages * kTileBytes;
-  // V region: the PV MMA's B operand is [V | ones]: N = D + 16, its 64-wide
-  // column groups kVGroup bytes apart.  Group c of stage s sits at
-  // kVOff + c * kVGroup + s * kBoxBytes; the last group is a tile of bf16
-  // ones, so the tensor core also accumulates the row sum of the rounded P
-  // into O columns D..D+15.
+  // V region: the PV MMA's B operand (MN-major) has its 64-wide column
+  // groups kVGroup bytes apart: group c of stage s sits at
+  // kVOff + c * kVGroup + s * kBoxBytes.
   static constexpr int kVGroup = kVStages * kBoxBytes;
   static constexpr int kVOff = kKOff + kKStages * kTileBytes;
-  static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;  // ones tiles, one per V stage
-  static constexpr int kBarOff = kOnesOff + kVStages * kBoxBytes;
+  // Row sum of the rounded P (the O denominator): at D = 64 the tensor core
+  // accumulates it next to O, the PV MMA multiplying P by [V | ones] (N =
+  // D + 16; the ones tile of each V stage sits one column group after the
+  // stage's V, at kOnesOff + s * kBoxBytes); at D = 128 the 16 extra tensor-
+  // memory columns are not free, and the softmax threads add it up.
+  static constexpr bool kOnes = D == 64;
+  static constexpr int kPvN = kOnes ? D + 16 : D;
+  static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;
+  static constexpr int kBarOff = kOnesOff + (kOnes ? kVStages * kBoxBytes : 0);
   static constexpr int kSmem = kBarOff + 1024;
-  static constexpr int kPvN = D + 16;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, kPvN, true);
 };
 
 constexpr int kSlotCols = 32;  // key blocks of a tile published with it
-constexpr int kMaxStages = 4;  // deepest K / V ring of any Cfg
+constexpr int kMaxStages = 3;  // deepest K / V ring of any Cfg
 
 // One scheduled tile as the scheduler warp publishes it to the producer, MMA
 // and softmax warps.
@@ -141,7 +148,7 @@ struct __align__(16) Bars {
   uint64_t p_full[2];   // all softmax threads wrote P(g) (indexed by g % 2)
   uint64_t tq_full[2];  // tile queue slot published
   uint64_t tq_empty[2]; // slot read by producer, MMA warp and every softmax thread
-  uint64_t drain;
+  uint64_t drain[2];    // all MMAs of the S / the PV issuer complete
   uint64_t req;         // the producer asks for the next tile (once per tile)
   TileInfo tq[2];
   uint32_t tmem_base;
@@ -396,82 +403,29 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 }
 
 // ---------------------------------------------------------------------------
-// warp 9: tcgen05 MMA issue (elected lane)
+// warps 9 and 12: tcgen05 MMA issue, one warp per product (elected lane)
 // ---------------------------------------------------------------------------
+// tcgen05.mma issue returns only about when the tensor core has taken the
+// instruction, so a single issuing thread that also waits on barriers leaves
+// the tensor core idle during every wait.  Two warps issue instead, one per
+// product, each waiting only on its own operands, so while one waits the
+// other keeps the tensor core busy.  Each warp's commits track only its own
+// MMAs.
+//
+// S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
+// swizzle row; a new 64-column box every 4 steps).  S(g) goes into S[g % 3]
+// once K(g) is loaded and PV(g-3), which read P(g-3) out of that buffer, is
+// complete; its commit frees the K stage and tells the softmax that S(g) is
+// ready.  A negative scale is applied as -Q (instruction-descriptor negate
+// bit) so the softmax always sees a non-negative multiplier.  After a tile's
+// last S the Q buffer is released.
 template <int D>
-__device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
-                        volatile int* abort_flag) {
+__device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
+                          volatile int* abort_flag) {
   using C = Cfg<D>;
   const uint64_t lim = p.timeout_ns;
-  // S = Q K^T : M=128, N=128, K=D in steps of 16 (32 bytes inside a 128-byte
-  // swizzle row; a new 64-column box every 4 steps).  A negative scale is
-  // applied as -Q (instruction-descriptor negate bit) so the softmax always
-  // sees a non-negative multiplier.
   const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
-  int kc = 0, vc = 0, qc = 0, tqc = 0;  // S issued, PV issued, tiles' Q used, tiles taken
-
-  auto commit = [&](uint32_t bar) {
-    if (elect_one()) mma_commit(bar);
-    __syncwarp();
-  };
-  // S(g) into S[g % 2] from K ring stage g % kKStages; its commit frees the
-  // stage and tells the softmax that S(g) is ready.
-  auto do_s = [&](uint32_t qaddr) -> bool {
-    const int st = kc % C::kKStages;
-    if (!wait_warp(smem_u32(&bars->k_full[st]), (uint32_t)(kc / C::kKStages) & 1u, abort_flag,
-                   p.status, lim))
-      return false;
-    const uint32_t kaddr = smem_base + C::kKOff + st * C::kTileBytes;
-    if (elect_one()) {
-      // descriptors advance by adding the byte offset >> 4 to the start-address field
-      const uint64_t qd = smem_desc_sw128(qaddr, 16, 1024);
-      const uint64_t kd = smem_desc_sw128(kaddr, 16, 1024);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + (kc & 1) * 128, qd + off, kd + off, idesc_s, kk > 0 ? 1u : 0u);
-      }
-      mma_commit(smem_u32(&bars->k_empty[st]));
-    }
-    __syncwarp();
-    ++kc;
-    return true;
-  };
-  // [O | l] (+)= P [V | 1] : M=128, N=D+16, K=128 keys in steps of 16.  P(g)
-  // is read from S[g % 2] (bf16 pairs, 8 columns per step; keys 0..63 at
-  // columns 0..31, keys 64..127 at columns 64..95); B is MN-major (D
-  // contiguous): 8-key groups 1024 bytes apart, 64-wide column groups
-  // kVGroup apart, the last group being the stage's ones tile.
-  auto do_pv = [&](bool accumulate) -> bool {
-    // P(g) in, g = vc: two barriers so that P(g+1) can never be mistaken for P(g)
-    if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
-                   p.status, lim))
-      return false;
-    const int st = vc % C::kVStages;
-    if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kVStages) & 1u, abort_flag,
-                   p.status, lim))
-      return false;
-    tc_fence_after();
-    const uint32_t vaddr = smem_base + C::kVOff + st * C::kBoxBytes;
-    const uint32_t pbuf = tmem + (vc % 2) * 128;  // block g's score buffer (g = vc)
-    if (elect_one()) {
-      const uint64_t vd = smem_desc_sw128(vaddr, C::kVGroup, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
-        mma_ts(tmem + 256, pbuf + pcol, vd + (uint32_t)(kk * 2048 >> 4), C::kIdescO,
-               (accumulate || kk > 0) ? 1u : 0u);
-      }
-      mma_commit(smem_u32(&bars->v_empty[st]));
-    }
-    __syncwarp();
-    ++vc;
-    return true;
-  };
-  // Per tile: S(0), S(1); then for j = 0..n-1: PV(j), S(j+2) while j+2 < n.
-  // The next tile's S(0) and S(1) follow the tile's last PV, so that PV (the
-  // one the softmax's epilogue waits for) never queues behind them; its Q
-  // and first K tiles are normally loaded long before.
+  int kc = 0, qc = 0, tqc = 0;  // S issued, tiles' Q used, tiles taken
   bool ok = true;
   while (ok) {
     int t = 0, r0 = 0, n = 0, col = 0;
@@ -479,25 +433,100 @@ __device__ void run_mma(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t 
     ++tqc;
     if (t < 0) break;
     const int qs = qc % C::kQStages;
-    if (!wait_warp(smem_u32(&bars->q_full[qs]), (uint32_t)(qc / C::kQStages) & 1u, abort_flag, p.status,
-                   lim))
+    if (!wait_warp(smem_u32(&bars->q_full[qs]), (uint32_t)(qc / C::kQStages) & 1u, abort_flag,
+                   p.status, lim))
       break;
     ++qc;
-    const uint32_t qaddr = smem_base + C::kQOff + qs * C::kTileBytes;
-    ok = do_s(qaddr);
-    if (ok && n > 1) ok = do_s(qaddr);
-    if (ok && n <= 2) commit(smem_u32(&bars->q_empty[qs]));  // the tile's last S: Q free
-    for (int j = 0; ok && j < n; ++j) {
-      ok = do_pv(j > 0);
-      if (ok && j + 2 < n) {
-        ok = do_s(qaddr);
-        if (ok && j + 2 == n - 1) commit(smem_u32(&bars->q_empty[qs]));
+    const uint64_t qd = smem_desc_sw128(smem_base + C::kQOff + qs * C::kTileBytes, 16, 1024);
+    for (int j = 0; j < n; ++j) {
+      if (kc >= kSBufs) {  // PV(kc-3) complete: S[kc % 3] holds nothing needed any more
+        const int pv = kc - kSBufs;
+        if (!wait_warp(smem_u32(&bars->v_empty[pv % C::kVStages]),
+                       (uint32_t)(pv / C::kVStages) & 1u, abort_flag, p.status, lim)) {
+          ok = false;
+          break;
+        }
       }
+      const int st = kc % C::kKStages;
+      if (!wait_warp(smem_u32(&bars->k_full[st]), (uint32_t)(kc / C::kKStages) & 1u, abort_flag,
+                     p.status, lim)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        // descriptors advance by adding the byte offset >> 4 to the start-address field
+        const uint64_t kd = smem_desc_sw128(smem_base + C::kKOff + st * C::kTileBytes, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + kTmemS + (kc % kSBufs) * 128, qd + off, kd + off, idesc_s,
+                 kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->k_empty[st]));
+        if (j == n - 1) mma_commit(smem_u32(&bars->q_empty[qs]));  // the tile's last S: Q free
+      }
+      __syncwarp();
+      ++kc;
     }
   }
-  // Every MMA issued so far must finish before TMEM is released.
-  commit(smem_u32(&bars->drain));
-  wait_drain(smem_u32(&bars->drain), 0);
+  // Every MMA issued here must finish before TMEM is released.
+  if (elect_one()) mma_commit(smem_u32(&bars->drain[0]));
+  __syncwarp();
+  wait_drain(smem_u32(&bars->drain[0]), 0);
+}
+
+// O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P(g) is read from
+// S[g % 3] (bf16 pairs, 8 columns per step; keys 0..63 at columns 0..31,
+// keys 64..127 at columns 64..95); B is MN-major (D contiguous): 8-key
+// groups 1024 bytes apart, 64-wide column groups kVGroup apart.  A tile's
+// first PV starts a fresh O.  The commit frees V's ring stage and tells the
+// softmax and the S issuer that PV(g) is done.
+template <int D>
+__device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
+                           volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const uint64_t lim = p.timeout_ns;
+  int vc = 0, tqc = 0;  // PV issued, tiles taken
+  bool ok = true;
+  while (ok) {
+    int t = 0, r0 = 0, n = 0, col = 0;
+    if (!take_tile(bars, tqc, p, abort_flag, t, r0, n, col)) break;
+    ++tqc;
+    if (t < 0) break;
+    for (int j = 0; j < n; ++j) {
+      // two P barriers so that P(g+1) can never be mistaken for P(g)
+      if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
+                     p.status, lim)) {
+        ok = false;
+        break;
+      }
+      const int st = vc % C::kVStages;
+      if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kVStages) & 1u, abort_flag,
+                     p.status, lim)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t vd = smem_desc_sw128(smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
+                                            1024);
+        const uint32_t pbuf = tmem + kTmemS + (vc % kSBufs) * 128;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // keys 16kk .. 16kk+15
+          mma_ts(tmem + kTmemO, pbuf + pcol, vd + (uint32_t)(kk * 2048 >> 4), C::kIdescO,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->v_empty[st]));
+      }
+      __syncwarp();
+      ++vc;
+    }
+  }
+  if (elect_one()) mma_commit(smem_u32(&bars->drain[1]));
+  __syncwarp();
+  wait_drain(smem_u32(&bars->drain[1]), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -521,12 +550,14 @@ __device__ void write_empty_tiles(const FwdParams& p) {
 }
 
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
-// pairs into pr[] (the A operand of the PV product); accumulates the fp32
-// row sum of the unrounded p (for the LSE) in two independent accumulators.
-// The sum of the rounded values (the O denominator) is accumulated by the
-// tensor core next to O.
+// pairs into pr[] (the A operand of the PV product).  Accumulates the row sum
+// a32 of the fp32 p (for the LSE) and, when ROUNDED, r32 of the bf16-rounded
+// p that multiply V (the O denominator, so that the weights on V sum to one
+// even when a single key dominates a row), each in two independent
+// accumulators.
+template <bool ROUNDED>
 __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
-                                              float nm, float (&a32)[2]) {
+                                              float nm, float (&a32)[2], float (&r32)[2]) {
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     float x0, x1;
@@ -535,6 +566,7 @@ __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, 
     const float p1 = ex2_approx(x1);
     pr[q] = pack_bf16x2(p0, p1);
     add2(a32[0], a32[1], a32[0], a32[1], p0, p1);
+    if (ROUNDED) add_bf16x2_f32(r32[0], r32[1], pr[q]);
   }
 }
 
@@ -565,7 +597,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
   // 16x32bx2 accesses: lanes 0..15 of the warp take the address's columns,
   // lanes 16..31 the same rows 64 (or DH) columns further on.
   const uint32_t lane_off = (uint32_t)(sub * 32 + lh * 16) << 16;
-  const uint32_t tO = tmem + 256 + lane_off;
+  const uint32_t tO = tmem + kTmemO + lane_off;
   const float sl = p.scale_log2;       // > 0 (see FwdParams)
   const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
@@ -581,22 +613,24 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int t = slot[0];
     const int n = slot[2];
     const int diag_last = slot[3];
-    mbar_arrive(smem_u32(&bars->tq_empty[e]));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars->tq_empty[e]));
     ++tq_cnt;
     if (t < 0) return;
     const int bh = t / p.nb;
     const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
-    float a32[2] = {0.f, 0.f};  // partial fp32 row sums of this half row
+    float a32[2] = {0.f, 0.f};  // partial sums of this half row: fp32 p
+    float r32[2] = {0.f, 0.f};  // and bf16-rounded p
     for (int jb = 0; jb < n; ++jb, ++g) {
-      const int b = g & 1;  // S buffer of this block
+      const int b = g & 1;  // P barrier of this block
       // S(g) ready = its commit released K(g)'s stage
       if (!wait_warp(smem_u32(&bars->k_empty[g % C::kKStages]), (uint32_t)(g / C::kKStages) & 1u,
                      abort_flag, p.status, lim))
         return;
       tc_fence_after();
-      const uint32_t tS = tmem + b * 128 + lane_off;
+      const uint32_t tS = tmem + kTmemS + (g % kSBufs) * 128 + lane_off;  // S buffer of this block
       uint32_t sr[64];
       tmem_ld16x2_32<64>(tS + 0, sr + 0);
       tmem_ld16x2_32<64>(tS + 32, sr + 32);
@@ -617,9 +651,11 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         m = xm;
         a32[0] *= f;
         a32[1] *= f;
+        r32[0] *= f;
+        r32[1] *= f;
       }
       uint32_t pr[32];
-      softmax_exp64(sr, pr, sl, -m, a32);
+      softmax_exp64<!C::kOnes>(sr, pr, sl, -m, a32, r32);
       tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
 
       // O rescale (this thread's columns) when a row's max moved: first wait
@@ -639,16 +675,19 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
           for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * f);
           tmem_st16x2_32<DH>(tO + c0, orr);
         }
-        uint32_t rs[1];  // the row-sum column this thread reads at the end scales with O
-        tmem_ld16x2_1<1>(tO + D, rs);
-        tmem_wait_ld();
-        reg_fence(rs, 1);
-        rs[0] = __float_as_uint(__uint_as_float(rs[0]) * f);
-        tmem_st16x2_1<1>(tO + D, rs);
+        if constexpr (C::kOnes) {  // the row-sum column read at the end scales with O
+          uint32_t rs[1];
+          tmem_ld16x2_1<1>(tO + D, rs);
+          tmem_wait_ld();
+          reg_fence(rs, 1);
+          rs[0] = __float_as_uint(__uint_as_float(rs[0]) * f);
+          tmem_st16x2_1<1>(tO + D, rs);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[b]));
+      __syncwarp();  // the warp's stores of P(g) are complete (each lane waited for its own)
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[b]));
     }
 
     // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
@@ -656,14 +695,19 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                    (uint32_t)((g - 1) / C::kVStages) & 1u, abort_flag, p.status, lim))
       return;  // the tile's last PV has landed in O
     tc_fence_after();
-    // sum of the rounded P accumulated by the tensor core in O column D
-    // (lanes 16..31 read the identical column D+1): the O denominator, so
-    // that the weights applied to V sum to one
-    uint32_t rs[1];
-    tmem_ld16x2_1<1>(tO + D, rs);
-    tmem_wait_ld();
-    reg_fence(rs, 1);
-    const float l = __uint_as_float(rs[0]);
+    float l;  // sum of the rounded P: the O denominator
+    if constexpr (C::kOnes) {
+      // accumulated by the tensor core in O column D (lanes 16..31 read the
+      // identical column D+1)
+      uint32_t rs[1];
+      tmem_ld16x2_1<1>(tO + D, rs);
+      tmem_wait_ld();
+      reg_fence(rs, 1);
+      l = __uint_as_float(rs[0]);
+    } else {
+      l = r32[0] + r32[1];
+      l += __shfl_xor_sync(0xffffffffu, l, 16);  // the other half of the row
+    }
     float l32 = a32[0] + a32[1];  // fp32 sum of the unrounded P: the LSE
     l32 += __shfl_xor_sync(0xffffffffu, l32, 16);  // the other half of the row
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
@@ -724,22 +768,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->q_full[i]), 1);
       mbar_init(smem_u32(&bars->q_empty[i]), 1);
     }
-    mbar_init(smem_u32(&bars->p_full[0]), kSoftmaxThreads);
-    mbar_init(smem_u32(&bars->p_full[1]), kSoftmaxThreads);
-    mbar_init(smem_u32(&bars->drain), 1);
+    // the softmax warps arrive once per warp (elected lane, after __syncwarp)
+    mbar_init(smem_u32(&bars->p_full[0]), kSoftmaxWarps);
+    mbar_init(smem_u32(&bars->p_full[1]), kSoftmaxWarps);
+    mbar_init(smem_u32(&bars->drain[0]), 1);
+    mbar_init(smem_u32(&bars->drain[1]), 1);
     mbar_init(smem_u32(&bars->req), 1);
     for (int e = 0; e < 2; ++e) {
       mbar_init(smem_u32(&bars->tq_full[e]), 1);
-      mbar_init(smem_u32(&bars->tq_empty[e]), 2 + kSoftmaxThreads);
+      mbar_init(smem_u32(&bars->tq_empty[e]), 3 + kSoftmaxWarps);
     }
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpMmaS) {
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  {  // bf16 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
+  if constexpr (C::kOnes) {  // bf16 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
     uint4* ones = reinterpret_cast<uint4*>(smem_raw + (base - raw) + C::kOnesOff);
     for (int i = threadIdx.x; i < C::kVStages * C::kBoxBytes / 16; i += kThreads)
       ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
@@ -760,8 +806,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<kRegsOther>();
     if (warp == kWarpLoad)
       run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
-    else if (warp == kWarpMma)
-      run_mma<D>(p, bars, tmem, base, abort_flag);
+    else if (warp == kWarpMmaS)
+      run_mma_s<D>(p, bars, tmem, base, abort_flag);
+    else if (warp == kWarpMmaPV)
+      run_mma_pv<D>(p, bars, tmem, base, abort_flag);
     else if (warp == kWarpSched)
       run_scheduler<D>(&tm_q, p, bars, base, abort_flag);
   } else {
@@ -772,7 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpMmaS) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -356,6 +356,15 @@ __device__ __forceinline__ void exp2_poly2(float& y0, float& y1, float x0, float
 }
 
 // Pack two floats to bf16x2 with round-to-nearest-even: `lo` in bits 0..15.
+// d0 += low bf16 of `pair`, d1 += high bf16 of `pair` (exact widening, one
+// fp32 rounding each): mixed-precision add, no separate conversion.
+__device__ __forceinline__ void add_bf16x2_f32(float& d0, float& d1, uint32_t pair) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(pair));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
