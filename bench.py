@@ -50,7 +50,7 @@ L2_FLUSH_BYTES = 512 << 20
 # DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the current forward kernel, from the ncu capture summarised in
 # profiles/bsattn_fwd_kernel-causal-s4096-d128.md; workloads not captured: None.
-TRAFFIC_BYTES = {}
+TRAFFIC_BYTES = {"w2_bf16": 309_350_400 + 46_678_784}
 
 
 def parse_args(argv=None):
