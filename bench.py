@@ -7,9 +7,11 @@ Prints ONE JSON line (rank 0):
            full), with its fraction of the bf16 dense tensor peak
   value    whole-job throughput with inputs resident in HBM: sum over ranks of
            live flop / max over ranks of the mean per-step kernel time
-  e2e      the same metric through the public API with host buffers: each
-           step copies Q, K, V from pinned host memory to the device, runs the
-           forward and copies O and LSE back, all inside the timed region
+  e2e      the same metric through the public API with host buffers
+           (HostPipeline): each step copies Q, K, V from pinned host memory to
+           the device, runs the forward and copies O and LSE back, all inside
+           the timed region; the copies of one piece of the (batch, head)
+           range overlap the forward of another
   roofline the forward kernel against the tensor-core peak: achieved =
            live flop per launch / average launch time (CUDA events on the
            launching stream)
@@ -46,6 +48,11 @@ UNIT = "TFLOP/s"
 FALLBACK_BF16_TFLOPS = 1900.0   # profiling recipe's fallback (GB300, burst)
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+# The host-buffer path overlaps pieces of the (batch, head) range: about
+# 24 MB of Q, K, V per piece (the upload, ~210 GB/s on the host link, bounds
+# the step; smaller pieces shorten the last piece's compute and download).
+E2E_PIECE_BYTES = 24 << 20
+E2E_MAX_PIECES = 8  # each piece costs a plan, a launch and five copies of host time
 
 # DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the current forward kernel, from the ncu capture summarised in
@@ -271,7 +278,8 @@ def run_ours(args):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
     q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
-    plan = bsattn.plan(torch.from_numpy(mask).to(dev), causal=w.causal, out_f32=args.out_f32)
+    mask_d = torch.from_numpy(mask).to(dev)
+    plan = bsattn.plan(mask_d, causal=w.causal, out_f32=args.out_f32)
     o, lse = bsattn.fwd(q, k, v, plan, w.scale)
     bsattn.plan_status(plan)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -314,22 +322,26 @@ def run_ours(args):
     h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
+    # the public host-buffer path: per piece of the (batch, head) range, the
+    # upload, the forward and the download run on their own streams, overlapped
+    pieces = min(w.B * w.H, E2E_MAX_PIECES, max(4, -(-h2d // E2E_PIECE_BYTES)))
+    pipe = bsattn.HostPipeline(mask_d, w.D, causal=w.causal, out_f32=args.out_f32,
+                               chunks=pieces)
+
     def e2e_step():
-        dq = hq.to(dev, non_blocking=True)
-        dk = hk.to(dev, non_blocking=True)
-        dv = hv.to(dev, non_blocking=True)
-        oo, ll = bsattn.fwd(dq, dk, dv, plan, w.scale)
-        ho.copy_(oo, non_blocking=True)
-        hl.copy_(ll, non_blocking=True)
+        pipe.run(hq, hk, hv, ho, hl, w.scale, stream=stream)
 
     e2e_step()
     torch.cuda.synchronize()
+    pipe.status()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
+    pipe.status()
+    pipe.close()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
     e2e_value = whole_job_tflops(flop, world, e2e_ms)
 

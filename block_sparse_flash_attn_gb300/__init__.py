@@ -32,7 +32,8 @@ CAUSAL, OUT_F32 = 1, 2
 
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
-           "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc"]
+           "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
+           "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free"]
 
 
 class BsattnError(RuntimeError):
@@ -80,6 +81,14 @@ def load():
     lib.bsattn_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float,
                                        u32, vp]
     lib.bsattn_fwd_noalloc.restype = i32
+    lib.bsattn_pipeline_create.argtypes = [vp, i32, i32, i32, i32, u32, i32, vp, ctypes.POINTER(vp)]
+    lib.bsattn_pipeline_create.restype = i32
+    lib.bsattn_pipeline_run.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_float, vp]
+    lib.bsattn_pipeline_run.restype = i32
+    lib.bsattn_pipeline_status.argtypes = [vp]
+    lib.bsattn_pipeline_status.restype = i32
+    lib.bsattn_pipeline_free.argtypes = [vp]
+    lib.bsattn_pipeline_free.restype = None
     _lib = lib
     return lib
 
@@ -238,6 +247,77 @@ def fwd_noalloc(q, k, v, mask, causal: bool = False, scale: float | None = None,
             ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()), B, H, S, D,
             float(scale), flags, _stream_handle(stream)), "bsattn_fwd_noalloc")
     return out, lse
+
+
+class HostPipeline:
+    """Forward passes on host-resident (pinned) tensors, transfers overlapped.
+
+    Wraps bsattn_pipeline_*: the library cuts the flattened (batch, head)
+    range into `chunks` parts (a plan each, built here once) and, on every
+    run, overlaps one part's upload, another's kernel and a third's download
+    on three streams.  Every run copies all of its inputs in and all of its
+    results out; results equal fwd()'s.
+    """
+
+    def __init__(self, mask: torch.Tensor, D: int, causal: bool = False, out_f32: bool = False,
+                 chunks: int = 4, stream=None):
+        if not (isinstance(mask, torch.Tensor) and mask.is_cuda and mask.dtype == torch.uint8):
+            raise TypeError("mask must be a CUDA uint8 tensor")
+        if mask.dim() != 4 or mask.shape[2] != mask.shape[3]:
+            raise ValueError("mask must be [B, H, nb, nb]")
+        mask = mask.contiguous()
+        B, H, nb, _ = mask.shape
+        self.B, self.H, self.S, self.D = B, H, nb * BLOCK, int(D)
+        self.out_dtype = torch.float32 if out_f32 else torch.bfloat16
+        flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0)
+        h = ctypes.c_void_p()
+        with torch.cuda.device(mask.device):
+            _check(load().bsattn_pipeline_create(ctypes.c_void_p(mask.data_ptr()), B, H, self.S,
+                                                 self.D, flags, int(chunks),
+                                                 _stream_handle(stream), ctypes.byref(h)),
+                   "bsattn_pipeline_create")
+        self._h = h.value
+        self.device = mask.device
+
+    def run(self, hq: torch.Tensor, hk: torch.Tensor, hv: torch.Tensor, ho: torch.Tensor,
+            hlse: torch.Tensor, scale: float | None = None, stream=None) -> None:
+        """Enqueue one forward pass: pinned host [B, H, S, D] bf16 in, pinned host O
+        [B, H, S, D] and LSE [B, H, S] out.  `stream` (default: the current one)
+        is made to wait for the results; synchronise it before reading them."""
+        shp = (self.B, self.H, self.S, self.D)
+        for t in (hq, hk, hv):
+            if t.is_cuda or t.dtype != torch.bfloat16 or tuple(t.shape) != shp or \
+                    not t.is_contiguous():
+                raise ValueError("hq, hk, hv must be contiguous host bf16 [B, H, S, D]")
+        if ho.is_cuda or ho.dtype != self.out_dtype or tuple(ho.shape) != shp or \
+                not ho.is_contiguous():
+            raise ValueError("ho must be a contiguous host tensor [B, H, S, D] of the output dtype")
+        if hlse.is_cuda or hlse.dtype != torch.float32 or tuple(hlse.shape) != shp[:3] or \
+                not hlse.is_contiguous():
+            raise ValueError("hlse must be a contiguous host fp32 tensor [B, H, S]")
+        if scale is None:
+            scale = 1.0 / math.sqrt(self.D)
+        with torch.cuda.device(self.device):
+            _check(load().bsattn_pipeline_run(
+                ctypes.c_void_p(self._h), ctypes.c_void_p(hq.data_ptr()),
+                ctypes.c_void_p(hk.data_ptr()), ctypes.c_void_p(hv.data_ptr()),
+                ctypes.c_void_p(ho.data_ptr()), ctypes.c_void_p(hlse.data_ptr()), float(scale),
+                _stream_handle(stream)), "bsattn_pipeline_run")
+
+    def status(self) -> None:
+        """Wait for the pipeline; raise if a kernel reported a timeout or internal error."""
+        _check(load().bsattn_pipeline_status(ctypes.c_void_p(self._h)), "pipeline status")
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            load().bsattn_pipeline_free(ctypes.c_void_p(self._h))
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # interpreter shutdown
+            pass
 
 
 def attention(q, k, v, mask, causal: bool = False, scale: float | None = None,

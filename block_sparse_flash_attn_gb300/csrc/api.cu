@@ -98,6 +98,58 @@ void free_plan_memory(bsattn_plan_s* p) {
 
 }  // namespace
 
+namespace bsattn {
+
+bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                          void* out, float* lse, int B, int H, int S, int D, float scale,
+                          PreparedFwd* pf) {
+  if (!plan_ok(plan) || !pf) return BSATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+    return BSATTN_ERR_INVALID_ARG;
+  if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
+  if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
+
+  const long long rows = (long long)B * H * S;
+  bsattn_status rc;
+  if ((rc = encode_bf16_map(&pf->tq, q, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&pf->tk, k, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&pf->tv, v, D, rows)) != BSATTN_OK) return rc;
+
+  FwdParams& prm = pf->prm;
+  prm = FwdParams{};
+  prm.row_ptr = plan->dev.row_ptr;
+  prm.col_idx = plan->dev.col_idx;
+  prm.tile_order = plan->dev.tile_order;
+  prm.empty_tiles = plan->dev.empty_tiles;
+  prm.out = out;
+  prm.lse = lse;
+  prm.counter = plan->dev.work + kWorkCounter;
+  prm.done = plan->dev.work + kWorkDone;
+  prm.status = plan->dev.work + kWorkStatus;
+  prm.n_live = (int)plan->n_live;
+  prm.n_empty = (int)plan->n_empty;
+  prm.nb = plan->nb;
+  prm.S = S;
+  set_scale_params(prm, scale);
+  prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
+  prm.timeout_ns = kDefaultWaitTimeoutNs;
+  pf->D = D;
+  pf->out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
+  pf->grid = device_sm_count(dev);
+  return BSATTN_OK;
+}
+
+cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream) {
+  return launch_fwd(pf.D, pf.out_f32, pf.tq, pf.tk, pf.tv, pf.prm, pf.grid, stream);
+}
+
+}  // namespace bsattn
+
 extern "C" {
 
 int bsattn_version(void) { return 100; }
@@ -219,46 +271,10 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
 bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                          void* out, float* lse, int B, int H, int S, int D, float scale,
                          void* stream) {
-  if (!plan_ok(plan)) return BSATTN_ERR_INVALID_ARG;
-  if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
-    return BSATTN_ERR_INVALID_ARG;
-  if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
-  if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
-
-  const long long rows = (long long)B * H * S;
-  CUtensorMap tq, tk, tv;
-  bsattn_status rc;
-  if ((rc = encode_bf16_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
-
-  FwdParams prm{};
-  prm.row_ptr = plan->dev.row_ptr;
-  prm.col_idx = plan->dev.col_idx;
-  prm.tile_order = plan->dev.tile_order;
-  prm.empty_tiles = plan->dev.empty_tiles;
-  prm.out = out;
-  prm.lse = lse;
-  prm.counter = plan->dev.work + kWorkCounter;
-  prm.done = plan->dev.work + kWorkDone;
-  prm.status = plan->dev.work + kWorkStatus;
-  prm.n_live = (int)plan->n_live;
-  prm.n_empty = (int)plan->n_empty;
-  prm.nb = plan->nb;
-  prm.S = S;
-  set_scale_params(prm, scale);
-  prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
-  prm.timeout_ns = kDefaultWaitTimeoutNs;
-
-  const int grid = device_sm_count(dev);
-  const bool out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
-  return from_cuda(launch_fwd(D, out_f32, tq, tk, tv, prm, grid,
-                              static_cast<cudaStream_t>(stream)));
+  PreparedFwd pf;
+  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf);
+  if (rc != BSATTN_OK) return rc;
+  return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }
 
 bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {

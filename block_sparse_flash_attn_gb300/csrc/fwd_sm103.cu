@@ -58,6 +58,7 @@
 // Every wait is bounded (globaltimer); on expiry the kernel records a timeout
 // in the status word, every role leaves its loop, outstanding TMA loads and
 // MMAs are drained (again with a limit) and TMEM is freed before exit.
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 
@@ -93,6 +94,7 @@ static_assert(kTmemS + kSBufs * 128 <= kTmemO && kTmemO + 128 <= kTmemCols &&
                   kTmemO + 64 + 16 <= kTmemCols,
               "tensor memory columns");
 constexpr unsigned long long kDrainNs = 200ull * 1000 * 1000;
+constexpr int kMaxDevices = 64;
 
 template <int D>
 struct Cfg {
@@ -854,9 +856,18 @@ template <int D, bool OUT_F32>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream) {
   const size_t smem = Cfg<D>::kSmem + 1024;
-  cudaError_t e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // The shared-memory opt-in is set once per device (it costs host time on
+  // every call otherwise); a failed attempt is retried on the next call.
+  static std::atomic<bool> opted_in[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
+  }
   bsattn_fwd_kernel<D, OUT_F32><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }

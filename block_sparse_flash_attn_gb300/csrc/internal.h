@@ -59,6 +59,21 @@ bool aligned16(const void* p);
 bsattn_status from_cuda(cudaError_t e);
 bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows);
 
+// One forward launch with everything resolved: tensor maps, kernel
+// parameters, grid.  prepare_fwd checks the arguments exactly as bsattn_fwd
+// does; launch_prepared only launches.
+struct PreparedFwd {
+  CUtensorMap tq, tk, tv;
+  FwdParams prm;
+  int D = 0;
+  bool out_f32 = false;
+  int grid = 0;
+};
+bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                          void* out, float* lse, int B, int H, int S, int D, float scale,
+                          PreparedFwd* pf);
+cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream);
+
 // plan.cu
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,

@@ -182,6 +182,57 @@ bsattn_status bsattn_fwd_noalloc(const void* q, const void* k, const void* v,
  */
 bsattn_status bsattn_selftest_wait_timeout(int64_t timeout_ns, void* stream);
 
+/*
+ * Forward passes on HOST-resident tensors, with the transfers overlapped.
+ *
+ * Not on the pages: the forward pass above needs Q, K, V in device memory.
+ * A pipeline owns device copies of the whole problem and cuts the flattened
+ * (b, h) range into `pieces` contiguous parts, each with its own plan (built
+ * at creation, from the corresponding slice of the mask).  bsattn_pipeline_run
+ * enqueues, for every part, the host-to-device copy of its Q, K, V on one
+ * stream, its forward kernel on a second and the device-to-host copy of its
+ * O and LSE on a third, so one part's upload overlaps another part's kernel
+ * and a third part's download.  Every run copies all inputs in and all
+ * results out; results are identical to bsattn_fwd's (same kernel, same
+ * tiles).  Copies are plain cudaMemcpyAsync calls; host buffers must be
+ * pinned (page-locked) for the copies to overlap.
+ *
+ * bsattn_pipeline_create
+ *   d_mask     device uint8 [B][H][S/128][S/128]; read during the call only.
+ *   B, H, S, D sizes as for bsattn_plan / bsattn_fwd (D = 64 or 128).
+ *   flags      BSATTN_CAUSAL | BSATTN_OUT_F32.
+ *   pieces     number of parts, clamped to [1, B*H].
+ *   stream     cudaStream_t for the plan kernels (synchronised once per part).
+ *   out        receives the handle; the library owns the device buffers
+ *              (Q, K, V, O, LSE of the whole problem), the plans, three
+ *              streams and the events until bsattn_pipeline_free.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA (as bsattn_plan).
+ *
+ * bsattn_pipeline_run
+ *   hq, hk, hv host bf16 [B][H][S][D]; hout host [B][H][S][D] bf16 (fp32 with
+ *              BSATTN_OUT_F32); hlse host fp32 [B][H][S].  Read / written
+ *              asynchronously: `stream` is made to wait for the run's last
+ *              copy, so synchronise it before touching the buffers.
+ *   scale      finite multiplier of q.k.
+ *   Runs on one pipeline are ordered: a part's device buffers are reused
+ *   only after the previous run is done with them.
+ * Errors: INVALID_ARG (null pipeline or pointers, non-finite scale), CUDA.
+ *
+ * bsattn_pipeline_status -- waits for the pipeline's streams and reports the
+ *   kernels' recorded status (TIMEOUT / INTERNAL) like bsattn_plan_status.
+ * bsattn_pipeline_free -- waits, then releases everything; NULL is a no-op.
+ */
+typedef struct bsattn_pipeline_s* bsattn_pipeline_t;
+
+bsattn_status bsattn_pipeline_create(const uint8_t* d_mask, int B, int H, int S, int D,
+                                     unsigned flags, int pieces, void* stream,
+                                     bsattn_pipeline_t* out);
+bsattn_status bsattn_pipeline_run(bsattn_pipeline_t pipe, const void* hq, const void* hk,
+                                  const void* hv, void* hout, float* hlse, float scale,
+                                  void* stream);
+bsattn_status bsattn_pipeline_status(bsattn_pipeline_t pipe);
+void bsattn_pipeline_free(bsattn_pipeline_t pipe);
+
 #ifdef __cplusplus
 }
 #endif

@@ -252,3 +252,34 @@ def test_fwd_argument_errors(bs):
                           128, ctypes.c_float(0.1), st) == bs.ERR_INVALID_ARG  # no plan
     bs.plan_status(p)
     p.close()
+
+
+# ----------------------------------------------------------------------------
+# host-buffer path: same kernel per piece, so bit-identical to the device path
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("wid,chunks", [(1, 2), (2, 3), (5, 4)])
+def test_host_pipeline_matches_device_path(bs, wid, chunks):
+    import torch
+    w = workloads.WORKLOADS[wid]
+    qb, kb, vb = workloads.make_qkv(w)
+    mask = workloads.make_mask(w)
+    mask_d = torch.from_numpy(mask).cuda()
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    p = bs.plan(mask_d, causal=w.causal)
+    o_ref, l_ref = bs.fwd(q, k, v, p, w.scale)
+    bs.plan_status(p)
+    p.close()
+    host = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hq, hk, hv = host(qb), host(kb), host(vb)
+    ho = torch.empty(o_ref.shape, dtype=o_ref.dtype).pin_memory()
+    hl = torch.empty(l_ref.shape, dtype=l_ref.dtype).pin_memory()
+    pipe = bs.HostPipeline(mask_d, w.D, causal=w.causal, chunks=chunks)
+    for _ in range(2):  # the second call reuses the device buffers
+        ho.zero_()
+        pipe.run(hq, hk, hv, ho, hl, w.scale)
+        torch.cuda.current_stream().synchronize()
+        pipe.status()
+        assert torch.equal(ho, o_ref.cpu())
+        assert torch.equal(hl, l_ref.cpu())
+    pipe.close()
