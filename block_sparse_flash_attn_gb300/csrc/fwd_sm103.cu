@@ -84,6 +84,9 @@ constexpr int kClaimAhead = 4;
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 48;
 constexpr float kTau = 8.0f;
+// A row whose probabilities, formed against a stale reference, sum to more
+// than this over one block is redone with the block's max as reference.
+constexpr float kGrowSum = 4294967296.0f;  // 2^32
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: three score buffers S[0..2] (128 each; the bf16 P
 // of a block overwrites its scores) and the output accumulator O (D).
@@ -643,21 +646,43 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
 #pragma unroll
         for (int c = 0; c < 64; ++c) sr[c] = (ch * 64 + c > r) ? kNegInf : sr[c];
       }
-      float mx = row_max64(sr);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
-      const float xm = mx * sl;
-      const bool need = xm > m + kTau;  // always true on the first block (m = -inf)
-      float f = 1.f;
-      if (need) {
-        f = ex2_approx(m - xm);  // 0 when m = -inf
-        m = xm;
-        a32[0] *= f;
-        a32[1] *= f;
-        r32[0] *= f;
-        r32[1] *= f;
-      }
+      // After a tile's first block the probabilities are formed against the
+      // current reference m without a max pass (any common reference gives
+      // the exact softmax).  Only when a row's sum over the block shows that
+      // its scores rose far above m (2^kGrowLog2) -- or on the tile's first
+      // block, where m = -inf -- is the block redone with its max, by the
+      // lazy rule, as the new reference.
       uint32_t pr[32];
-      softmax_exp64<!C::kOnes>(sr, pr, sl, -m, a32, r32);
+      float b32[2] = {0.f, 0.f}, br32[2] = {0.f, 0.f};  // this block's sums
+      bool redo = jb == 0;
+      if (!redo) {
+        softmax_exp64<!C::kOnes>(sr, pr, sl, -m, b32, br32);
+        float bs = b32[0] + b32[1];
+        bs += __shfl_xor_sync(0xffffffffu, bs, 16);  // the other half of the row
+        redo = __any_sync(0xffffffffu, !(bs <= kGrowSum));  // also catches inf / NaN
+      }
+      bool need = false;
+      float f = 1.f;
+      if (redo) {
+        float mx = row_max64(sr);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
+        const float xm = mx * sl;
+        need = xm > m + kTau;  // always true on the first block (m = -inf)
+        if (need) {
+          f = ex2_approx(m - xm);  // 0 when m = -inf
+          m = xm;
+          a32[0] *= f;
+          a32[1] *= f;
+          r32[0] *= f;
+          r32[1] *= f;
+        }
+        b32[0] = b32[1] = br32[0] = br32[1] = 0.f;
+        softmax_exp64<!C::kOnes>(sr, pr, sl, -m, b32, br32);
+      }
+      a32[0] += b32[0];
+      a32[1] += b32[1];
+      r32[0] += br32[0];
+      r32[1] += br32[1];
       tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
 
       // O rescale (this thread's columns) when a row's max moved: first wait
