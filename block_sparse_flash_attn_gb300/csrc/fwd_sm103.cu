@@ -649,7 +649,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       // After a tile's first block the probabilities are formed against the
       // current reference m without a max pass (any common reference gives
       // the exact softmax).  Only when a row's sum over the block shows that
-      // its scores rose far above m (2^kGrowLog2) -- or on the tile's first
+      // its scores rose far above m (kGrowSum) -- or on the tile's first
       // block, where m = -inf -- is the block redone with its max, by the
       // lazy rule, as the new reference.
       uint32_t pr[32];
