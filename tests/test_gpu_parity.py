@@ -283,3 +283,61 @@ def test_host_pipeline_matches_device_path(bs, wid, chunks):
         assert torch.equal(ho, o_ref.cpu())
         assert torch.equal(hl, l_ref.cpu())
     pipe.close()
+
+
+# ----------------------------------------------------------------------------
+# the largest supported sequence (S/128 = 4096 key blocks per row), sampled rows
+# ----------------------------------------------------------------------------
+
+def test_max_blocks_per_row_sampled(bs):
+    import torch
+    B, H, S, D = 1, 1, 4096 * 128, 128
+    nb = S // 128
+    rng = np.random.default_rng(11)
+    mask = np.zeros((B, H, nb, nb), np.uint8)
+    mask[0, 0, np.arange(nb), np.arange(nb)] = 1                       # diagonal
+    mask[0, 0, np.arange(nb)[:, None], rng.integers(0, nb, (nb, 2))] = 1  # two random blocks per row
+    mask[0, 0, 5, :] = 1                                                 # one row with every block live
+    qb, kb, vb = workloads.custom(211, B, H, S, D, 1.0)
+    scale = D ** -0.5
+    o, lse, p = _run(bs, qb, kb, vb, mask, scale, False, True)
+    p.close()
+    rows = np.unique(np.concatenate([5 * 128 + np.arange(128),            # the dense tile
+                                     rng.integers(0, S, 96)])).astype(np.int64)
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(scale), False, rows=rows)
+    ok, rep = compare(o.reshape(-1, D)[rows], lse.reshape(-1)[rows], O_ref, L_ref, out_bf16=False)
+    assert ok, rep
+
+
+# ----------------------------------------------------------------------------
+# a later key block whose scores far exceed the first block's (the softmax
+# must abandon its running reference for that block and rescale)
+# ----------------------------------------------------------------------------
+
+def _bf16_bits(x: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _bf16_float(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_scores_jump_in_a_later_block(bs, D):
+    B, H, S = 1, 2, 768
+    qb, kb, vb = workloads.custom(313, B, H, S, D, 1.0)
+    q = np.abs(_bf16_float(qb))                 # positive queries
+    k = _bf16_float(kb)
+    k[:, :, 384:512, :] = np.abs(k[:, :, 384:512, :]) * 6.0    # block 3: scores far above block 0
+    k[:, :, 640:, :] = np.abs(k[:, :, 640:, :]) * 12.0         # block 5: far above block 3
+    qb, kb = _bf16_bits(q), _bf16_bits(k)
+    mask = np.ones((B, H, S // 128, S // 128), np.uint8)
+    scale = D ** -0.5
+    for out_f32 in (True, False):
+        o, lse, p = _run(bs, qb, kb, vb, mask, scale, False, out_f32)
+        p.close()
+        O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(scale), False)
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+        ok, rep = compare(o, lse, O_ref, L_ref, out_bf16=not out_f32)
+        assert ok, (out_f32, rep)
