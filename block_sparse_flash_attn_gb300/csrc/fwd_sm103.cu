@@ -13,7 +13,7 @@
 //
 // GB300 design (one persistent CTA per SM, 512 threads = 4 warpgroups, one
 // query tile in the softmax at a time):
-//   warps 0-7  softmax + epilogue.  Each warp covers 16 query rows (TMEM
+//   warps 0-7  softmax (and the LSE).  Each warp covers 16 query rows (TMEM
 //              lanes); lanes 0..15 own key columns 0..63 of every block (O
 //              columns [0, D/2)), lanes 16..31 the same rows' columns 64..127
 //              (O columns [D/2, D)); tcgen05 16x32bx2 accesses put both halves
@@ -24,8 +24,10 @@
 //              for it (a few blocks before the current tile's end),
 //              publishes it (CSR range and first key blocks) in a 2-slot
 //              queue and loads its Q (elected lane)
-//   warp  12   tcgen05 issuer of O += P V (elected lane)
-//   warps 11, 13-15 idle (complete warpgroups 2 and 3 for setmaxnreg)
+//   warp  11   tcgen05 issuer of O += P V (elected lane)
+//   warps 12-15 epilogue: one thread per query row reads O from tensor
+//              memory, divides it by the row's rounded sum and stores it,
+//              while the softmax warps already work on the next tile
 // Tensor memory (512 columns allocated): three score buffers S[0] = [0,128),
 // S[1] = [128,256), S[2] = [256,384) and the fp32 output accumulator
 // O = [384, 384+D) (at D = 64 followed by 16 columns of the rounded row sum,
@@ -47,8 +49,8 @@
 // a fresh O.  The commit after S(g) frees K(g)'s ring stage and is the
 // softmax's "S(g) ready" signal; the commit after PV(g) frees V(g)'s stage
 // and is "PV(g) done", which the softmax waits for only before an O rescale
-// and, for the tile's last block, before the epilogue (which therefore
-// always precedes the next tile's first PV, the one that overwrites O).
+// and the epilogue warps for a tile's last block.  The next tile's first PV,
+// the one that overwrites O, waits until the epilogue warps have read O.
 // Online softmax in base 2 with lazy rescale: the running max m only moves
 // when a block's max exceeds it by more than 8 (log2 units), so P <= 256 and
 // the O rescale is rare.  O is normalised by the row sum of the bf16-rounded
@@ -74,7 +76,14 @@ constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMmaS = 9;  // also allocates and frees tensor memory
 constexpr int kWarpSched = 10;
-constexpr int kWarpMmaPV = 12;
+constexpr int kWarpMmaPV = 11;
+constexpr int kWarpEpi0 = 12;  // warps 12-15: epilogue (TMEM sub-partitions 0-3)
+constexpr int kEpiWarps = 4;
+constexpr uint32_t kEpiBarrier = 1;  // named barrier of the epilogue warps
+// Waits off the critical path (the scheduler's wait for a request, the
+// epilogue leader's waits) test the barrier about this often (ns) and sleep
+// in between: a spinning warp takes issue slots from the softmax warps.
+constexpr uint32_t kSleepNs = 200;
 // The producer asks for the next tile when its K cursor has this many blocks
 // of the current tile left: claiming a tile (four dependent global reads)
 // and loading its Q take about as long as this many blocks' MMAs.
@@ -125,7 +134,7 @@ struct Cfg {
   static constexpr int kPvN = kOnes ? D + 16 : D;
   static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;
   static constexpr int kBarOff = kOnesOff + (kOnes ? kVStages * kBoxBytes : 0);
-  static constexpr int kSmem = kBarOff + 1024;
+  static constexpr int kSmem = kBarOff + 2048;  // barriers, tile queue, 1/l
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(128, kPvN, true);
 };
@@ -150,16 +159,24 @@ struct __align__(16) Bars {
   uint64_t v_empty[kMaxStages];  // PV(g) complete: V stage free, O holds block g
   uint64_t q_full[2];
   uint64_t q_empty[2];  // the tile's last S complete: Q buffer free
-  uint64_t p_full[2];   // all softmax threads wrote P(g) (indexed by g % 2)
+  // every softmax warp wrote its rows of P(g), indexed by g % kSBufs: the
+  // softmax can run up to kSBufs blocks ahead of the PV issue, and P(g +
+  // kSBufs) needs S(g + kSBufs), i.e. PV(g) complete, so a barrier never
+  // completes a phase for a later block before its waiter saw the earlier one
+  uint64_t p_full[kSBufs];
   uint64_t tq_full[2];  // tile queue slot published
-  uint64_t tq_empty[2]; // slot read by producer, MMA warp and every softmax thread
-  uint64_t drain[2];    // all MMAs of the S / the PV issuer complete
+  uint64_t tq_empty[2]; // slot read by the producer, both MMA warps, every softmax warp, epilogue leader
+  uint64_t drain;       // all MMAs of both issuers complete (one commit from each)
   uint64_t req;         // the producer asks for the next tile (once per tile)
+  uint64_t epi_full;    // the softmax handed a tile's O over to the epilogue warps
+  uint64_t o_free;      // the epilogue warps read O (and inv_l): the next tile may overwrite it
   TileInfo tq[2];
   uint32_t tmem_base;
   int abort_flag;
+  int epi_tile[2];       // tile the epilogue warps write next (by tile parity); < 0: stop
+  float inv_l[kBlock];  // D = 128: 1 / (rounded row sum) of the tile being written out
 };
-static_assert(sizeof(Bars) <= 1024, "barrier block must fit its 1 KB region");
+static_assert(sizeof(Bars) <= 2048, "barrier block must fit its 2 KB region");
 static_assert(Cfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(Cfg<64>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(Cfg<128>::kKStages <= kMaxStages && Cfg<64>::kKStages <= kMaxStages &&
@@ -188,6 +205,14 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
+// wait_warp for waits off the critical path: sleeps about `sleep_ns` between tests
+__device__ __forceinline__ bool wait_warp_idle(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status,
+                                               uint64_t limit_ns, uint32_t sleep_ns) {
+  const bool ok = wait_bounded_idle(bar, parity, abort_flag, status, limit_ns, sleep_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ---------------------------------------------------------------------------
 // warp 10: tile scheduler
 // ---------------------------------------------------------------------------
@@ -212,8 +237,9 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
   bool ok = true;
   for (int i = 0; ok; ++i) {
     const int e = i & 1;
-    if (i > 0 && !wait_warp(smem_u32(&bars->req), (uint32_t)(i - 1) & 1u, abort_flag, p.status,
-                            lim)) {
+    // the producer asks a few blocks ahead of need: this wait sleeps between tests
+    if (i > 0 && !wait_warp_idle(smem_u32(&bars->req), (uint32_t)(i - 1) & 1u, abort_flag,
+                                 p.status, lim, kSleepNs)) {
       ok = false;
       break;
     }
@@ -286,11 +312,13 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
 // it read.  Returns false when the wait failed.
 __device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& p,
                                           volatile int* abort_flag, int& t, int& r0, int& n,
-                                          int& col) {
+                                          int& col, uint32_t sleep_ns = 0) {
   const int lane = threadIdx.x & 31;
   const int e = tqc & 1;
-  if (!wait_warp(smem_u32(&bars->tq_full[e]), (uint32_t)(tqc >> 1) & 1u, abort_flag, p.status,
-                 p.timeout_ns))
+  const uint32_t bar = smem_u32(&bars->tq_full[e]);
+  const uint32_t par = (uint32_t)(tqc >> 1) & 1u;
+  if (!(sleep_ns ? wait_warp_idle(bar, par, abort_flag, p.status, p.timeout_ns, sleep_ns)
+                 : wait_warp(bar, par, abort_flag, p.status, p.timeout_ns)))
     return false;
   const volatile TileInfo* slot = &bars->tq[e];
   t = slot->t;
@@ -476,9 +504,9 @@ __device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_
     }
   }
   // Every MMA issued here must finish before TMEM is released.
-  if (elect_one()) mma_commit(smem_u32(&bars->drain[0]));
+  if (elect_one()) mma_commit(smem_u32(&bars->drain));
   __syncwarp();
-  wait_drain(smem_u32(&bars->drain[0]), 0);
+  wait_drain(smem_u32(&bars->drain), 0);
 }
 
 // O (+)= P V : M=128, N=D, K=128 keys in steps of 16.  P(g) is read from
@@ -492,16 +520,22 @@ __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32
                            volatile int* abort_flag) {
   using C = Cfg<D>;
   const uint64_t lim = p.timeout_ns;
-  int vc = 0, tqc = 0;  // PV issued, tiles taken
+  int vc = 0, tqc = 0, ntile = 0;  // PV issued, tiles taken, tiles started
   bool ok = true;
   while (ok) {
     int t = 0, r0 = 0, n = 0, col = 0;
     if (!take_tile(bars, tqc, p, abort_flag, t, r0, n, col)) break;
     ++tqc;
     if (t < 0) break;
+    // the tile's first PV overwrites O: the epilogue warps must have read the
+    // previous tile's O
+    if (ntile > 0 && !wait_warp(smem_u32(&bars->o_free), (uint32_t)(ntile - 1) & 1u, abort_flag,
+                                p.status, lim))
+      break;
+    ++ntile;
     for (int j = 0; j < n; ++j) {
-      // two P barriers so that P(g+1) can never be mistaken for P(g)
-      if (!wait_warp(smem_u32(&bars->p_full[vc & 1]), (uint32_t)(vc >> 1) & 1u, abort_flag,
+      // P(vc) in (one barrier per score buffer, see Bars::p_full)
+      if (!wait_warp(smem_u32(&bars->p_full[vc % kSBufs]), (uint32_t)(vc / kSBufs) & 1u, abort_flag,
                      p.status, lim)) {
         ok = false;
         break;
@@ -529,9 +563,9 @@ __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32
       ++vc;
     }
   }
-  if (elect_one()) mma_commit(smem_u32(&bars->drain[1]));
+  if (elect_one()) mma_commit(smem_u32(&bars->drain));
   __syncwarp();
-  wait_drain(smem_u32(&bars->drain[1]), 0);
+  wait_drain(smem_u32(&bars->drain), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -556,21 +590,22 @@ __device__ void write_empty_tiles(const FwdParams& p) {
 
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
 // pairs into pr[] (the A operand of the PV product).  Accumulates the row sum
-// a32 of the fp32 p (for the LSE) and, when ROUNDED, r32 of the bf16-rounded
-// p that multiply V (the O denominator, so that the weights on V sum to one
-// even when a single key dominates a row), each in two independent
-// accumulators.
+// of the fp32 p (for the LSE) in a2, two partial sums in one f32x2 pair, and,
+// when ROUNDED, r32 of the bf16-rounded p that multiply V (the O denominator,
+// so that the weights on V sum to one even when a single key dominates a
+// row), again in two partial sums.  sl2 = (sl, sl), nm2 = (-m, -m).
 template <bool ROUNDED>
-__device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, float sl,
-                                              float nm, float (&a32)[2], float (&r32)[2]) {
+__device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, uint64_t sl2,
+                                              uint64_t nm2, uint64_t& a2, float (&r32)[2]) {
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
     float x0, x1;
-    fma2(x0, x1, __uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1]), sl, sl, nm, nm);
+    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])), sl2, nm2),
+              x0, x1);
     const float p0 = ex2_approx(x0);
     const float p1 = ex2_approx(x1);
     pr[q] = pack_bf16x2(p0, p1);
-    add2(a32[0], a32[1], a32[0], a32[1], p0, p1);
+    a2 = f2_add(a2, f2_pack(p0, p1));
     if (ROUNDED) add_bf16x2_f32(r32[0], r32[1], pr[q]);
   }
 }
@@ -604,12 +639,14 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
   const uint32_t lane_off = (uint32_t)(sub * 32 + lh * 16) << 16;
   const uint32_t tO = tmem + kTmemO + lane_off;
   const float sl = p.scale_log2;       // > 0 (see FwdParams)
+  const uint64_t sl2 = f2_pack(sl, sl);
   const uint32_t kNegInf = 0xff800000u;
   const uint64_t lim = p.timeout_ns;
 
   write_empty_tiles<D, OUT_F32>(p);
 
   int tq_cnt = 0, g = 0;  // g: blocks processed by this CTA (selects S buffer / ring stages)
+  int ntile = 0;          // tiles handed to the epilogue warps
   for (;;) {
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
@@ -626,10 +663,10 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
-    float a32[2] = {0.f, 0.f};  // partial sums of this half row: fp32 p
+    uint64_t a2 = 0;            // partial sums of this half row: fp32 p (an f32x2 pair)
     float r32[2] = {0.f, 0.f};  // and bf16-rounded p
     for (int jb = 0; jb < n; ++jb, ++g) {
-      const int b = g & 1;  // P barrier of this block
+      const int b = g % kSBufs;  // P barrier of this block
       // S(g) ready = its commit released K(g)'s stage
       if (!wait_warp(smem_u32(&bars->k_empty[g % C::kKStages]), (uint32_t)(g / C::kKStages) & 1u,
                      abort_flag, p.status, lim))
@@ -653,11 +690,14 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       // block, where m = -inf -- is the block redone with its max, by the
       // lazy rule, as the new reference.
       uint32_t pr[32];
-      float b32[2] = {0.f, 0.f}, br32[2] = {0.f, 0.f};  // this block's sums
+      uint64_t b2 = 0;  // this block's sums
+      float br32[2] = {0.f, 0.f};
       bool redo = jb == 0;
       if (!redo) {
-        softmax_exp64<!C::kOnes>(sr, pr, sl, -m, b32, br32);
-        float bs = b32[0] + b32[1];
+        softmax_exp64<!C::kOnes>(sr, pr, sl2, f2_pack(-m, -m), b2, br32);
+        float b0, b1;
+        f2_unpack(b2, b0, b1);
+        float bs = b0 + b1;
         bs += __shfl_xor_sync(0xffffffffu, bs, 16);  // the other half of the row
         redo = __any_sync(0xffffffffu, !(bs <= kGrowSum));  // also catches inf / NaN
       }
@@ -671,16 +711,15 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         if (need) {
           f = ex2_approx(m - xm);  // 0 when m = -inf
           m = xm;
-          a32[0] *= f;
-          a32[1] *= f;
+          a2 = f2_mul(a2, f2_pack(f, f));
           r32[0] *= f;
           r32[1] *= f;
         }
-        b32[0] = b32[1] = br32[0] = br32[1] = 0.f;
-        softmax_exp64<!C::kOnes>(sr, pr, sl, -m, b32, br32);
+        b2 = 0;
+        br32[0] = br32[1] = 0.f;
+        softmax_exp64<!C::kOnes>(sr, pr, sl2, f2_pack(-m, -m), b2, br32);
       }
-      a32[0] += b32[0];
-      a32[1] += b32[1];
+      a2 = f2_add(a2, b2);
       r32[0] += br32[0];
       r32[1] += br32[1];
       tmem_st16x2_32<64>(tS, pr);  // P over the scores just read (keys 0..63 -> cols 0..31, 64..127 -> 64..95)
@@ -717,55 +756,117 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[b]));
     }
 
-    // epilogue: O = O_acc / l, LSE = ln2 * (m + log2 l32), sums combined over both halves
-    if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) % C::kVStages]),
-                   (uint32_t)((g - 1) / C::kVStages) & 1u, abort_flag, p.status, lim))
-      return;  // the tile's last PV has landed in O
-    tc_fence_after();
-    float l;  // sum of the rounded P: the O denominator
-    if constexpr (C::kOnes) {
-      // accumulated by the tensor core in O column D (lanes 16..31 read the
-      // identical column D+1)
-      uint32_t rs[1];
-      tmem_ld16x2_1<1>(tO + D, rs);
-      tmem_wait_ld();
-      reg_fence(rs, 1);
-      l = __uint_as_float(rs[0]);
-    } else {
-      l = r32[0] + r32[1];
-      l += __shfl_xor_sync(0xffffffffu, l, 16);  // the other half of the row
-    }
-    float l32 = a32[0] + a32[1];  // fp32 sum of the unrounded P: the LSE
+    // Hand the tile over to the epilogue warps and go straight on to the next
+    // tile: the LSE is written here; at D = 128 the O denominator 1/l goes
+    // through shared memory (at D = 64 it sits in tensor memory next to O).
+    float a0, a1;
+    f2_unpack(a2, a0, a1);
+    float l32 = a0 + a1;  // fp32 sum of the unrounded P: the LSE
     l32 += __shfl_xor_sync(0xffffffffu, l32, 16);  // the other half of the row
     const size_t row = (size_t)bh * p.S + (size_t)qb * kBlock + r;
-    const float inv_l = 1.0f / l;
     if (ch == 0) p.lse[row] = (m + __log2f(l32)) * 0.69314718055994530942f;
-#pragma unroll
-    for (int c0 = 0; c0 < DH; c0 += 32) {
-      uint32_t orr[32];
-      tmem_ld16x2_32<DH>(tO + c0, orr);
+    // The epilogue warps are done with the previous tile (its 1/l is read):
+    // this keeps the softmax at most one tile ahead of them, so a later tile's
+    // epi_full phase can never complete before they waited for this one.
+    if (ntile > 0 && !wait_warp(smem_u32(&bars->o_free), (uint32_t)(ntile - 1) & 1u, abort_flag,
+                                p.status, lim))
+      return;
+    if constexpr (!C::kOnes) {
+      float l = r32[0] + r32[1];  // sum of the rounded P: the O denominator
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (ch == 0) bars->inv_l[r] = 1.0f / l;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&bars->epi_full));
+    ++ntile;
+    // Compiler barrier between tiles: nothing of the next tile's setup is
+    // scheduled into this one.  Without it the block loop above compiles to
+    // code that runs about 15 % slower per block.
+    asm volatile("" ::: "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// warps 12-15: epilogue, one thread per query row (TMEM lane)
+// ---------------------------------------------------------------------------
+// For each tile the softmax hands over: wait for its last PV, read O row by
+// row (16 columns at a time), divide by the rounded row sum and store it;
+// then release O for the next tile's first PV.  Only the leader warp takes
+// tiles and waits (sleeping between tests); it passes the tile on through
+// shared memory and a named barrier, where the other three warps wait
+// without issuing.  The leader reaches the barrier on every path, with a
+// negative tile to stop, so the four warps always leave together.
+template <int D, bool OUT_F32>
+__device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
+                             volatile int* abort_flag) {
+  using C = Cfg<D>;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = (warp & 3) * 32 + lane;  // query row of the tile = TMEM lane
+  const uint32_t tO = tmem + kTmemO + ((uint32_t)((warp & 3) * 32) << 16);
+  const uint64_t lim = p.timeout_ns;
+  int tqc = 0, g = 0, ntile = 0;  // (leader) tiles taken, blocks of the stream passed; tiles written
+  for (;;) {
+    if (warp == kWarpEpi0) {
+      int t = 0, r0 = 0, n = 0, col = 0;
+      bool ok = take_tile(bars, tqc, p, abort_flag, t, r0, n, col, kSleepNs);
+      ++tqc;
+      if (ok && t >= 0) {
+        const int gl = g + n - 1;  // the tile's last block
+        g += n;
+        // the softmax is done with the tile (its LSE written, 1/l in shared
+        // memory at D = 128), and the tile's last PV has landed in O
+        ok = wait_warp_idle(smem_u32(&bars->epi_full), (uint32_t)ntile & 1u, abort_flag, p.status,
+                            lim, kSleepNs) &&
+             wait_warp_idle(smem_u32(&bars->v_empty[gl % C::kVStages]),
+                            (uint32_t)(gl / C::kVStages) & 1u, abort_flag, p.status, lim, kSleepNs);
+      }
+      if (lane == 0) bars->epi_tile[ntile & 1] = ok ? t : -1;
+    }
+    named_bar_sync(kEpiBarrier, kEpiWarps * 32);
+    const int t = *reinterpret_cast<volatile int*>(&bars->epi_tile[ntile & 1]);
+    if (t < 0) return;
+    tc_fence_after();
+    float inv_l = 0.f;
+    if constexpr (!C::kOnes) inv_l = bars->inv_l[r];
+    if constexpr (C::kOnes) {  // rounded row sum accumulated by the tensor core in column D
+      uint32_t rs[1];
+      tmem_ld32_1(tO + D, rs);
       tmem_wait_ld();
-      reg_fence(orr, 32);
-      if constexpr (OUT_F32) {
-        float* dst = reinterpret_cast<float*>(p.out) + row * D + ch * DH + c0;
+      reg_fence(rs, 1);
+      inv_l = 1.0f / __uint_as_float(rs[0]);
+    }
+    const int bh = t / p.nb;
+    const size_t row = (size_t)bh * p.S + (size_t)(t - bh * p.nb) * kBlock + r;
 #pragma unroll
-        for (int i = 0; i < 32; i += 4)
+    for (int c0 = 0; c0 < D; c0 += 16) {
+      uint32_t orr[16];
+      tmem_ld32_16(tO + c0, orr);
+      tmem_wait_ld();
+      reg_fence(orr, 16);
+      if constexpr (OUT_F32) {
+        float* dst = reinterpret_cast<float*>(p.out) + row * D + c0;
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
           st_global_v4(dst + i, __float_as_uint(__uint_as_float(orr[i]) * inv_l),
                        __float_as_uint(__uint_as_float(orr[i + 1]) * inv_l),
                        __float_as_uint(__uint_as_float(orr[i + 2]) * inv_l),
                        __float_as_uint(__uint_as_float(orr[i + 3]) * inv_l));
       } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + ch * DH + c0;
-        uint32_t pk[16];
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + c0;
+        uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
+        for (int i = 0; i < 8; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
                               __uint_as_float(orr[2 * i + 1]) * inv_l);
-#pragma unroll
-        for (int i = 0; i < 16; i += 4) st_global_v4(dst + 2 * i, pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+        st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
+        st_global_v4(dst + 8, pk[4], pk[5], pk[6], pk[7]);
       }
     }
     tc_fence_before();
+    __syncwarp();  // every lane's reads of O are complete
+    if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
+    ++ntile;
   }
 }
 
@@ -796,14 +897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->q_empty[i]), 1);
     }
     // the softmax warps arrive once per warp (elected lane, after __syncwarp)
-    mbar_init(smem_u32(&bars->p_full[0]), kSoftmaxWarps);
-    mbar_init(smem_u32(&bars->p_full[1]), kSoftmaxWarps);
-    mbar_init(smem_u32(&bars->drain[0]), 1);
-    mbar_init(smem_u32(&bars->drain[1]), 1);
+    for (int i = 0; i < kSBufs; ++i) mbar_init(smem_u32(&bars->p_full[i]), kSoftmaxWarps);
+    mbar_init(smem_u32(&bars->drain), 2);
     mbar_init(smem_u32(&bars->req), 1);
+    mbar_init(smem_u32(&bars->epi_full), kSoftmaxWarps);
+    mbar_init(smem_u32(&bars->o_free), kEpiWarps);
     for (int e = 0; e < 2; ++e) {
       mbar_init(smem_u32(&bars->tq_full[e]), 1);
-      mbar_init(smem_u32(&bars->tq_empty[e]), 3 + kSoftmaxWarps);
+      mbar_init(smem_u32(&bars->tq_empty[e]), 3 + kSoftmaxWarps + 1);
     }
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -837,6 +938,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       run_mma_s<D>(p, bars, tmem, base, abort_flag);
     else if (warp == kWarpMmaPV)
       run_mma_pv<D>(p, bars, tmem, base, abort_flag);
+    else if (warp >= kWarpEpi0)
+      run_epilogue<D, OUT_F32>(p, bars, tmem, abort_flag);
     else if (warp == kWarpSched)
       run_scheduler<D>(&tm_q, p, bars, base, abort_flag);
   } else {

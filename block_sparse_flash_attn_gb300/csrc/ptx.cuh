@@ -102,6 +102,31 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// wait_bounded for waits off the critical path: between tests the thread
+// sleeps for about `sleep_ns` (nanosleep), so that a warp that waits for
+// long takes few issue slots from the warps doing the math.
+__device__ __forceinline__ bool wait_bounded_idle(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, int* status,
+                                                  uint64_t limit_ns, uint32_t sleep_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(sleep_ns);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// Named barrier `id` (1..15) over `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // TMA: 2-D tiled bulk tensor load global -> shared, completion on an mbarrier
 // ---------------------------------------------------------------------------
@@ -214,6 +239,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld32_16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld32_1(uint32_t taddr, uint32_t* r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r[0]) : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -304,23 +343,32 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// Packed fp32 pair arithmetic (sm_100+): one instruction for two lanes of work.
-__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,
-                                     float c0, float c1) {
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+// Packed fp32 pair arithmetic (sm_100+, one instruction for two lanes of
+// work).  Two fp32 values as one f32x2 operand (a 64-bit register pair, `lo` in
+// bits 0..31).  Values that stay packed across many operations (a constant,
+// an accumulator) are kept in this form so that no pair is rebuilt per use.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
 }
-
-__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0,
-                                     float b1) {
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
 }
 
 // Register budget of the executing warpgroup (all four warps execute it).
@@ -333,27 +381,6 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// 2^x for a pair, on the FMA pipe instead of the MUFU unit (x <= 126).
-// Range reduction x = n + f with n = rint(x), |f| <= 1/2, then a cubic for
-// 2^f (coefficients fitted here for minimum relative error on [-1/2, 1/2]:
-// max relative error 7.6e-5, far below bf16's 2^-9 half-ulp), then 2^n is
-// applied by adding n to the exponent field.  x is clamped at -125 so the
-// exponent field never underflows (2^-125 stands in for smaller values).
-__device__ __forceinline__ void exp2_poly2(float& y0, float& y1, float x0, float x1) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23: adding it rounds to an integer
-  constexpr float c0 = 0.99992847f, c1 = 0.69326085f, c2 = 0.24260531f, c3 = 0.05516921f;
-  x0 = fmaxf(x0, -125.f);
-  x1 = fmaxf(x1, -125.f);
-  float t0, t1, n0, n1, f0, f1, q0, q1;
-  add2(t0, t1, x0, x1, kRound, kRound);       // low mantissa bits of t hold rint(x)
-  add2(n0, n1, t0, t1, -kRound, -kRound);     // rint(x) as a float
-  fma2(f0, f1, n0, n1, -1.f, -1.f, x0, x1);  // f = x - rint(x) in [-1/2, 1/2]
-  fma2(q0, q1, f0, f1, c3, c3, c2, c2);
-  fma2(q0, q1, q0, q1, f0, f1, c1, c1);
-  fma2(q0, q1, q0, q1, f0, f1, c0, c0);
-  y0 = __uint_as_float(__float_as_uint(q0) + (__float_as_uint(t0) << 23));
-  y1 = __uint_as_float(__float_as_uint(q1) + (__float_as_uint(t1) << 23));
-}
 
 // Pack two floats to bf16x2 with round-to-nearest-even: `lo` in bits 0..15.
 // d0 += low bf16 of `pair`, d1 += high bf16 of `pair` (exact widening, one
