@@ -838,6 +838,9 @@ __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
     }
     const int bh = t / p.nb;
     const size_t row = (size_t)bh * p.S + (size_t)(t - bh * p.nb) * kBlock + r;
+    // Each thread writes its own row: 32-byte stores (one full sector each)
+    // when the output is 32-byte aligned, else 16-byte ones.
+    const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
 #pragma unroll
     for (int c0 = 0; c0 < D; c0 += 16) {
       uint32_t orr[16];
@@ -846,12 +849,16 @@ __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
       reg_fence(orr, 16);
       if constexpr (OUT_F32) {
         float* dst = reinterpret_cast<float*>(p.out) + row * D + c0;
+        uint32_t v[16];
 #pragma unroll
-        for (int i = 0; i < 16; i += 4)
-          st_global_v4(dst + i, __float_as_uint(__uint_as_float(orr[i]) * inv_l),
-                       __float_as_uint(__uint_as_float(orr[i + 1]) * inv_l),
-                       __float_as_uint(__uint_as_float(orr[i + 2]) * inv_l),
-                       __float_as_uint(__uint_as_float(orr[i + 3]) * inv_l));
+        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(orr[i]) * inv_l);
+        if (wide) {
+          st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(v));
+          st_global_v8(dst + 8, *reinterpret_cast<const uint32_t(*)[8]>(v + 8));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) st_global_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
       } else {
         uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + c0;
         uint32_t pk[8];
@@ -859,8 +866,12 @@ __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
         for (int i = 0; i < 8; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
                               __uint_as_float(orr[2 * i + 1]) * inv_l);
-        st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
-        st_global_v4(dst + 8, pk[4], pk[5], pk[6], pk[7]);
+        if (wide) {
+          st_global_v8(dst, pk);
+        } else {
+          st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
+          st_global_v4(dst + 8, pk[4], pk[5], pk[6], pk[7]);
+        }
       }
     }
     tc_fence_before();

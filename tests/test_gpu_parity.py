@@ -175,6 +175,40 @@ def test_repeated_calls_same_plan(bs):
     p.close()
 
 
+@pytest.mark.parametrize("out_f32", [True, False], ids=["o_f32", "o_bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_output_only_16_byte_aligned(bs, D, out_f32):
+    """An output buffer that is 16- but not 32-byte aligned (a view into a
+    larger allocation) gets the same values as an aligned one, and nothing
+    around it is written."""
+    import torch
+    B, H, S = 1, 4, 512
+    qb, kb, vb = workloads.custom(91 + D, B, H, S, D)
+    mask = _mask_iid(11, B, H, S // 128, 0.5, diag=True)
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    p = bs.plan(torch.from_numpy(mask).cuda(), causal=True, out_f32=out_f32)
+    o_al, l_al = bs.fwd(q, k, v, p, D ** -0.5)
+    odt = torch.float32 if out_f32 else torch.bfloat16
+    n = B * H * S * D
+    pad = 16 // odt.itemsize + 32 // odt.itemsize  # 16-byte offset, then a guard band
+    raw = torch.full((n + 2 * pad,), -7.0, dtype=odt, device="cuda")
+    off = 16 // odt.itemsize
+    base = raw.data_ptr() % 32
+    if base != 0:  # make raw[off:] sit 16 bytes past a 32-byte boundary
+        off += (32 - base) // odt.itemsize
+    out = raw[off:off + n].view(B, H, S, D)
+    assert out.data_ptr() % 32 == 16
+    o_un, l_un = bs.fwd(q, k, v, p, D ** -0.5, out=out)
+    bs.plan_status(p)
+    assert torch.equal(o_un, o_al) and torch.equal(l_un, l_al)
+    assert bool((raw[:off] == -7.0).all()) and bool((raw[off + n:] == -7.0).all())
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(D ** -0.5), True)
+    ok, rep = compare(o_un.float().cpu().numpy(), l_un.cpu().numpy(), O_ref, L_ref,
+                      out_bf16=not out_f32)
+    assert ok, rep
+    p.close()
+
+
 # ----------------------------------------------------------------------------
 # full-size workloads, sampled rows
 # ----------------------------------------------------------------------------
