@@ -108,7 +108,8 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
  *
  *   q, k, v    device bf16 [B][H][S][D], 16-byte aligned.
  *   plan       from bsattn_plan with the same B, H, S.
- *   out        device [B][H][S][D], bf16 (or fp32 with BSATTN_OUT_F32), 16-byte aligned.
+ *   out        device [B][H][S][D], bf16 (or fp32 with BSATTN_OUT_F32), 16-byte aligned
+ *              (32-byte aligned: written with full-sector stores, slightly faster).
  *   lse        device fp32 [B][H][S], 16-byte aligned.
  *   D          64 or 128.
  *   scale      finite; multiplies q.k before masking (1/sqrt(D) in the pages).
