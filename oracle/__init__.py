@@ -13,7 +13,8 @@ the formulas and the readings taken where the pages are silent.
 
 Every function here is pinned by tests/test_oracle_pins.py (brute force,
 library special cases, closed forms and invariants); none is "parity
-unpinned".
+unpinned".  The gradients and the transposed plan (``backward.py``, numpy
+fp64) are pinned by tests/test_oracle_bwd_pins.py.
 """
 from __future__ import annotations
 
@@ -152,3 +153,6 @@ def flops_live(mask, D: int, causal: bool = False) -> int:
     """Work the method does, counted over live blocks: 4*128*128*D per block."""
     row_ptr, _ = csr(mask, causal)
     return int(row_ptr[-1]) * 4 * BLOCK * BLOCK * D
+
+
+from .backward import BWD_MUTATIONS, attention_bwd, csc, set_bwd_mutation  # noqa: E402,F401

@@ -1,0 +1,168 @@
+"""ORACLE -- test infrastructure, not product code.
+
+Gradients of exact block-sparse attention, in fp64 (numpy), and the
+transposed plan (per key block, the live query blocks).  Only the tests and
+the bench's reference leg may use this module; it shares nothing with the
+CUDA path.
+
+"Writing Pallas Kernels for JAX: Stepping Outside the XLA Safety Net"
+(section "The Empathy of the Void") notes that a hand-written attention
+kernel needs hand-written gradient definitions.  The definition used here is
+the derivative of the forward operation of the same article (sections
+"Designing the Block Specification" and "Writing the Kernel Logic: Load,
+Compute, Store"), made exact across key blocks as in "Pallas-Triton kernels
+and kernel auto-tuning" (section "Flash Attention").  For one (batch, head),
+with allowed(i, j) the block mask ANDed with the causal restriction:
+
+    s_ij  = scale * q_i . k_j        (-inf where not allowed)
+    P_ij  = exp(s_ij - max_j s_ij) / sum_j exp(...)   (0 where not allowed;
+                                                       rows with no allowed key: P = 0)
+    O_i   = sum_j P_ij v_j
+    dP_ij = dO_i . v_j
+    Dl_i  = sum_j P_ij dP_ij         (= dO_i . O_i)
+    dS_ij = P_ij (dP_ij - Dl_i)
+    dQ_i  = scale * sum_j dS_ij k_j
+    dK_j  = scale * sum_i dS_ij q_i
+    dV_j  = sum_i P_ij dO_i
+
+Each step is written out with numpy matrix products as the only library
+primitive; there is no blocking and no reordering beyond the formulas above.
+Pinned by tests/test_oracle_bwd_pins.py (finite differences of the forward
+oracle, torch float64 autograd, closed forms, invariants, planted mistakes).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BLOCK = 128
+
+# Planted mistakes (test-only): each must make at least one pin fail.
+BWD_MUTATIONS = {
+    1: "Dl term dropped from dS",
+    2: "dV uses P instead of its transpose",
+    3: "scale missing from dQ",
+    4: "dK built from dS without transposing",
+    5: "dP uses K in place of V",
+    6: "sign of dS flipped",
+    7: "causal restriction ignored in the gradients",
+}
+_mutation = 0
+
+
+def set_bwd_mutation(m: int) -> None:
+    """Plant mistake number m (0 = none).  Tests only."""
+    global _mutation
+    _mutation = int(m)
+
+
+def _as_f64(x: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) or float64 values -> float64."""
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if x.dtype == np.float64:
+        return x
+    raise TypeError("expected uint16 bf16 bit patterns or float64")
+
+
+def allowed_matrix(mask_bh: np.ndarray, S: int, causal: bool) -> np.ndarray:
+    """allowed[i, j] for one (batch, head): the block mask, ANDed with j <= i under causal."""
+    nb = S // BLOCK
+    assert mask_bh.shape == (nb, nb)
+    allowed = np.repeat(np.repeat(mask_bh != 0, BLOCK, axis=0), BLOCK, axis=1)
+    if causal and _mutation != 7:
+        allowed &= np.tril(np.ones((S, S), dtype=bool))
+    return allowed
+
+
+def _head(q, k, v, do, allowed, scale, bounds):
+    """One (batch, head): the formulas of the module docstring, in order."""
+    s = scale * (q @ k.T)
+    s = np.where(allowed, s, -np.inf)
+    live = allowed.any(axis=1)
+    m = np.where(live, s.max(axis=1, initial=-np.inf), 0.0)
+    e = np.where(allowed, np.exp(s - m[:, None]), 0.0)
+    l = e.sum(axis=1)
+    P = np.where(live[:, None], e / np.where(live, l, 1.0)[:, None], 0.0)
+    O = P @ v
+    dP = do @ (k.T if _mutation == 5 else v.T)
+    Dl = (P * dP).sum(axis=1)
+    if _mutation == 1:
+        dS = P * dP
+    else:
+        dS = P * (dP - Dl[:, None])
+    if _mutation == 6:
+        dS = -dS
+    dq = (1.0 if _mutation == 3 else scale) * (dS @ k)
+    dk = scale * ((dS if _mutation == 4 else dS.T) @ q)
+    dv = (P if _mutation == 2 else P.T) @ do
+    if not bounds:
+        return dq, dk, dv, None
+    # Per-element error bounds of a kernel that rounds P and dS to bf16 (relative
+    # 2^-9 each) and forms Dl from a bf16-rounded O (relative 2^-9 per product).
+    u = 2.0 ** -9
+    E = np.abs(do * O).sum(axis=1)                   # sum_d |dO_id O_id|
+    dS_w = np.abs(dS) + P * E[:, None]               # weight of the dS error
+    b = (u * abs(scale) * (dS_w @ np.abs(k)),
+         u * abs(scale) * (dS_w.T @ np.abs(q)),
+         u * (np.abs(P).T @ np.abs(do)))
+    return dq, dk, dv, b
+
+
+def attention_bwd(q, k, v, do, mask, scale: float, causal: bool = False, heads=None,
+                  bounds: bool = False):
+    """Gradients (dQ, dK, dV) of exact block-sparse attention, fp64.
+
+    q, k, v, do: [B][H][S][D] as bf16 bit patterns (uint16) or float64.
+    mask: uint8 [B][H][S/128][S/128].  heads: iterable of (b, h) to compute,
+    or None for all.  Returns float64 arrays [B][H][S][D] (heads not computed
+    are NaN); with bounds=True also a tuple of per-element error bounds
+    (same shapes) for a kernel computing in the precision described in
+    ``_head``.
+    """
+    q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    mask = np.asarray(mask, dtype=np.uint8)
+    B, H, S, D = q.shape
+    for x in (k, v, do):
+        if x.shape != q.shape:
+            raise ValueError("q, k, v, do shapes differ")
+    if S % BLOCK:
+        raise ValueError("S must be a multiple of 128")
+    if mask.shape != (B, H, S // BLOCK, S // BLOCK):
+        raise ValueError("mask shape does not match")
+    out = [np.full(q.shape, np.nan) for _ in range(3)]
+    bnd = [np.full(q.shape, np.nan) for _ in range(3)] if bounds else None
+    if heads is None:
+        heads = [(b, h) for b in range(B) for h in range(H)]
+    for b, h in heads:
+        allowed = allowed_matrix(mask[b, h], S, causal)
+        dq, dk, dv, bb = _head(q[b, h], k[b, h], v[b, h], do[b, h], allowed, float(scale), bounds)
+        out[0][b, h], out[1][b, h], out[2][b, h] = dq, dk, dv
+        if bounds:
+            for t in range(3):
+                bnd[t][b, h] = bb[t]
+    if bounds:
+        return tuple(out), tuple(bnd)
+    return tuple(out)
+
+
+def csc(mask, causal: bool = False):
+    """Per key block, the ascending live query blocks: (col_ptr int32, row_idx int32).
+
+    Entry (b, h, kb) lists qb with mask[b, h, qb, kb] != 0 (and qb >= kb under
+    causal), in ascending qb; col_ptr has B*H*nb + 1 entries.
+    """
+    mask = np.asarray(mask, dtype=np.uint8)
+    B, H, nb, nb2 = mask.shape
+    if nb != nb2:
+        raise ValueError("mask must be [B][H][nb][nb]")
+    col_ptr = [0]
+    rows = []
+    for b in range(B):
+        for h in range(H):
+            for kb in range(nb):
+                for qb in range(nb):
+                    if mask[b, h, qb, kb] and (not causal or qb >= kb):
+                        rows.append(qb)
+                col_ptr.append(len(rows))
+    return np.asarray(col_ptr, dtype=np.int32), np.asarray(rows, dtype=np.int32)
