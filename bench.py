@@ -72,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="fwd (default: the forward hot path) or bwd (gradients dQ, dK, dV)")
     return ap.parse_args(argv)
 
 
@@ -385,8 +387,127 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+BWD_METRIC = "bs-attn bwd effective TFLOP/s (live blocks)"
+
+
+def run_bwd(args):
+    """Backward pass: one step = one bsattn_bwd call (the dO.O row term and the
+    gradient kernel) on the workload, inputs resident, L2 flushed before each."""
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_flash_attn_gb300 as bsattn
+    from block_sparse_flash_attn_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    bsattn.load()
+
+    w = workloads.WORKLOADS[args.workload]
+    shape = (w.B, w.H, w.S, w.D)
+    qb, kb, vb = (workloads.normal_bf16(w.data_seed + 100 * rank, s, shape, w.mult)
+                  for s in (workloads.STREAM_Q, workloads.STREAM_K, workloads.STREAM_V))
+    gb = workloads.upstream_grad(w.data_seed + 100 * rank, *shape)
+    mask = workloads.make_mask(w)
+    nlive = live_blocks(mask, w.causal)
+    flop = nlive * 10 * 128 * 128 * w.D  # five 128 x 128 x D products per live block
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, g = to_dev(qb), to_dev(kb), to_dev(vb), to_dev(gb)
+    plan = bsattn.plan(torch.from_numpy(mask).to(dev), causal=w.causal, out_f32=args.out_f32)
+    o, lse = bsattn.fwd(q, k, v, plan, w.scale)
+    dq, dk, dv = bsattn.bwd(q, k, v, o, lse, g, plan, w.scale)
+    bsattn.plan_status(plan)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        flush.zero_()
+        bsattn.bwd(q, k, v, o, lse, g, plan, w.scale, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s, e in ev:
+        flush.zero_()
+        s.record(stream)
+        bsattn.bwd(q, k, v, o, lse, g, plan, w.scale, dq=dq, dk=dk, dv=dv)
+        e.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    bsattn.plan_status(plan)
+    plan.close()
+    ms_mean = statistics.mean(s.elapsed_time(e) for s, e in ev)
+    ms_max = max_over_ranks(ms_mean, dev)
+    value = whole_job_tflops(flop, world, ms_max)
+    peaks = read_peaks()
+    achieved = flop / (ms_mean * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and w.S > 8192:
+        cpu = {"value": None, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": "skipped: the gradient oracle forms S x S matrices per head "
+                         f"(S = {w.S} would need tens of GB)"}
+    elif rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        t0 = time.perf_counter()
+        oracle.attention_bwd(qb, kb, vb, gb, mask, np.float32(w.scale), w.causal, heads=[(0, 0)])
+        dt = time.perf_counter() - t0
+        head_flop = live_blocks(mask[:1, :1], w.causal) * 10 * 128 * 128 * w.D
+        cpu = {"value": head_flop / dt / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"gradients of head (0, 0) of workload {w.id} ({dt:.1f} s, fp64 numpy)"}
+
+    if rank == 0:
+        line = {
+            "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{w.id}:{w.name}", "pass": "bwd", "shape": w.describe(),
+                       "grad_dtype": "f32", "live_blocks": nlive, "flop_per_step": flop,
+                       "l2": "flushed (512 MB write) before every timed step",
+                       "parallelism": f"replicas x{world} (independent problems, no collective)"},
+            "e2e": None,
+            "gpu_launches": 2 * args.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
+                         "unit": UNIT, "frac": achieved / peaks["bf16"], "traffic": None,
+                         "peak_source": f"bf16 dense burst, {peaks['source']}",
+                         "frac_of_spec_2250": achieved / 2250.0,
+                         "kernel": "bsattn_bwd_kernel (with the dO.O row-term kernel)",
+                         "ms_per_launch": ms_mean},
+            "cpu_baseline": cpu,
+            "clocks": clk,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.which == "bwd":
+        if args.impl == "reference":
+            raise SystemExit("--pass bwd times the CUDA path only")
+        run_bwd(args)
+        return
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) == 0:
             run_reference(args)

@@ -33,7 +33,8 @@ CAUSAL, OUT_F32 = 1, 2
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
            "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
-           "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free"]
+           "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free",
+           "bsattn_plan_csc", "bsattn_bwd"]
 
 
 class BsattnError(RuntimeError):
@@ -68,6 +69,11 @@ def load():
     lib.bsattn_plan_schedule.restype = i32
     lib.bsattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
     lib.bsattn_fwd.restype = i32
+    lib.bsattn_plan_csc.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)]
+    lib.bsattn_plan_csc.restype = i32
+    lib.bsattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
+                               ctypes.c_float, vp]
+    lib.bsattn_bwd.restype = i32
     lib.bsattn_plan_status.argtypes = [vp, vp]
     lib.bsattn_plan_status.restype = i32
     lib.bsattn_plan_free.argtypes = [vp]
@@ -194,6 +200,45 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float
     return out, lse
 
 
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, p: Plan, scale: float | None = None, dq: torch.Tensor | None = None,
+        dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, stream=None):
+    """dQ, dK, dV (CUDA fp32 [B, H, S, D]) of block-sparse attention.
+
+    q/k/v/dout: CUDA bf16 [B, H, S, D], contiguous; o, lse: the forward's
+    outputs for plan p; scale: the forward's scale."""
+    for t in (q, k, v, dout):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16):
+            raise TypeError("q, k, v, dout must be CUDA bf16 tensors")
+        if not t.is_contiguous():
+            raise ValueError("q, k, v, dout must be contiguous")
+    if q.dim() != 4 or any(t.shape != q.shape for t in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share the shape [B, H, S, D]")
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    odt = torch.float32 if p.out_f32 else torch.bfloat16
+    if o.dtype != odt or o.shape != q.shape or not o.is_contiguous():
+        raise ValueError("o has the wrong dtype/shape/layout for this plan")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, S]")
+    grads = []
+    for g in (dq, dk, dv):
+        if g is None:
+            g = torch.empty((B, H, S, D), dtype=torch.float32, device=q.device)
+        if g.dtype != torch.float32 or g.shape != q.shape or not g.is_contiguous():
+            raise ValueError("dq, dk, dv must be contiguous fp32 [B, H, S, D]")
+        grads.append(g)
+    vp = ctypes.c_void_p
+    with torch.cuda.device(q.device):
+        _check(load().bsattn_bwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
+                                 vp(o.data_ptr()), vp(lse.data_ptr()), vp(dout.data_ptr()),
+                                 p.handle, vp(grads[0].data_ptr()), vp(grads[1].data_ptr()),
+                                 vp(grads[2].data_ptr()), B, H, S, D, float(scale),
+                                 _stream_handle(stream)), "bsattn_bwd")
+    return tuple(grads)
+
+
 def plan_status(p: Plan, stream=None) -> None:
     """Wait for the stream; raise if a kernel reported a timeout or internal error."""
     _check(load().bsattn_plan_status(p.handle, _stream_handle(stream)), "device status")
@@ -206,6 +251,15 @@ def plan_csr(p: Plan):
            "bsattn_plan_csr")
     rows = p.B * p.H * (p.S // BLOCK)
     return _view_i32(rp.value, rows + 1), _view_i32(ci.value, nnz.value)
+
+
+def plan_csc(p: Plan):
+    """(col_ptr, row_idx) of the transposed plan as fresh CUDA int32 tensors."""
+    cp, ri, nnz = ctypes.c_void_p(), ctypes.c_void_p(), ctypes.c_int64()
+    _check(load().bsattn_plan_csc(p.handle, ctypes.byref(cp), ctypes.byref(ri), ctypes.byref(nnz)),
+           "bsattn_plan_csc")
+    cols = p.B * p.H * (p.S // BLOCK)
+    return _view_i32(cp.value, cols + 1), _view_i32(ri.value, nnz.value)
 
 
 def plan_schedule(p: Plan):

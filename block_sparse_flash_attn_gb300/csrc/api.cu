@@ -93,6 +93,9 @@ void free_plan_memory(bsattn_plan_s* p) {
   cudaFree(p->dev.tile_order);
   cudaFree(p->dev.empty_tiles);
   cudaFree(p->dev.work);
+  cudaFree(p->dev.col_ptr);
+  cudaFree(p->dev.row_idx);
+  cudaFree(p->dev.dl);
   p->dev = PlanDevice{};
 }
 
@@ -239,6 +242,18 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
                                device_sm_count(p->device), st)) !=
       cudaSuccess)
     return fail(from_cuda(e));
+  // Transposed plan for the backward pass (same number of live blocks) and
+  // its per-row scratch; d_counts is free again once the CSR is built.
+  if ((e = cudaMalloc(&p->dev.col_ptr, sizeof(int) * ((size_t)rows + 1))) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&p->dev.row_idx, sizeof(int) * (size_t)(p->nnz > 0 ? p->nnz : 1))) !=
+      cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = cudaMalloc(&p->dev.dl, sizeof(float) * (size_t)B * H * S)) != cudaSuccess)
+    return fail(from_cuda(e));
+  if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st)) !=
+      cudaSuccess)
+    return fail(from_cuda(e));
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
   cudaFree(tmp);
   tmp = nullptr;
@@ -252,6 +267,15 @@ bsattn_status bsattn_plan_csr(bsattn_plan_t plan, const int32_t** d_row_ptr,
   if (!plan_ok(plan) || !d_row_ptr || !d_col_idx || !nnz) return BSATTN_ERR_INVALID_ARG;
   *d_row_ptr = plan->dev.row_ptr;
   *d_col_idx = plan->dev.col_idx;
+  *nnz = plan->nnz;
+  return BSATTN_OK;
+}
+
+bsattn_status bsattn_plan_csc(bsattn_plan_t plan, const int32_t** d_col_ptr,
+                              const int32_t** d_row_idx, int64_t* nnz) {
+  if (!plan_ok(plan) || !d_col_ptr || !d_row_idx || !nnz) return BSATTN_ERR_INVALID_ARG;
+  *d_col_ptr = plan->dev.col_ptr;
+  *d_row_idx = plan->dev.row_idx;
   *nnz = plan->nnz;
   return BSATTN_OK;
 }
@@ -275,6 +299,50 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
   const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf);
   if (rc != BSATTN_OK) return rc;
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
+}
+
+bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
+                         float* dk, float* dv, int B, int H, int S, int D, float scale,
+                         void* stream) {
+  if (!plan_ok(plan)) return BSATTN_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return BSATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return BSATTN_ERR_INVALID_ARG;
+  if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
+  if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
+  const long long rows = (long long)B * H * S;
+  CUtensorMap tq, tk, tv, tdo;
+  bsattn_status rc;
+  if ((rc = encode_bf16_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tdo, dout, D, rows)) != BSATTN_OK) return rc;
+  BwdParams prm{};
+  prm.col_ptr = plan->dev.col_ptr;
+  prm.row_idx = plan->dev.row_idx;
+  prm.lse = lse;
+  prm.dl = plan->dev.dl;
+  prm.dq = dq;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.status = plan->dev.work + kWorkStatus;
+  prm.nb = plan->nb;
+  prm.S = S;
+  prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
+  prm.scale = scale;
+  prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
+  prm.timeout_ns = kDefaultWaitTimeoutNs;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_bwd_prep(D, (plan->flags & BSATTN_OUT_F32) != 0, o, dout, plan->dev.dl,
+                                  dq, rows, st);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_bwd(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st));
 }
 
 bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {

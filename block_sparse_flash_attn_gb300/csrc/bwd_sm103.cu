@@ -1,0 +1,467 @@
+// Block-sparse flash-attention backward for sm_103a (GB300).
+//
+// What it computes: the gradients dQ, dK, dV of the forward operation
+// O = softmax(scale * Q K^T + mask) V over the same live blocks.  "Writing
+// Pallas Kernels for JAX: Stepping Outside the XLA Safety Net" (section "The
+// Empathy of the Void") notes that a hand-written attention kernel needs its
+// own gradient definitions; these are the derivative of that article's
+// forward operation (sections "Designing the Block Specification" and
+// "Writing the Kernel Logic: Load, Compute, Store"), formed blockwise the way
+// flash attention forms the exact softmax ("Pallas-Triton kernels and kernel
+// auto-tuning", section "Flash Attention"):
+//
+//   P_ij  = exp(scale q_i.k_j - LSE_i)         (recomputed from the saved LSE)
+//   dP_ij = dO_i . v_j,   Dl_i = dO_i . O_i,   dS_ij = P_ij (dP_ij - Dl_i)
+//   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
+//
+// GB300 design: one CTA per key tile (128 keys of one (batch, head)), 128
+// threads, one thread per TMEM lane.  The CTA walks the plan's transposed
+// list (the live query blocks of its key block) and keeps dV and dK in tensor
+// memory for the whole walk; dQ is added into an fp32 buffer with vector
+// reductions (several key tiles contribute to each query row).  Per query
+// block, with the scores transposed so that keys are TMEM lanes:
+//   S^T  = K Q^T, dP^T = V dO^T                      (tcgen05, both operands in smem)
+//   P^T = 2^(S^T scale log2 e - LSE log2 e), dS^T = P^T (dP^T - Dl)  (CUDA cores)
+//   P^T (bf16) goes back to tensor memory over S^T; dS^T (bf16) to shared memory
+//   dV += P^T dO   (A from tensor memory, B = dO read MN-major)
+//   dK += dS^T Q   (A = dS^T K-major, B = Q read MN-major)
+//   dQ_part = dS K (A = the same dS^T tile read MN-major, B = K read MN-major)
+// Q and dO are double-buffered: the next query block's tiles load while the
+// current one is processed.  Every mbarrier wait is bounded; on expiry the
+// status word records a timeout and the CTA drains its copies and MMAs before
+// it frees tensor memory.
+#include <atomic>
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace bsattn {
+namespace {
+
+constexpr int kBwdThreads = 128;
+constexpr uint32_t kBwdTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634074f;
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
+  static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
+  static constexpr int kKOff = 0;
+  static constexpr int kVOff = kKOff + kTileBytes;
+  static constexpr int kQOff = kVOff + kTileBytes;     // two buffers
+  static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // two buffers
+  static constexpr int kdSOff = kdOOff + 2 * kTileBytes;  // 128 x 128 bf16: two boxes
+  static constexpr int kVecOff = kdSOff + 2 * kBoxBytes;  // LSE log2 e [128], Dl [128]
+  static constexpr int kBarOff = kVecOff + 2 * kBlock * 4;
+  static constexpr int kSmem = kBarOff + 256;
+  // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 queries, both K-major
+  static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);
+  // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, B MN-major
+  static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, true);
+  // dQ_part = dS K: M = 128 queries, N = D, A and B MN-major
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true, true);
+  // tensor-memory columns
+  static constexpr uint32_t kTS = 0;         // S^T (fp32), then P^T (bf16) in [0, 64)
+  static constexpr uint32_t kTdP = 128;      // dP^T (fp32), then dQ_part (fp32, D columns)
+  static constexpr uint32_t kTdV = 256;      // dV accumulator (D columns)
+  static constexpr uint32_t kTdK = 256 + D;  // dK accumulator (D columns)
+};
+static_assert(BwdCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
+static_assert(BwdCfg<128>::kTdK + 128 <= kBwdTmemCols, "tensor memory exceeded");
+
+struct __align__(8) BwdBars {
+  uint64_t kv_full;      // K and V of the key tile loaded
+  uint64_t qd_full[2];   // Q and dO of a query block loaded (by buffer)
+  uint64_t st_done;      // S^T and dP^T computed
+  uint64_t grad_done;    // dV, dK updated and dQ_part computed
+  uint64_t drain;        // every MMA issued so far complete
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+// Dl_i = dO_i . O_i (fp32 over the stored O and dO) and dQ_i = 0; one warp per row.
+template <int D, bool O_F32>
+__global__ void bwd_prep_kernel(const void* __restrict__ o, const uint16_t* __restrict__ dout,
+                                float* __restrict__ dl, float* __restrict__ dq, long long rows) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int kPer = D / 32;  // elements per lane: 4 (D = 128) or 2 (D = 64)
+  const size_t base = (size_t)row * D + (size_t)lane * kPer;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) {
+    const float g = __uint_as_float((uint32_t)dout[base + e] << 16);
+    float x;
+    if constexpr (O_F32)
+      x = reinterpret_cast<const float*>(o)[base + e];
+    else
+      x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(o)[base + e] << 16);
+    acc = fmaf(g, x, acc);
+    dq[base + e] = 0.f;
+  }
+  acc += __shfl_xor_sync(0xffffffffu, acc, 16);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 8);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  if (lane == 0) dl[row] = acc;
+}
+
+__device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status, uint64_t limit_ns) {
+  const bool ok = wait_bounded(bar, parity, abort_flag, status, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used while draining (no abort check: the copies and MMAs in
+// flight finish on their own; the limit only guards against a broken state).
+__device__ __forceinline__ void bwd_drain_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bsattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = BwdCfg<D>;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int tile = blockIdx.x;  // (b * H + h) * nb + kb
+  const int bh = tile / p.nb;
+  const int kb = tile - bh * p.nb;
+  const int c0 = p.col_ptr[tile];
+  const int n = p.col_ptr[tile + 1] - c0;
+  const int krow0 = bh * p.S + kb * kBlock;  // first key row of the tile
+  if (n <= 0) {  // no live query block: dK = dV = 0
+    float4* dk4 = reinterpret_cast<float4*>(p.dk + (size_t)krow0 * D);
+    float4* dv4 = reinterpret_cast<float4*>(p.dv + (size_t)krow0 * D);
+    for (int i = tid; i < kBlock * D / 4; i += kBwdThreads) {
+      dk4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+  // The plan's list must hold valid query blocks; anything else is an internal error.
+  bool bad = n > p.nb;
+  for (int i = tid; !bad && i < n; i += kBwdThreads) {
+    const int qb = p.row_idx[c0 + i];
+    bad = qb < 0 || qb >= p.nb || (p.causal && qb < kb);
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) atomicOr(p.status, kStatusInternal);
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw + (base - raw) + C::kBarOff);
+  float* sL = reinterpret_cast<float*>(smem_raw + (base - raw) + C::kVecOff);  // LSE log2 e
+  float* sD = sL + kBlock;                                                     // Dl
+  const uint64_t lim = p.timeout_ns;
+  volatile int* abort_flag = &bars->abort_flag;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars->kv_full), 1);
+    mbar_init(smem_u32(&bars->qd_full[0]), 1);
+    mbar_init(smem_u32(&bars->qd_full[1]), 1);
+    mbar_init(smem_u32(&bars->st_done), 1);
+    mbar_init(smem_u32(&bars->grad_done), 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+
+  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+    for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+  };
+  // Q and dO of query block number i of the list into buffer i % 2 (thread 0).
+  auto load_qd = [&](int i) {
+    const int b = i & 1;
+    const uint32_t bar = smem_u32(&bars->qd_full[b]);
+    const int row = bh * p.S + p.row_idx[c0 + i] * kBlock;
+    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+    load_tile(&tm_q, base + C::kQOff + b * C::kTileBytes, bar, row);
+    load_tile(&tm_do, base + C::kdOOff + b * C::kTileBytes, bar, row);
+  };
+
+  int n_issued = 0, n_waited = 0;  // (thread 0 / warp 0) Q-dO loads issued and awaited
+  bool kv_waited = false;
+  if (tid == 0) {
+    const uint32_t bar = smem_u32(&bars->kv_full);
+    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+    load_tile(&tm_k, base + C::kKOff, bar, krow0);
+    load_tile(&tm_v, base + C::kVOff, bar, krow0);
+    load_qd(0);
+  }
+  n_issued = 1;
+  // this thread's row of LSE (log2 units) and Dl for the next query block
+  int qrow = bh * p.S + p.row_idx[c0] * kBlock + tid;
+  float lse_next = p.lse[qrow] * kLog2e;
+  float dl_next = p.dl[qrow];
+
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const int qb = p.row_idx[c0 + j];
+    const int b = j & 1;
+    sL[tid] = lse_next;
+    sD[tid] = dl_next;
+    if (j + 1 < n) {
+      // the other buffer was last read by the previous block's MMAs, which are complete
+      if (tid == 0) load_qd(j + 1);
+      n_issued = j + 2;
+      qrow = bh * p.S + p.row_idx[c0 + j + 1] * kBlock + tid;
+      lse_next = p.lse[qrow] * kLog2e;
+      dl_next = p.dl[qrow];
+    }
+    __syncthreads();  // sL, sD written
+
+    // S^T = K Q^T and dP^T = V dO^T (keys are the TMEM lanes)
+    if (warp == 0) {
+      bool w = kv_waited || bwd_wait(smem_u32(&bars->kv_full), 0, abort_flag, p.status, lim);
+      kv_waited = kv_waited || w;
+      w = w && bwd_wait(smem_u32(&bars->qd_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
+                        lim);
+      if (w) {
+        n_waited = j + 1;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t kd = smem_desc_sw128(base + C::kKOff, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(base + C::kVOff, 16, 1024);
+          const uint64_t qd = smem_desc_sw128(base + C::kQOff + b * C::kTileBytes, 16, 1024);
+          const uint64_t dd = smem_desc_sw128(base + C::kdOOff + b * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kTS, kd + off, qd + off, C::kIdescT, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kTdP, vd + off, dd + off, C::kIdescT, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->st_done));
+        }
+        __syncwarp();
+      }
+      ok = w;
+    }
+    if (ok) ok = bwd_wait(smem_u32(&bars->st_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+
+    // P^T and dS^T, one key row (TMEM lane) per thread, 32 queries at a time.
+    // P^T (bf16 pairs, queries 2c and 2c+1 in column c) goes over the scores
+    // already read; dS^T (bf16) goes to shared memory, 128-byte swizzled like
+    // a TMA tile: row r, 16-byte chunk c of 64-query box x at
+    // x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16).
+    {
+      const bool diag = p.causal && qb == kb;  // key r is allowed for query q iff r <= q
+      const int r = tid;
+      const float sl = p.scale_log2;
+      const uint32_t tS = tmem + C::kTS + lane_off;
+      const uint32_t tdP = tmem + C::kTdP + lane_off;
+      const uint32_t sdS = base + C::kdSOff;
+#pragma unroll 1
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tS + ch * 32, s);
+        tmem_ld32(tdP + ch * 32, dp);
+        tmem_wait_ld();
+        reg_fence(s, 32);
+        reg_fence(dp, 32);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int q = ch * 32 + i;
+          float p0 = ex2_approx(fmaf(__uint_as_float(s[i]), sl, -sL[q]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(s[i + 1]), sl, -sL[q + 1]));
+          if (diag) {
+            p0 = r > q ? 0.f : p0;
+            p1 = r > q + 1 ? 0.f : p1;
+          }
+          const float d0 = p0 * (__uint_as_float(dp[i]) - sD[q]);
+          const float d1 = p1 * (__uint_as_float(dp[i + 1]) - sD[q + 1]);
+          pk[i >> 1] = pack_bf16x2(p0, p1);
+          dk[i >> 1] = pack_bf16x2(d0, d1);
+        }
+        tmem_st32_16(tS + ch * 16, pk);
+        const uint32_t rowa = sdS + (uint32_t)(ch >> 1) * C::kBoxBytes + (uint32_t)r * 128u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t c = (uint32_t)((ch & 1) * 4 + u);
+          st_shared_v4(rowa + ((c ^ (uint32_t)(r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
+                       dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+    }
+    __syncthreads();  // P^T in tensor memory, dS^T in shared memory
+
+    // dV += P^T dO, dK += dS^T Q (K = 128 queries), dQ_part = dS K (K = 128 keys)
+    if (warp == 0) {
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t qoff = base + C::kQOff + b * C::kTileBytes;
+        const uint32_t dooff = base + C::kdOOff + b * C::kTileBytes;
+        const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
+        const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
+        const uint64_t k_mn = smem_desc_sw128(base + C::kKOff, C::kBoxBytes, 1024);
+        const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
+        const uint64_t ds_mn = smem_desc_sw128(base + C::kdSOff, C::kBoxBytes, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
+          const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+          mma_ts(tmem + C::kTdV, tmem + C::kTS + kk * 8, do_mn + mn, C::kIdescKV, acc);
+          mma_ss(tmem + C::kTdK, ds_k + km, q_mn + mn, C::kIdescKV, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
+          mma_ss(tmem + C::kTdP, ds_mn + mn, k_mn + mn, C::kIdescQ, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->grad_done));
+      }
+      __syncwarp();
+    }
+    ok = bwd_wait(smem_u32(&bars->grad_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+
+    // dQ rows of this query block += scale * dQ_part (one query row per thread)
+    {
+      float* dqr = p.dq + (size_t)(bh * p.S + qb * kBlock + tid) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + C::kTdP + lane_off + c, v);
+        tmem_wait_ld();
+        reg_fence(v, 32);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          red_add_v4(dqr + c + i, __uint_as_float(v[i]) * p.scale,
+                     __uint_as_float(v[i + 1]) * p.scale, __uint_as_float(v[i + 2]) * p.scale,
+                     __uint_as_float(v[i + 3]) * p.scale);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();  // S^T / dP^T columns and sL / sD free for the next block
+  }
+
+  // Drain: every copy issued and every MMA issued completes before tensor
+  // memory is freed and the CTA exits.
+  if (warp == 0) {
+    if (!kv_waited) bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
+    for (int i = n_waited; i < n_issued; ++i)
+      bwd_drain_wait(smem_u32(&bars->qd_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+    if (elect_one()) mma_commit(smem_u32(&bars->drain));
+    __syncwarp();
+    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (ok) {  // dV and dK (times scale), one key row per thread
+    float* dvr = p.dv + (size_t)(krow0 + tid) * D;
+    float* dkr = p.dk + (size_t)(krow0 + tid) * D;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      uint32_t v[32], k[32];
+      tmem_ld32(tmem + C::kTdV + lane_off + c, v);
+      tmem_ld32(tmem + C::kTdK + lane_off + c, k);
+      tmem_wait_ld();
+      reg_fence(v, 32);
+      reg_fence(k, 32);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        st_global_v4(dvr + c + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
+        st_global_v4(dkr + c + i, __float_as_uint(__uint_as_float(k[i]) * p.scale),
+                     __float_as_uint(__uint_as_float(k[i + 1]) * p.scale),
+                     __float_as_uint(__uint_as_float(k[i + 2]) * p.scale),
+                     __float_as_uint(__uint_as_float(k[i + 3]) * p.scale));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdParams& p, int grid,
+                         cudaStream_t stream) {
+  static std::atomic<bool> opted_in[64];
+  const size_t smem = BwdCfg<D>::kSmem + 1024;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(bsattn_bwd_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    opted_in[dev].store(true, std::memory_order_release);
+  }
+  bsattn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
+                            float* dq, long long rows, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
+  const uint16_t* g = static_cast<const uint16_t*>(dout);
+  if (D == 128) {
+    if (o_f32) bwd_prep_kernel<128, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+    else bwd_prep_kernel<128, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+  } else {
+    if (o_f32) bwd_prep_kernel<64, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+    else bwd_prep_kernel<64, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  return D == 128 ? launch_bwd_t<128>(tq, tk, tv, tdo, p, grid, stream)
+                  : launch_bwd_t<64>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+}  // namespace bsattn

@@ -26,6 +26,11 @@ struct PlanDevice {
   int* tile_order = nullptr;   // [n_live] non-empty tiles, head-major, longest first
   int* empty_tiles = nullptr;  // [n_empty]
   int* work = nullptr;         // [kWorkWords] tile counter, status word
+  // transposed plan: per key block c = (b*H + h)*nb + kb, the ascending live
+  // query blocks row_idx[col_ptr[c] .. col_ptr[c+1])
+  int* col_ptr = nullptr;      // [R + 1]
+  int* row_idx = nullptr;      // [nnz]
+  float* dl = nullptr;         // [B*H*S] backward scratch: dO_i . O_i
 };
 
 // Everything the forward kernel needs besides the three tensor maps.
@@ -46,6 +51,24 @@ struct FwdParams {
   float scale_log2;  // |scale| * log2(e) (> 0; a tiny positive value stands in for scale = 0)
   int neg_scale;     // scale < 0: the S MMA computes -Q K^T
   int causal;
+  unsigned long long timeout_ns;
+};
+
+// Everything the backward kernel needs besides its four tensor maps.
+struct BwdParams {
+  const int* col_ptr;
+  const int* row_idx;
+  const float* lse;  // natural-log LSE of the forward pass
+  const float* dl;   // dO_i . O_i
+  float* dq;         // fp32, zeroed by the preparation kernel, accumulated by reductions
+  float* dk;
+  float* dv;
+  int* status;
+  int nb;
+  int S;
+  int causal;
+  float scale;
+  float scale_log2;  // scale * log2(e), signed
   unsigned long long timeout_ns;
 };
 
@@ -82,6 +105,10 @@ cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causa
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
                                 int* d_tile_order, int* d_empty_tiles, int nsm,
                                 cudaStream_t stream);
+// Transposed plan (per key block, the ascending live query blocks); d_counts
+// is scratch of R ints.
+cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
+                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream);
 // Heads per schedule chunk for S/128 = nb key blocks per head.
 int schedule_chunk_heads(int nb);
 
@@ -91,5 +118,11 @@ cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtenso
 size_t fwd_smem_bytes(int D);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
                                  cudaStream_t stream);
+
+// bwd_sm103.cu
+cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
+                            float* dq, long long rows, cudaStream_t stream);
+cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
 
 }  // namespace bsattn

@@ -15,6 +15,8 @@
 // count descending (longest-processing-time first), with the few tiles that
 // are long for their chunk moved one chunk earlier (see order_kernel); empty
 // tiles listed separately (the forward kernel writes O = 0, LSE = -inf there).
+// The transposed plan (col_ptr / row_idx: per key block, the ascending live
+// query blocks) drives the backward kernel, one CTA per key block.
 #include <cstdint>
 
 #include "internal.h"
@@ -198,6 +200,49 @@ __global__ void __launch_bounds__(1024)
   }
 }
 
+// Transposed plan, one warp per key block c = (b*H + h)*nb + kb: the query
+// blocks qb with mask[b][h][qb][kb] != 0 (and qb >= kb when causal).
+__device__ __forceinline__ bool col_live(const uint8_t* mask_bh, int nb, int qb, int kb,
+                                         int causal) {
+  return mask_bh[(size_t)qb * nb + kb] != 0 && (!causal || qb >= kb);
+}
+
+__global__ void csc_count_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
+                                 int* __restrict__ counts) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= cols) return;
+  const int kb = warp % nb;
+  const uint8_t* mbh = mask + (size_t)(warp / nb) * nb * nb;
+  int c = 0;
+  for (int qb = lane; qb < nb; qb += 32) c += col_live(mbh, nb, qb, kb, causal) ? 1 : 0;
+  c = __reduce_add_sync(0xffffffffu, c);
+  if (lane == 0) counts[warp] = c;
+}
+
+__global__ void __launch_bounds__(kScanThreads)
+    csc_scan_kernel(const int* __restrict__ counts, int cols, int* __restrict__ col_ptr) {
+  __shared__ long long sh[kScanThreads];
+  block_exclusive_scan(counts, col_ptr, cols, sh);
+}
+
+__global__ void csc_fill_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
+                                const int* __restrict__ col_ptr, int* __restrict__ row_idx) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= cols) return;
+  const int kb = warp % nb;
+  const uint8_t* mbh = mask + (size_t)(warp / nb) * nb * nb;
+  int pos = col_ptr[warp];
+  for (int q0 = 0; q0 < nb; q0 += 32) {
+    const int qb = q0 + lane;
+    const bool live = qb < nb && col_live(mbh, nb, qb, kb, causal);
+    const unsigned bal = __ballot_sync(0xffffffffu, live);
+    if (live) row_idx[pos + __popc(bal & ((1u << lane) - 1u))] = qb;
+    pos += __popc(bal);
+  }
+}
+
 }  // namespace
 
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
@@ -233,6 +278,18 @@ cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causa
   while (n2 < 2 * kh * nb) n2 <<= 1;
   order_kernel<<<chunks, 1024, sizeof(uint32_t) * n2, stream>>>(
       d_row_ptr, d_live_off, BH, nb, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles);
+  return cudaGetLastError();
+}
+
+cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
+                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream) {
+  const int cols = BH * nb;
+  const int warps_per_block = 8;
+  const int grid = (cols + warps_per_block - 1) / warps_per_block;
+  csc_count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, d_counts);
+  csc_scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, cols, d_col_ptr);
+  csc_fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, d_col_ptr,
+                                                             d_row_idx);
   return cudaGetLastError();
 }
 

@@ -97,6 +97,13 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
 bsattn_status bsattn_plan_csr(bsattn_plan_t plan, const int32_t** d_row_ptr,
                               const int32_t** d_col_idx, int64_t* nnz);
 
+/* Device pointers to the plan's transposed list (col_ptr: B*H*S/128 + 1
+   int32 indexed by key block (b*H + h)*nb + kb; row_idx: nnz int32, the
+   ascending live query blocks of each key block) and its size; valid until
+   bsattn_plan_free.  For tests/tools. */
+bsattn_status bsattn_plan_csc(bsattn_plan_t plan, const int32_t** d_col_ptr,
+                              const int32_t** d_row_idx, int64_t* nnz);
+
 /* Device pointers to the schedule: non-empty tile ids in processing order
    (n_live int32) and empty tile ids (n_empty int32).  For tests/tools. */
 bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_order,
@@ -123,6 +130,37 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
  */
 bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                          void* out, float* lse, int B, int H, int S, int D, float scale,
+                         void* stream);
+
+/*
+ * bsattn_bwd -- dQ, dK, dV: gradients of bsattn_fwd's O with respect to Q, K, V,
+ * given the upstream gradient dO.  "Writing Pallas Kernels for JAX: Stepping
+ * Outside the XLA Safety Net" (section "The Empathy of the Void") asks for
+ * hand-written gradient definitions; these are the exact derivative of the
+ * forward operation over the plan's live blocks:
+ *   P = softmax of the scaled, masked scores (recomputed from lse),
+ *   dS = P * (dO V^T - rowsum(dO * O)),
+ *   dQ = scale dS K,  dK = scale dS^T Q,  dV = P^T dO.
+ *
+ *   q, k, v    device bf16 [B][H][S][D], the forward's inputs, 16-byte aligned.
+ *   o, lse     the forward's outputs for the same plan: o bf16 (or fp32 when the
+ *              plan has BSATTN_OUT_F32) [B][H][S][D], lse fp32 [B][H][S].
+ *   dout       device bf16 [B][H][S][D]: the upstream gradient dO.
+ *   plan       from bsattn_plan with the same B, H, S (its transposed list is used).
+ *   dq, dk, dv device fp32 [B][H][S][D], 16-byte aligned, written in full (rows
+ *              of query tiles with no live key block get dQ = 0, key blocks no
+ *              query attends get dK = dV = 0).
+ *   D, scale   as in bsattn_fwd (the same scale as the forward call).
+ *   stream     cudaStream_t; stream-ordered, never synchronises.
+ * Uses the plan's workspace (status word, a B*H*S fp32 scratch row term), so
+ * calls with the same plan must not overlap on the GPU; a kernel-side failure
+ * is returned by bsattn_plan_status.
+ * Errors: INVALID_ARG (null/misaligned, sizes differ from the plan, non-finite
+ * scale), UNSUPPORTED (D), CUDA (launch failure).
+ */
+bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
+                         float* dk, float* dv, int B, int H, int S, int D, float scale,
                          void* stream);
 
 /* Wait for `stream`, then report and clear the device-side status of the

@@ -39,6 +39,7 @@ BLOCK = 128
 
 # stream ids inside one seed
 STREAM_Q, STREAM_K, STREAM_V = 1, 2, 3
+STREAM_DO = 4  # upstream gradient dO of the backward pass
 STREAM_MASK_IID, STREAM_MASK_BIGBIRD = 10, 11
 
 
@@ -223,3 +224,8 @@ def custom(seed: int, B: int, H: int, S: int, D: int, mult: float = 1.0):
     """Q, K, V bit patterns for an ad-hoc shape (edge-case tests)."""
     shape = (B, H, S, D)
     return tuple(normal_bf16(seed, s, shape, mult) for s in (STREAM_Q, STREAM_K, STREAM_V))
+
+
+def upstream_grad(seed: int, B: int, H: int, S: int, D: int, mult: float = 1.0):
+    """dO bit patterns (bf16, N(0,1) * mult) for the backward pass."""
+    return normal_bf16(seed, STREAM_DO, (B, H, S, D), mult)
