@@ -326,6 +326,8 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
   BwdParams prm{};
   prm.col_ptr = plan->dev.col_ptr;
   prm.row_idx = plan->dev.row_idx;
+  prm.row_ptr = plan->dev.row_ptr;
+  prm.col_idx = plan->dev.col_idx;
   prm.lse = lse;
   prm.dl = plan->dev.dl;
   prm.dq = dq;
@@ -340,9 +342,11 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
   prm.timeout_ns = kDefaultWaitTimeoutNs;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_prep(D, (plan->flags & BSATTN_OUT_F32) != 0, o, dout, plan->dev.dl,
-                                  dq, rows, st);
+                                  rows, st);
   if (e != cudaSuccess) return from_cuda(e);
-  return from_cuda(launch_bwd(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st));
+  if ((e = launch_bwd(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st)) != cudaSuccess)
+    return from_cuda(e);
+  return from_cuda(launch_bwd_dq(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st));
 }
 
 bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {

@@ -14,22 +14,32 @@
 //   dP_ij = dO_i . v_j,   Dl_i = dO_i . O_i,   dS_ij = P_ij (dP_ij - Dl_i)
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
 //
-// GB300 design: one CTA per key tile (128 keys of one (batch, head)), 128
-// threads, one thread per TMEM lane.  The CTA walks the plan's transposed
+// GB300 design: two kernels, neither with atomics (several key tiles feed
+// each dQ row and several query tiles each dK/dV row; fp32 reductions for
+// either were measured to bound the whole pass by L2 atomic throughput).
+//
+// bsattn_bwd_kernel (dK, dV): one CTA per key tile (128 keys of one (batch,
+// head)), 256 threads: two warps per TMEM sub-partition, each thread one key
+// row (TMEM lane) and half of the columns.  It walks the plan's transposed
 // list (the live query blocks of its key block) and keeps dV and dK in tensor
-// memory for the whole walk; dQ is added into an fp32 buffer with vector
-// reductions (several key tiles contribute to each query row).  Per query
-// block, with the scores transposed so that keys are TMEM lanes:
-//   S^T  = K Q^T, dP^T = V dO^T                      (tcgen05, both operands in smem)
-//   P^T = 2^(S^T scale log2 e - LSE log2 e), dS^T = P^T (dP^T - Dl)  (CUDA cores)
-//   P^T (bf16) goes back to tensor memory over S^T; dS^T (bf16) to shared memory
+// memory.  Per query block, with keys as TMEM lanes:
+//   S^T = K Q^T, dP^T = V dO^T                         (tcgen05, operands in smem)
+//   P^T = 2^(S^T scale log2 e - LSE log2 e), dS^T = P^T (dP^T - Dl)   (CUDA cores)
+//   P^T (bf16) goes back to tensor memory over S^T (queries 0-63 at columns
+//   0-31, 64-127 at 64-95: each half writes inside the scores it read);
+//   dS^T (bf16) goes to shared memory
 //   dV += P^T dO   (A from tensor memory, B = dO read MN-major)
-//   dK += dS^T Q   (A = dS^T K-major, B = Q read MN-major)
-//   dQ_part = dS K (A = the same dS^T tile read MN-major, B = K read MN-major)
+//   dK += dS^T Q   (A = dS^T, B = Q read MN-major)
 // Q and dO are double-buffered: the next query block's tiles load while the
-// current one is processed.  Every mbarrier wait is bounded; on expiry the
-// status word records a timeout and the CTA drains its copies and MMAs before
-// it frees tensor memory.
+// current one is processed.
+//
+// bsattn_bwd_dq_kernel (dQ): one CTA per query tile, walking the forward
+// plan's list of live key blocks with queries as TMEM lanes: S = Q K^T and
+// dP = dO V^T recomputed, dS = P (dP - Dl) to shared memory, dQ += dS K in
+// tensor memory (K and V double-buffered), dQ written once at the end.
+//
+// Every mbarrier wait is bounded; on expiry the status word records a
+// timeout and the CTA drains its copies and MMAs before it frees tensor memory.
 #include <atomic>
 #include <cstdint>
 
@@ -39,7 +49,7 @@
 namespace bsattn {
 namespace {
 
-constexpr int kBwdThreads = 128;
+constexpr int kBwdThreads = 256;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634074f;
 
@@ -60,11 +70,9 @@ struct BwdCfg {
   static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);
   // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, B MN-major
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, true);
-  // dQ_part = dS K: M = 128 queries, N = D, A and B MN-major
-  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true, true);
   // tensor-memory columns
-  static constexpr uint32_t kTS = 0;         // S^T (fp32), then P^T (bf16) in [0, 64)
-  static constexpr uint32_t kTdP = 128;      // dP^T (fp32), then dQ_part (fp32, D columns)
+  static constexpr uint32_t kTS = 0;         // S^T (fp32), then P^T (bf16) in [0,32) and [64,96)
+  static constexpr uint32_t kTdP = 128;      // dP^T (fp32)
   static constexpr uint32_t kTdV = 256;      // dV accumulator (D columns)
   static constexpr uint32_t kTdK = 256 + D;  // dK accumulator (D columns)
 };
@@ -75,16 +83,16 @@ struct __align__(8) BwdBars {
   uint64_t kv_full;      // K and V of the key tile loaded
   uint64_t qd_full[2];   // Q and dO of a query block loaded (by buffer)
   uint64_t st_done;      // S^T and dP^T computed
-  uint64_t grad_done;    // dV, dK updated and dQ_part computed
+  uint64_t grad_done;    // dV and dK updated
   uint64_t drain;        // every MMA issued so far complete
   uint32_t tmem_base;
   int abort_flag;
 };
 
-// Dl_i = dO_i . O_i (fp32 over the stored O and dO) and dQ_i = 0; one warp per row.
+// Dl_i = dO_i . O_i (fp32 over the stored O and dO); one warp per row.
 template <int D, bool O_F32>
 __global__ void bwd_prep_kernel(const void* __restrict__ o, const uint16_t* __restrict__ dout,
-                                float* __restrict__ dl, float* __restrict__ dq, long long rows) {
+                                float* __restrict__ dl, long long rows) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -100,7 +108,6 @@ __global__ void bwd_prep_kernel(const void* __restrict__ o, const uint16_t* __re
     else
       x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(o)[base + e] << 16);
     acc = fmaf(g, x, acc);
-    dq[base + e] = 0.f;
   }
   acc += __shfl_xor_sync(0xffffffffu, acc, 16);
   acc += __shfl_xor_sync(0xffffffffu, acc, 8);
@@ -191,7 +198,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t lane_off = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lanes
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+  const int r = tid & (kBlock - 1);  // TMEM lane: key row
+  const int half = tid >> 7;         // which half of the columns this thread handles
 
   auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
 #pragma unroll
@@ -217,24 +226,32 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     load_qd(0);
   }
   n_issued = 1;
-  // this thread's row of LSE (log2 units) and Dl for the next query block
-  int qrow = bh * p.S + p.row_idx[c0] * kBlock + tid;
-  float lse_next = p.lse[qrow] * kLog2e;
-  float dl_next = p.dl[qrow];
+  // LSE (log2 units) and Dl of the next query block, one row per thread of
+  // the first half
+  float lse_next = 0.f, dl_next = 0.f;
+  if (half == 0) {
+    const int qrow = bh * p.S + p.row_idx[c0] * kBlock + r;
+    lse_next = p.lse[qrow] * kLog2e;
+    dl_next = p.dl[qrow];
+  }
 
   bool ok = true;
   for (int j = 0; j < n; ++j) {
     const int qb = p.row_idx[c0 + j];
     const int b = j & 1;
-    sL[tid] = lse_next;
-    sD[tid] = dl_next;
+    if (half == 0) {
+      sL[r] = lse_next;
+      sD[r] = dl_next;
+    }
     if (j + 1 < n) {
       // the other buffer was last read by the previous block's MMAs, which are complete
       if (tid == 0) load_qd(j + 1);
       n_issued = j + 2;
-      qrow = bh * p.S + p.row_idx[c0 + j + 1] * kBlock + tid;
-      lse_next = p.lse[qrow] * kLog2e;
-      dl_next = p.dl[qrow];
+      if (half == 0) {
+        const int qrow = bh * p.S + p.row_idx[c0 + j + 1] * kBlock + r;
+        lse_next = p.lse[qrow] * kLog2e;
+        dl_next = p.dl[qrow];
+      }
     }
     __syncthreads();  // sL, sD written
 
@@ -275,20 +292,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_after();
 
-    // P^T and dS^T, one key row (TMEM lane) per thread, 32 queries at a time.
-    // P^T (bf16 pairs, queries 2c and 2c+1 in column c) goes over the scores
-    // already read; dS^T (bf16) goes to shared memory, 128-byte swizzled like
-    // a TMA tile: row r, 16-byte chunk c of 64-query box x at
-    // x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16).
+    // P^T and dS^T, one key row (TMEM lane) and 64 queries per thread, 32 at
+    // a time.  P^T (bf16 pairs) goes over the scores this thread's half has
+    // already read: queries 64h + 2c, 64h + 2c + 1 in column 64h + c.  dS^T
+    // (bf16) goes to shared memory, 128-byte swizzled like a TMA tile: row r,
+    // 16-byte chunk c of 64-query box x at x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16).
     {
       const bool diag = p.causal && qb == kb;  // key r is allowed for query q iff r <= q
-      const int r = tid;
       const float sl = p.scale_log2;
       const uint32_t tS = tmem + C::kTS + lane_off;
       const uint32_t tdP = tmem + C::kTdP + lane_off;
       const uint32_t sdS = base + C::kdSOff;
 #pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
         uint32_t s[32], dp[32];
         tmem_ld32(tS + ch * 32, s);
         tmem_ld32(tdP + ch * 32, dp);
@@ -310,7 +326,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pk[i >> 1] = pack_bf16x2(p0, p1);
           dk[i >> 1] = pack_bf16x2(d0, d1);
         }
-        tmem_st32_16(tS + ch * 16, pk);
+        tmem_st32_16(tS + (uint32_t)(64 * (ch >> 1) + 16 * (ch & 1)), pk);
         const uint32_t rowa = sdS + (uint32_t)(ch >> 1) * C::kBoxBytes + (uint32_t)r * 128u;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -325,7 +341,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncthreads();  // P^T in tensor memory, dS^T in shared memory
 
-    // dV += P^T dO, dK += dS^T Q (K = 128 queries), dQ_part = dS K (K = 128 keys)
+    // dV += P^T dO, dK += dS^T Q (K = 128 queries)
     if (warp == 0) {
       tc_fence_after();
       if (elect_one()) {
@@ -333,21 +349,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t dooff = base + C::kdOOff + b * C::kTileBytes;
         const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
         const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
-        const uint64_t k_mn = smem_desc_sw128(base + C::kKOff, C::kBoxBytes, 1024);
         const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
-        const uint64_t ds_mn = smem_desc_sw128(base + C::kdSOff, C::kBoxBytes, 1024);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
           const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
           const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + C::kTdV, tmem + C::kTS + kk * 8, do_mn + mn, C::kIdescKV, acc);
+          const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // queries 16kk ..
+          mma_ts(tmem + C::kTdV, tmem + C::kTS + pcol, do_mn + mn, C::kIdescKV, acc);
           mma_ss(tmem + C::kTdK, ds_k + km, q_mn + mn, C::kIdescKV, acc);
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
-          mma_ss(tmem + C::kTdP, ds_mn + mn, k_mn + mn, C::kIdescQ, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars->grad_done));
       }
@@ -360,22 +370,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     tc_fence_after();
 
-    // dQ rows of this query block += scale * dQ_part (one query row per thread)
-    {
-      float* dqr = p.dq + (size_t)(bh * p.S + qb * kBlock + tid) * D;
-#pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + C::kTdP + lane_off + c, v);
-        tmem_wait_ld();
-        reg_fence(v, 32);
-#pragma unroll
-        for (int i = 0; i < 32; i += 4)
-          red_add_v4(dqr + c + i, __uint_as_float(v[i]) * p.scale,
-                     __uint_as_float(v[i + 1]) * p.scale, __uint_as_float(v[i + 2]) * p.scale,
-                     __uint_as_float(v[i + 3]) * p.scale);
-      }
-    }
     tc_fence_before();
     __syncthreads();  // S^T / dP^T columns and sL / sD free for the next block
   }
@@ -392,11 +386,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   __syncthreads();
   tc_fence_after();
-  if (ok) {  // dV and dK (times scale), one key row per thread
-    float* dvr = p.dv + (size_t)(krow0 + tid) * D;
-    float* dkr = p.dk + (size_t)(krow0 + tid) * D;
+  if (ok) {  // dV and dK (times scale), one key row and half of the columns per thread
+    float* dvr = p.dv + (size_t)(krow0 + r) * D;
+    float* dkr = p.dk + (size_t)(krow0 + r) * D;
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
+    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
       uint32_t v[32], k[32];
       tmem_ld32(tmem + C::kTdV + lane_off + c, v);
       tmem_ld32(tmem + C::kTdK + lane_off + c, k);
@@ -421,6 +415,292 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 }
 
+// dQ kernel layout: Q, dO once per tile; K and V double-buffered; dS with
+// queries as rows.
+template <int D>
+struct DqCfg {
+  static constexpr int kTileBytes = kBlock * D * 2;
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kBoxBytes = kBlock * 128;
+  static constexpr int kQOff = 0;
+  static constexpr int kdOOff = kTileBytes;
+  static constexpr int kKOff = 2 * kTileBytes;   // two buffers
+  static constexpr int kVOff = 4 * kTileBytes;   // two buffers
+  static constexpr int kdSOff = 6 * kTileBytes;  // 128 queries x 128 keys bf16: two boxes
+  static constexpr int kBarOff = kdSOff + 2 * kBoxBytes;
+  static constexpr int kSmem = kBarOff + 256;
+  // S = Q K^T and dP = dO V^T: M = 128 queries, N = 128 keys, both K-major
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
+  // dQ += dS K: M = 128 queries, N = D, B (K) read MN-major
+  static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true);
+  static constexpr uint32_t kTS = 0;     // S (fp32)
+  static constexpr uint32_t kTdP = 128;  // dP (fp32)
+  static constexpr uint32_t kTdQ = 256;  // dQ accumulator (D columns)
+};
+static_assert(DqCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
+
+struct __align__(8) DqBars {
+  uint64_t qd_full;     // Q and dO of the tile loaded
+  uint64_t kv_full[2];  // K and V of a key block loaded (by buffer)
+  uint64_t st_done;     // S and dP computed
+  uint64_t grad_done;   // dQ updated
+  uint64_t drain;       // every MMA issued so far complete
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bsattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v,
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  using C = DqCfg<D>;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int tile = blockIdx.x;  // (b * H + h) * nb + qb
+  const int bh = tile / p.nb;
+  const int qb = tile - bh * p.nb;
+  const int r0 = p.row_ptr[tile];
+  const int n = p.row_ptr[tile + 1] - r0;
+  const int qrow0 = bh * p.S + qb * kBlock;  // first query row of the tile
+  if (n <= 0) {  // no live key block: dQ = 0
+    float4* dq4 = reinterpret_cast<float4*>(p.dq + (size_t)qrow0 * D);
+    for (int i = tid; i < kBlock * D / 4; i += kBwdThreads) dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  bool bad = n > p.nb;
+  for (int i = tid; !bad && i < n; i += kBwdThreads) {
+    const int kb = p.col_idx[r0 + i];
+    bad = kb < 0 || kb >= p.nb || (p.causal && kb > qb);
+  }
+  if (__syncthreads_or(bad)) {
+    if (tid == 0) atomicOr(p.status, kStatusInternal);
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  DqBars* bars = reinterpret_cast<DqBars*>(smem_raw + (base - raw) + C::kBarOff);
+  const uint64_t lim = p.timeout_ns;
+  volatile int* abort_flag = &bars->abort_flag;
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars->qd_full), 1);
+    mbar_init(smem_u32(&bars->kv_full[0]), 1);
+    mbar_init(smem_u32(&bars->kv_full[1]), 1);
+    mbar_init(smem_u32(&bars->st_done), 1);
+    mbar_init(smem_u32(&bars->grad_done), 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&bars->tmem_base), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+  const int r = tid & (kBlock - 1);  // TMEM lane: query row
+  const int half = tid >> 7;         // which half of the key (or output) columns
+  const float l2 = p.lse[qrow0 + r] * kLog2e;  // this row's LSE in log2 units
+  const float dlr = p.dl[qrow0 + r];
+
+  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+    for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+  };
+  auto load_kv = [&](int i) {  // K and V of key block number i into buffer i % 2 (thread 0)
+    const int b = i & 1;
+    const uint32_t bar = smem_u32(&bars->kv_full[b]);
+    const int row = bh * p.S + p.col_idx[r0 + i] * kBlock;
+    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+    load_tile(&tm_k, base + C::kKOff + b * C::kTileBytes, bar, row);
+    load_tile(&tm_v, base + C::kVOff + b * C::kTileBytes, bar, row);
+  };
+  if (tid == 0) {
+    const uint32_t bar = smem_u32(&bars->qd_full);
+    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+    load_tile(&tm_q, base + C::kQOff, bar, qrow0);
+    load_tile(&tm_do, base + C::kdOOff, bar, qrow0);
+    load_kv(0);
+  }
+  int n_issued = 1, n_waited = 0;
+  bool qd_waited = false;
+
+  bool ok = true;
+  for (int j = 0; j < n; ++j) {
+    const int kb = p.col_idx[r0 + j];
+    const int b = j & 1;
+    if (j + 1 < n) {
+      // the other buffer was last read by the previous block's MMAs, which are complete
+      if (tid == 0) load_kv(j + 1);
+      n_issued = j + 2;
+    }
+    // S = Q K^T and dP = dO V^T (queries are the TMEM lanes)
+    if (warp == 0) {
+      bool w = qd_waited || bwd_wait(smem_u32(&bars->qd_full), 0, abort_flag, p.status, lim);
+      qd_waited = qd_waited || w;
+      w = w && bwd_wait(smem_u32(&bars->kv_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
+                        lim);
+      if (w) {
+        n_waited = j + 1;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t qd = smem_desc_sw128(base + C::kQOff, 16, 1024);
+          const uint64_t dd = smem_desc_sw128(base + C::kdOOff, 16, 1024);
+          const uint64_t kd = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(base + C::kVOff + b * C::kTileBytes, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kTS, qd + off, kd + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tmem + C::kTdP, dd + off, vd + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->st_done));
+        }
+        __syncwarp();
+      }
+      ok = w;
+    }
+    if (ok) ok = bwd_wait(smem_u32(&bars->st_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+
+    // dS = P (dP - Dl), one query row and 64 keys per thread, 32 at a time, to
+    // shared memory (bf16, 128-byte swizzled: row r, 16-byte chunk c of
+    // 64-key box x at x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16)).
+    {
+      const bool diag = p.causal && kb == qb;  // key c is allowed for query r iff c <= r
+      const float sl = p.scale_log2;
+      const uint32_t tS = tmem + C::kTS + lane_off;
+      const uint32_t tdP = tmem + C::kTdP + lane_off;
+      const uint32_t sdS = base + C::kdSOff;
+#pragma unroll 1
+      for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS + ch * 32, sv);
+        tmem_ld32(tdP + ch * 32, dp);
+        tmem_wait_ld();
+        reg_fence(sv, 32);
+        reg_fence(dp, 32);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int c = ch * 32 + i;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l2));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l2));
+          if (diag) {
+            p0 = c > r ? 0.f : p0;
+            p1 = c + 1 > r ? 0.f : p1;
+          }
+          dk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - dlr),
+                                   p1 * (__uint_as_float(dp[i + 1]) - dlr));
+        }
+        const uint32_t rowa = sdS + (uint32_t)(ch >> 1) * C::kBoxBytes + (uint32_t)r * 128u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint32_t c = (uint32_t)((ch & 1) * 4 + u);
+          st_shared_v4(rowa + ((c ^ (uint32_t)(r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
+                       dk[4 * u + 2], dk[4 * u + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+    }
+    __syncthreads();  // dS in shared memory
+
+    // dQ += dS K (K = 128 keys)
+    if (warp == 0) {
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
+        const uint64_t k_mn = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, C::kBoxBytes,
+                                              1024);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
+          mma_ss(tmem + C::kTdQ, ds_k + km, k_mn + mn, C::kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->grad_done));
+      }
+      __syncwarp();
+    }
+    ok = bwd_wait(smem_u32(&bars->grad_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
+    if (!__syncthreads_and(ok)) {  // dS, this K buffer and S / dP free for the next block
+      ok = false;
+      break;
+    }
+  }
+
+  if (warp == 0) {  // drain copies and MMAs in flight
+    if (!qd_waited) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
+    for (int i = n_waited; i < n_issued; ++i)
+      bwd_drain_wait(smem_u32(&bars->kv_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+    if (elect_one()) mma_commit(smem_u32(&bars->drain));
+    __syncwarp();
+    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (ok) {  // dQ times scale, one query row and half of the columns per thread
+    float* dqr = p.dq + (size_t)(qrow0 + r) * D;
+#pragma unroll 1
+    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+      uint32_t v[32];
+      tmem_ld32(tmem + C::kTdQ + lane_off + c, v);
+      tmem_wait_ld();
+      reg_fence(v, 32);
+#pragma unroll
+      for (int i = 0; i < 32; i += 4)
+        st_global_v4(dqr + c + i, __float_as_uint(__uint_as_float(v[i]) * p.scale),
+                     __float_as_uint(__uint_as_float(v[i + 1]) * p.scale),
+                     __float_as_uint(__uint_as_float(v[i + 2]) * p.scale),
+                     __float_as_uint(__uint_as_float(v[i + 3]) * p.scale));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kBwdTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, int grid,
+                            cudaStream_t stream) {
+  static std::atomic<bool> opted_in[64];
+  const size_t smem = DqCfg<D>::kSmem + 1024;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(bsattn_bwd_dq_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    opted_in[dev].store(true, std::memory_order_release);
+  }
+  bsattn_bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const BwdParams& p, int grid,
@@ -443,16 +723,16 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
-                            float* dq, long long rows, cudaStream_t stream) {
+                            long long rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
   const uint16_t* g = static_cast<const uint16_t*>(dout);
   if (D == 128) {
-    if (o_f32) bwd_prep_kernel<128, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
-    else bwd_prep_kernel<128, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+    if (o_f32) bwd_prep_kernel<128, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, rows);
+    else bwd_prep_kernel<128, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, rows);
   } else {
-    if (o_f32) bwd_prep_kernel<64, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
-    else bwd_prep_kernel<64, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, dq, rows);
+    if (o_f32) bwd_prep_kernel<64, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, rows);
+    else bwd_prep_kernel<64, false><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, rows);
   }
   return cudaGetLastError();
 }
@@ -462,6 +742,14 @@ cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, cons
   if (grid <= 0) return cudaSuccess;
   return D == 128 ? launch_bwd_t<128>(tq, tk, tv, tdo, p, grid, stream)
                   : launch_bwd_t<64>(tq, tk, tv, tdo, p, grid, stream);
+}
+
+cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                          int grid, cudaStream_t stream) {
+  if (grid <= 0) return cudaSuccess;
+  return D == 128 ? launch_bwd_dq_t<128>(tq, tk, tv, tdo, p, grid, stream)
+                  : launch_bwd_dq_t<64>(tq, tk, tv, tdo, p, grid, stream);
 }
 
 }  // namespace bsattn

@@ -56,11 +56,13 @@ struct FwdParams {
 
 // Everything the backward kernel needs besides its four tensor maps.
 struct BwdParams {
-  const int* col_ptr;
+  const int* col_ptr;  // transposed plan (dK, dV kernel)
   const int* row_idx;
+  const int* row_ptr;  // forward plan (dQ kernel)
+  const int* col_idx;
   const float* lse;  // natural-log LSE of the forward pass
   const float* dl;   // dO_i . O_i
-  float* dq;         // fp32, zeroed by the preparation kernel, accumulated by reductions
+  float* dq;
   float* dk;
   float* dv;
   int* status;
@@ -121,8 +123,12 @@ cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
 
 // bwd_sm103.cu
 cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
-                            float* dq, long long rows, cudaStream_t stream);
+                            long long rows, cudaStream_t stream);
+// dK, dV (grid: one CTA per key tile) and dQ (one CTA per query tile)
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                          int grid, cudaStream_t stream);
 
 }  // namespace bsattn

@@ -133,9 +133,8 @@ def test_bwd_through_forward(bs):
 
 
 def test_bwd_repeated_calls(bs):
-    """dQ is re-zeroed on every call (reductions never accumulate across calls).
-    dK and dV are written once per key tile and repeat bit for bit; dQ is summed
-    by fp32 reductions in no fixed order, so it repeats to rounding level."""
+    """Every gradient row is written once by one CTA in a fixed order: repeated
+    calls give bit-identical dQ, dK and dV."""
     import torch
     B, H, S, D, mask, causal, scale, qb, kb, vb, gb = _inputs("d64_sparse")
     O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(scale), causal)
@@ -147,9 +146,8 @@ def test_bwd_repeated_calls(bs):
         again = bs.bwd(q, k, v, o, lse, g, p, scale)
     bs.plan_status(p)
     p.close()
-    assert torch.equal(first[1], again[1]) and torch.equal(first[2], again[2])
-    scale_q = float(first[0].abs().max())
-    assert float((first[0] - again[0]).abs().max()) <= 1e-5 * scale_q
+    for a, b in zip(first, again):
+        assert torch.equal(a, b)
 
 
 def test_bwd_full_size_causal_sampled_heads(bs):
