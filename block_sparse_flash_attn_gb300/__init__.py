@@ -28,13 +28,13 @@ BLOCK = 128
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_INTERNAL = range(7)
 ERR_SCRATCH_LIMIT = 7
-CAUSAL, OUT_F32 = 1, 2
+CAUSAL, OUT_F32, MASK_SHARED_HEADS = 1, 2, 4
 
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
            "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
            "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free",
-           "bsattn_plan_csc", "bsattn_bwd"]
+           "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa"]
 
 
 class BsattnError(RuntimeError):
@@ -69,6 +69,9 @@ def load():
     lib.bsattn_plan_schedule.restype = i32
     lib.bsattn_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp]
     lib.bsattn_fwd.restype = i32
+    lib.bsattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
+                                   vp]
+    lib.bsattn_fwd_gqa.restype = i32
     lib.bsattn_plan_csc.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)]
     lib.bsattn_plan_csc.restype = i32
     lib.bsattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -154,8 +157,12 @@ class Plan:
             pass
 
 
-def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream=None) -> Plan:
-    """Build the plan for a uint8 block mask [B, H, S/128, S/128] on the GPU."""
+def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream=None,
+         heads: int | None = None) -> Plan:
+    """Build the plan for a uint8 block mask [B, H, S/128, S/128] on the GPU.
+
+    With heads=H and a mask of shape [B, 1, S/128, S/128], the one mask of
+    each batch entry applies to all its H heads."""
     if not (isinstance(mask, torch.Tensor) and mask.is_cuda and mask.dtype == torch.uint8):
         raise TypeError("mask must be a CUDA uint8 tensor")
     if mask.dim() != 4 or mask.shape[2] != mask.shape[3]:
@@ -163,6 +170,11 @@ def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream
     mask = mask.contiguous()
     B, H, nb, _ = mask.shape
     flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0)
+    if heads is not None and heads != H:
+        if H != 1:
+            raise ValueError("a mask shared by the heads must have shape [B, 1, nb, nb]")
+        H = int(heads)
+        flags |= MASK_SHARED_HEADS
     h = ctypes.c_void_p()
     with torch.cuda.device(mask.device):
         _check(load().bsattn_plan(ctypes.c_void_p(mask.data_ptr()), B, H, nb * BLOCK, flags,
@@ -172,15 +184,18 @@ def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float | None = None,
         out: torch.Tensor | None = None, lse: torch.Tensor | None = None, stream=None):
-    """O, LSE = block-sparse attention.  q/k/v: CUDA bf16 [B, H, S, D], contiguous."""
+    """O, LSE = block-sparse attention.  q: CUDA bf16 [B, H, S, D]; k, v: [B, Hkv, S, D]
+    with H % Hkv == 0 (Hkv < H: grouped-query attention); all contiguous."""
     for t in (q, k, v):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16):
             raise TypeError("q, k, v must be CUDA bf16 tensors")
         if not t.is_contiguous():
             raise ValueError("q, k, v must be contiguous")
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
-        raise ValueError("q, k, v must share the shape [B, H, S, D]")
+    if q.dim() != 4 or k.shape != v.shape or k.dim() != 4 or k.shape[0] != q.shape[0] \
+            or k.shape[2:] != q.shape[2:] or q.shape[1] % k.shape[1] != 0:
+        raise ValueError("q must be [B, H, S, D] and k, v [B, Hkv, S, D] with H % Hkv == 0")
     B, H, S, D = q.shape
+    Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     odt = torch.float32 if p.out_f32 else torch.bfloat16
@@ -192,11 +207,17 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float
         raise ValueError("out has the wrong dtype/shape/layout for this plan")
     if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, S]")
+    vp = ctypes.c_void_p
     with torch.cuda.device(q.device):
-        _check(load().bsattn_fwd(ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
-                                 ctypes.c_void_p(v.data_ptr()), p.handle,
-                                 ctypes.c_void_p(out.data_ptr()), ctypes.c_void_p(lse.data_ptr()),
-                                 B, H, S, D, float(scale), _stream_handle(stream)), "bsattn_fwd")
+        if Hkv == H:
+            _check(load().bsattn_fwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
+                                     p.handle, vp(out.data_ptr()), vp(lse.data_ptr()), B, H, S, D,
+                                     float(scale), _stream_handle(stream)), "bsattn_fwd")
+        else:
+            _check(load().bsattn_fwd_gqa(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
+                                         p.handle, vp(out.data_ptr()), vp(lse.data_ptr()), B, H,
+                                         Hkv, S, D, float(scale), _stream_handle(stream)),
+                   "bsattn_fwd_gqa")
     return out, lse
 
 

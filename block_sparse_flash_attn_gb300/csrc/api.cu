@@ -105,7 +105,7 @@ namespace bsattn {
 
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf) {
+                          PreparedFwd* pf, int Hkv) {
   if (!plan_ok(plan) || !pf) return BSATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
@@ -113,15 +113,17 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  if (Hkv <= 0 || H % Hkv != 0) return BSATTN_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
   if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
 
   const long long rows = (long long)B * H * S;
+  const long long kv_rows = (long long)B * Hkv * S;
   bsattn_status rc;
   if ((rc = encode_bf16_map(&pf->tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&pf->tk, k, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&pf->tv, v, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&pf->tk, k, D, kv_rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&pf->tv, v, D, kv_rows)) != BSATTN_OK) return rc;
 
   FwdParams& prm = pf->prm;
   prm = FwdParams{};
@@ -141,6 +143,8 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   set_scale_params(prm, scale);
   prm.causal = (plan->flags & BSATTN_CAUSAL) ? 1 : 0;
   prm.timeout_ns = kDefaultWaitTimeoutNs;
+  prm.H = H;
+  prm.kv_group = H / Hkv;
   pf->D = D;
   pf->out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
   pf->grid = device_sm_count(dev);
@@ -175,7 +179,8 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
                           void* stream, bsattn_plan_t* out_plan) {
   if (!d_mask || !out_plan) return BSATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || S <= 0 || (S % kBlock) != 0) return BSATTN_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)(BSATTN_CAUSAL | BSATTN_OUT_F32)) return BSATTN_ERR_INVALID_ARG;
+  if (flags & ~(unsigned)(BSATTN_CAUSAL | BSATTN_OUT_F32 | BSATTN_MASK_SHARED_HEADS))
+    return BSATTN_ERR_INVALID_ARG;
   const int nb = S / kBlock;
   if (nb > kMaxBlocksPerRow) return BSATTN_ERR_UNSUPPORTED;
   if ((long long)B * H * S >= (1ll << 31)) return BSATTN_ERR_UNSUPPORTED;
@@ -192,6 +197,7 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
   p->flags = flags;
   cudaGetDevice(&p->device);
   const int causal = (flags & BSATTN_CAUSAL) ? 1 : 0;
+  const int mdiv = (flags & BSATTN_MASK_SHARED_HEADS) ? H : 1;  // mask heads: H or 1
 
   int* tmp = nullptr;  // counts[rows] | live_per_head[BH] | live_off[BH+1] | totals (2 x int64)
   const size_t tmp_ints = (size_t)rows + BH + (BH + 1) + 1 + 4;
@@ -217,7 +223,7 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
   if ((e = cudaMemsetAsync(p->dev.work, 0, sizeof(int) * kWorkWords, st)) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = plan_count_and_scan(d_mask, BH, nb, causal, d_counts, p->dev.row_ptr, d_live_off,
-                               d_totals, st)) != cudaSuccess)
+                               d_totals, st, mdiv)) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = cudaMemcpyAsync(h_tot, d_totals, sizeof(h_tot), cudaMemcpyDeviceToHost, st)) !=
       cudaSuccess)
@@ -239,8 +245,7 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
     return fail(from_cuda(e));
   if ((e = plan_fill_and_order(d_mask, BH, nb, causal, p->dev.row_ptr, d_live_off,
                                p->dev.col_idx, p->dev.tile_order, p->dev.empty_tiles,
-                               device_sm_count(p->device), st)) !=
-      cudaSuccess)
+                               device_sm_count(p->device), st, mdiv)) != cudaSuccess)
     return fail(from_cuda(e));
   // Transposed plan for the backward pass (same number of live blocks) and
   // its per-row scratch; d_counts is free again once the CSR is built.
@@ -251,8 +256,8 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
     return fail(from_cuda(e));
   if ((e = cudaMalloc(&p->dev.dl, sizeof(float) * (size_t)B * H * S)) != cudaSuccess)
     return fail(from_cuda(e));
-  if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st)) !=
-      cudaSuccess)
+  if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st,
+                    mdiv)) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
   cudaFree(tmp);
@@ -296,7 +301,16 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
                          void* out, float* lse, int B, int H, int S, int D, float scale,
                          void* stream) {
   PreparedFwd pf;
-  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf);
+  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, H);
+  if (rc != BSATTN_OK) return rc;
+  return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
+}
+
+bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                             void* out, float* lse, int B, int H, int Hkv, int S, int D,
+                             float scale, void* stream) {
+  PreparedFwd pf;
+  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, Hkv);
   if (rc != BSATTN_OK) return rc;
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }

@@ -379,7 +379,11 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
         k_rem = 0;
         return true;
       }
-      k_hrow = (t / p.nb) * p.S;
+      // K/V rows of the tile's head (its group's K/V head under grouped-query attention)
+      const int bh = t / p.nb;
+      const int kvbh =
+          p.kv_group > 1 ? (bh / p.H) * (p.H / p.kv_group) + (bh % p.H) / p.kv_group : bh;
+      k_hrow = kvbh * p.S;
       k_j = 0;
       k_ask = k_rem - 1 < kClaimAhead ? k_rem - 1 : kClaimAhead;
     } else if ((k_j & 31) == 0) {  // next 32 entries of the tile's CSR list

@@ -52,6 +52,11 @@ struct FwdParams {
   int neg_scale;     // scale < 0: the S MMA computes -Q K^T
   int causal;
   unsigned long long timeout_ns;
+  // grouped-query attention: query head h of a batch entry reads K/V head
+  // h / kv_group (H query heads, H / kv_group K/V heads); 1 = one K/V head per
+  // query head
+  int H = 1;
+  int kv_group = 1;
 };
 
 // Everything the backward kernel needs besides its four tensor maps.
@@ -94,23 +99,26 @@ struct PreparedFwd {
   bool out_f32 = false;
   int grid = 0;
 };
+// Hkv: K/V heads (H % Hkv == 0; Hkv == H for plain multi-head attention).
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf);
+                          PreparedFwd* pf, int Hkv);
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream);
 
 // plan.cu
+// mdiv: head (b*H + h) reads mask (b*H + h) / mdiv (1: a mask per head; H: one
+// mask per batch entry shared by its heads)
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int mdiv = 1);
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
                                 int* d_tile_order, int* d_empty_tiles, int nsm,
-                                cudaStream_t stream);
+                                cudaStream_t stream, int mdiv = 1);
 // Transposed plan (per key block, the ascending live query blocks); d_counts
 // is scratch of R ints.
 cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
-                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream);
+                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream, int mdiv = 1);
 // Heads per schedule chunk for S/128 = nb key blocks per head.
 int schedule_chunk_heads(int nb);
 

@@ -133,7 +133,7 @@ extern "C" bsattn_status bsattn_pipeline_create(const uint8_t* d_mask, int B, in
                      static_cast<const char*>(p->dk) + off * 2,
                      static_cast<const char*>(p->dv) + off * 2, pl,
                      static_cast<char*>(p->dout) + off * p->out_elem, p->dlse + (size_t)a * S, 1,
-                     h, S, D, 1.0f, &p->prep[c]);
+                     h, S, D, 1.0f, &p->prep[c], h);
     if (rc != BSATTN_OK) return fail(rc);
   }
   p->magic = kPipeMagic;

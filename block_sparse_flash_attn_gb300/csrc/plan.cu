@@ -9,7 +9,9 @@
 // here, so dead blocks cost nothing.
 //
 // Layout: row r = (b*H + h)*nb + qb; row_ptr[r]..row_ptr[r+1] index col_idx,
-// which lists kb ascending with mask != 0 (and kb <= qb when causal).
+// which lists kb ascending with mask != 0 (and kb <= qb when causal).  The
+// mask of head (b*H + h) is mask[(b*H + h) / mdiv]: mdiv = 1 for one mask per
+// head, H for one mask per batch entry shared by its heads.
 // Schedule: non-empty tiles in chunks of consecutive heads (so a chunk's K/V
 // stay resident in L2 while its tiles run), inside a chunk sorted by live
 // count descending (longest-processing-time first), with the few tiles that
@@ -36,12 +38,12 @@ __device__ __forceinline__ bool block_live(const uint8_t* mask_row, int kb, int 
 // One warp per CSR row: number of live key blocks.  Also counts, per head, the
 // rows with at least one live block.
 __global__ void count_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int causal,
-                             int* __restrict__ counts, int* __restrict__ live_per_head) {
+                             int mdiv, int* __restrict__ counts, int* __restrict__ live_per_head) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int qb = warp % nb;
-  const uint8_t* mrow = mask + (size_t)warp * nb;
+  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nb;
   int c = 0;
   for (int kb = lane; kb < nb; kb += 32) c += block_live(mrow, kb, qb, causal) ? 1 : 0;
   c = __reduce_add_sync(0xffffffffu, c);
@@ -95,12 +97,12 @@ __global__ void __launch_bounds__(kScanThreads)
 
 // One warp per CSR row: write the live kb in ascending order.
 __global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int causal,
-                            const int* __restrict__ row_ptr, int* __restrict__ col_idx) {
+                            int mdiv, const int* __restrict__ row_ptr, int* __restrict__ col_idx) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int qb = warp % nb;
-  const uint8_t* mrow = mask + (size_t)warp * nb;
+  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nb;
   int base = row_ptr[warp];
   for (int kb0 = 0; kb0 < nb; kb0 += 32) {
     const int kb = kb0 + lane;
@@ -208,12 +210,12 @@ __device__ __forceinline__ bool col_live(const uint8_t* mask_bh, int nb, int qb,
 }
 
 __global__ void csc_count_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
-                                 int* __restrict__ counts) {
+                                 int mdiv, int* __restrict__ counts) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= cols) return;
   const int kb = warp % nb;
-  const uint8_t* mbh = mask + (size_t)(warp / nb) * nb * nb;
+  const uint8_t* mbh = mask + (size_t)(warp / nb / mdiv) * nb * nb;
   int c = 0;
   for (int qb = lane; qb < nb; qb += 32) c += col_live(mbh, nb, qb, kb, causal) ? 1 : 0;
   c = __reduce_add_sync(0xffffffffu, c);
@@ -227,12 +229,13 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 __global__ void csc_fill_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
-                                const int* __restrict__ col_ptr, int* __restrict__ row_idx) {
+                                int mdiv, const int* __restrict__ col_ptr,
+                                int* __restrict__ row_idx) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= cols) return;
   const int kb = warp % nb;
-  const uint8_t* mbh = mask + (size_t)(warp / nb) * nb * nb;
+  const uint8_t* mbh = mask + (size_t)(warp / nb / mdiv) * nb * nb;
   int pos = col_ptr[warp];
   for (int q0 = 0; q0 < nb; q0 += 32) {
     const int qb = q0 + lane;
@@ -247,15 +250,15 @@ __global__ void csc_fill_kernel(const uint8_t* __restrict__ mask, int cols, int 
 
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int mdiv) {
   const int rows = BH * nb;
   int* live_per_head = d_counts + rows;  // caller sized d_counts as rows + BH
   cudaError_t e = cudaMemsetAsync(live_per_head, 0, sizeof(int) * BH, stream);
   if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, d_counts,
-                                                          live_per_head);
+  count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, mdiv,
+                                                          d_counts, live_per_head);
   scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, rows, live_per_head, BH, d_row_ptr,
                                               d_live_off, reinterpret_cast<long long*>(d_totals));
   return cudaGetLastError();
@@ -266,12 +269,12 @@ int schedule_chunk_heads(int nb) { return nb >= kChunkKeyBlocks ? 1 : kChunkKeyB
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
                                 int* d_tile_order, int* d_empty_tiles, int nsm,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, int mdiv) {
   const int rows = BH * nb;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, d_row_ptr,
-                                                         d_col_idx);
+  fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, mdiv,
+                                                         d_row_ptr, d_col_idx);
   const int kh = schedule_chunk_heads(nb);
   const int chunks = (BH + kh - 1) / kh;
   int n2 = 1;
@@ -282,14 +285,15 @@ cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causa
 }
 
 cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
-                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream) {
+                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream, int mdiv) {
   const int cols = BH * nb;
   const int warps_per_block = 8;
   const int grid = (cols + warps_per_block - 1) / warps_per_block;
-  csc_count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, d_counts);
+  csc_count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, mdiv,
+                                                              d_counts);
   csc_scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, cols, d_col_ptr);
-  csc_fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, d_col_ptr,
-                                                             d_row_idx);
+  csc_fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, mdiv,
+                                                             d_col_ptr, d_row_idx);
   return cudaGetLastError();
 }
 

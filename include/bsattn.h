@@ -63,7 +63,9 @@ typedef struct bsattn_plan_s* bsattn_plan_t;
 /* Plan flags. */
 enum {
   BSATTN_CAUSAL = 1u,   /* also require key j <= query i (element level, inclusive) */
-  BSATTN_OUT_F32 = 2u   /* bsattn_fwd writes O as fp32 instead of bf16 */
+  BSATTN_OUT_F32 = 2u,  /* bsattn_fwd writes O as fp32 instead of bf16 */
+  BSATTN_MASK_SHARED_HEADS = 4u  /* bsattn_plan only: d_mask is [B][1][S/128][S/128],
+                                    one mask per batch entry for all its H heads */
 };
 
 /*
@@ -81,9 +83,10 @@ enum {
  * only call that synchronises: it waits for `stream` once to learn the number
  * of live blocks before allocating.
  *
- *   d_mask     device uint8 [B][H][S/128][S/128]; read during the call only.
+ *   d_mask     device uint8 [B][H][S/128][S/128] ([B][1][S/128][S/128] with
+ *              BSATTN_MASK_SHARED_HEADS); read during the call only.
  *   B, H, S    sizes; S % 128 == 0.
- *   flags      BSATTN_CAUSAL | BSATTN_OUT_F32.
+ *   flags      BSATTN_CAUSAL | BSATTN_OUT_F32 | BSATTN_MASK_SHARED_HEADS.
  *   stream     cudaStream_t.
  *   out_plan   receives the handle; the library owns its device memory until
  *              bsattn_plan_free.  Unchanged on error.
@@ -162,6 +165,21 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
                          const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
                          float* dk, float* dv, int B, int H, int S, int D, float scale,
                          void* stream);
+
+/*
+ * bsattn_fwd_gqa -- bsattn_fwd with grouped-query attention: K and V have Hkv
+ * heads and query head h of a batch entry attends with K/V head h / (H / Hkv)
+ * (Hkv = 1: multi-query attention; Hkv = H: bsattn_fwd).  The result equals
+ * bsattn_fwd on K and V with each head repeated H / Hkv times.
+ *
+ *   q, out, lse  as bsattn_fwd ([B][H][S][D] / [B][H][S]).
+ *   k, v         device bf16 [B][Hkv][S][D], 16-byte aligned.
+ *   Hkv          K/V heads, 1 <= Hkv, H % Hkv == 0.
+ * Errors: as bsattn_fwd; INVALID_ARG also when H % Hkv != 0.
+ */
+bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn_plan_t plan,
+                             void* out, float* lse, int B, int H, int Hkv, int S, int D,
+                             float scale, void* stream);
 
 /* Wait for `stream`, then report and clear the device-side status of the
    plan's kernels: OK, TIMEOUT or INTERNAL (or CUDA if the wait failed). */

@@ -155,4 +155,29 @@ def flops_live(mask, D: int, causal: bool = False) -> int:
     return int(row_ptr[-1]) * 4 * BLOCK * BLOCK * D
 
 
+
+def attention_gqa(q, k, v, mask, scale: float, causal: bool = False, rows=None):
+    """Grouped-query attention, fp64: q [B][H][S][D], k and v [B][Hkv][S][D]
+    with H % Hkv == 0; query head h attends with K/V head h // (H // Hkv).
+    mask [B][H][nb][nb], or [B][1][nb][nb] shared by the heads of a batch entry.
+
+    Defined as the attention above on K and V with each head repeated
+    H // Hkv times and the mask broadcast over the heads (the pages use one
+    K/V head per query head; this is the plain extension of their shapes).
+    Pinned by tests/test_oracle_pins.py against torch's float64
+    scaled_dot_product_attention with enable_gqa.
+    """
+    q = np.asarray(q)
+    B, H = q.shape[:2]
+    Hkv = np.asarray(k).shape[1]
+    if H % Hkv:
+        raise ValueError("H must be a multiple of the K/V heads")
+    g = H // Hkv
+    k_rep = np.ascontiguousarray(np.repeat(np.asarray(k), g, axis=1))
+    v_rep = np.ascontiguousarray(np.repeat(np.asarray(v), g, axis=1))
+    mask = np.asarray(mask, dtype=np.uint8)
+    if mask.shape[1] == 1 and H > 1:
+        mask = np.ascontiguousarray(np.broadcast_to(mask, (B, H) + mask.shape[2:]))
+    return attention(q, k_rep, v_rep, mask, scale, causal, rows=rows)
+
 from .backward import BWD_MUTATIONS, attention_bwd, csc, set_bwd_mutation  # noqa: E402,F401

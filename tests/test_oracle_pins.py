@@ -363,3 +363,43 @@ def test_workload_masks(gen):
     assert np.all(np.diagonal(m1, axis1=2, axis2=3) == 1)
     m2 = workloads.make_mask(w[2], B=1, H=1)
     assert np.array_equal(m2[0, 0], np.tril(np.ones((32, 32), dtype=np.uint8)))
+
+
+# ----------------------------------------------------------------------------
+# grouped-query attention and a mask shared by the heads
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("Hkv,causal", [(1, False), (2, True), (4, False)])
+def test_gqa_against_torch_sdpa(Hkv, causal):
+    """torch float64 SDPA with enable_gqa (a library routine) for an all-ones mask."""
+    torch = pytest.importorskip("torch")
+    B, H, S, D = 1, 4, 256, 8
+    rng = np.random.default_rng(60 + Hkv)
+    q = rng.standard_normal((B, H, S, D))
+    k = rng.standard_normal((B, Hkv, S, D))
+    v = rng.standard_normal((B, Hkv, S, D))
+    mask = np.ones((B, 1, S // 128, S // 128), np.uint8)
+    O, _ = oracle.attention_gqa(q, k, v, mask, 0.3, causal)
+    try:
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            torch.tensor(q), torch.tensor(k), torch.tensor(v), is_causal=causal, scale=0.3,
+            enable_gqa=True).numpy()
+    except TypeError:
+        pytest.skip("torch without enable_gqa")
+    assert np.max(np.abs(O - ref)) < 1e-12
+
+
+def test_shared_mask_equals_per_head_copies():
+    """A [B, 1, nb, nb] mask gives, for every head, the result of that head with the
+    mask copied to it (checked head by head against single-head calls)."""
+    B, H, S, D = 2, 3, 256, 8
+    rng = np.random.default_rng(70)
+    q, k, v = (rng.standard_normal((B, H, S, D)) for _ in range(3))
+    mask = np.array([[[[1, 0], [1, 1]]], [[[0, 1], [1, 0]]]], np.uint8)  # [B=2, 1, 2, 2]
+    O, L = oracle.attention_gqa(q, k, v, mask, 0.5, False)
+    for b in range(B):
+        for h in range(H):
+            Oh, Lh = oracle.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                      mask[b:b + 1], 0.5, False)
+            assert np.array_equal(O[b, h], Oh[0, 0]) and np.array_equal(L[b, h], Lh[0, 0],
+                                                                        equal_nan=True)
