@@ -57,7 +57,7 @@ E2E_MAX_PIECES = 8  # each piece costs a plan, a launch and five copies of host 
 # DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
 # of the current forward kernel, from the ncu capture summarised in
 # profiles/bsattn_fwd_kernel-causal-s4096-d128.md; workloads not captured: None.
-TRAFFIC_BYTES = {"w2_bf16": 311_130_112 + 48_610_816}
+TRAFFIC_BYTES = {"w2_bf16": 308_948_736 + 48_557_312}
 
 
 def parse_args(argv=None):

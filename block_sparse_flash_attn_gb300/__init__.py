@@ -34,7 +34,7 @@ EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
            "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
            "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free",
-           "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa"]
+           "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa", "bsattn_bwd_gqa"]
 
 
 class BsattnError(RuntimeError):
@@ -77,6 +77,9 @@ def load():
     lib.bsattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                ctypes.c_float, vp]
     lib.bsattn_bwd.restype = i32
+    lib.bsattn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                   ctypes.c_float, vp]
+    lib.bsattn_bwd_gqa.restype = i32
     lib.bsattn_plan_status.argtypes = [vp, vp]
     lib.bsattn_plan_status.restype = i32
     lib.bsattn_plan_free.argtypes = [vp]
@@ -224,18 +227,21 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
         dout: torch.Tensor, p: Plan, scale: float | None = None, dq: torch.Tensor | None = None,
         dk: torch.Tensor | None = None, dv: torch.Tensor | None = None, stream=None):
-    """dQ, dK, dV (CUDA fp32 [B, H, S, D]) of block-sparse attention.
+    """dQ [B, H, S, D], dK and dV [B, Hkv, S, D] (CUDA fp32) of block-sparse attention.
 
-    q/k/v/dout: CUDA bf16 [B, H, S, D], contiguous; o, lse: the forward's
-    outputs for plan p; scale: the forward's scale."""
+    q/dout: CUDA bf16 [B, H, S, D], k/v: [B, Hkv, S, D] (H % Hkv == 0; Hkv < H:
+    grouped-query attention), contiguous; o, lse: the forward's outputs for
+    plan p; scale: the forward's scale."""
     for t in (q, k, v, dout):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16):
             raise TypeError("q, k, v, dout must be CUDA bf16 tensors")
         if not t.is_contiguous():
             raise ValueError("q, k, v, dout must be contiguous")
-    if q.dim() != 4 or any(t.shape != q.shape for t in (k, v, dout)):
-        raise ValueError("q, k, v, dout must share the shape [B, H, S, D]")
+    if q.dim() != 4 or dout.shape != q.shape or k.dim() != 4 or v.shape != k.shape \
+            or k.shape[0] != q.shape[0] or k.shape[2:] != q.shape[2:] or q.shape[1] % k.shape[1]:
+        raise ValueError("q, dout must be [B, H, S, D] and k, v [B, Hkv, S, D] with H % Hkv == 0")
     B, H, S, D = q.shape
+    Hkv = k.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     odt = torch.float32 if p.out_f32 else torch.bfloat16
@@ -244,19 +250,19 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [B, H, S]")
     grads = []
-    for g in (dq, dk, dv):
+    for g, shape in ((dq, q.shape), (dk, k.shape), (dv, k.shape)):
         if g is None:
-            g = torch.empty((B, H, S, D), dtype=torch.float32, device=q.device)
-        if g.dtype != torch.float32 or g.shape != q.shape or not g.is_contiguous():
-            raise ValueError("dq, dk, dv must be contiguous fp32 [B, H, S, D]")
+            g = torch.empty(shape, dtype=torch.float32, device=q.device)
+        if g.dtype != torch.float32 or g.shape != shape or not g.is_contiguous():
+            raise ValueError("dq must be contiguous fp32 like q, dk and dv like k")
         grads.append(g)
     vp = ctypes.c_void_p
     with torch.cuda.device(q.device):
-        _check(load().bsattn_bwd(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
-                                 vp(o.data_ptr()), vp(lse.data_ptr()), vp(dout.data_ptr()),
-                                 p.handle, vp(grads[0].data_ptr()), vp(grads[1].data_ptr()),
-                                 vp(grads[2].data_ptr()), B, H, S, D, float(scale),
-                                 _stream_handle(stream)), "bsattn_bwd")
+        _check(load().bsattn_bwd_gqa(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
+                                     vp(o.data_ptr()), vp(lse.data_ptr()), vp(dout.data_ptr()),
+                                     p.handle, vp(grads[0].data_ptr()), vp(grads[1].data_ptr()),
+                                     vp(grads[2].data_ptr()), B, H, Hkv, S, D, float(scale),
+                                     _stream_handle(stream)), "bsattn_bwd_gqa")
     return tuple(grads)
 
 

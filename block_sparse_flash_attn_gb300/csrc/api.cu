@@ -315,10 +315,10 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }
 
-bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void* o,
-                         const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
-                         float* dk, float* dv, int B, int H, int S, int D, float scale,
-                         void* stream) {
+bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
+                             float* dk, float* dv, int B, int H, int Hkv, int S, int D,
+                             float scale, void* stream) {
   if (!plan_ok(plan)) return BSATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return BSATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -327,15 +327,18 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
   if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
   if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  if (Hkv <= 0 || H % Hkv != 0) return BSATTN_ERR_INVALID_ARG;
+  if (H / Hkv > 64) return BSATTN_ERR_UNSUPPORTED;  // query heads per K/V head walked by one CTA
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
   if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
   const long long rows = (long long)B * H * S;
+  const long long kv_rows = (long long)B * Hkv * S;
   CUtensorMap tq, tk, tv, tdo;
   bsattn_status rc;
   if ((rc = encode_bf16_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tk, k, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tv, v, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tk, k, D, kv_rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tv, v, D, kv_rows)) != BSATTN_OK) return rc;
   if ((rc = encode_bf16_map(&tdo, dout, D, rows)) != BSATTN_OK) return rc;
   BwdParams prm{};
   prm.col_ptr = plan->dev.col_ptr;
@@ -354,13 +357,22 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
   prm.scale = scale;
   prm.scale_log2 = (float)((double)scale * 1.4426950408889634074);
   prm.timeout_ns = kDefaultWaitTimeoutNs;
+  prm.H = H;
+  prm.kv_group = H / Hkv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_prep(D, (plan->flags & BSATTN_OUT_F32) != 0, o, dout, plan->dev.dl,
                                   rows, st);
   if (e != cudaSuccess) return from_cuda(e);
-  if ((e = launch_bwd(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st)) != cudaSuccess)
+  if ((e = launch_bwd(D, tq, tk, tv, tdo, prm, B * Hkv * plan->nb, st)) != cudaSuccess)
     return from_cuda(e);
   return from_cuda(launch_bwd_dq(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st));
+}
+
+bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
+                         float* dk, float* dv, int B, int H, int S, int D, float scale,
+                         void* stream) {
+  return bsattn_bwd_gqa(q, k, v, o, lse, dout, plan, dq, dk, dv, B, H, H, S, D, scale, stream);
 }
 
 bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {

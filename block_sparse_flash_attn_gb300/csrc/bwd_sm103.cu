@@ -52,6 +52,7 @@ namespace {
 constexpr int kBwdThreads = 256;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634074f;
+constexpr int kMaxKvGroup = 64;  // query heads per K/V head the dK/dV kernel walks
 
 template <int D>
 struct BwdCfg {
@@ -65,7 +66,8 @@ struct BwdCfg {
   static constexpr int kdSOff = kdOOff + 2 * kTileBytes;  // 128 x 128 bf16: two boxes
   static constexpr int kVecOff = kdSOff + 2 * kBoxBytes;  // LSE log2 e [128], Dl [128]
   static constexpr int kBarOff = kVecOff + 2 * kBlock * 4;
-  static constexpr int kSmem = kBarOff + 256;
+  static constexpr int kGrpOff = kBarOff + 128;  // per query head of the group: list start, prefix
+  static constexpr int kSmem = kGrpOff + 4 * (2 * kMaxKvGroup + 1) + 124;
   // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 queries, both K-major
   static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);
   // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, B MN-major
@@ -88,6 +90,7 @@ struct __align__(8) BwdBars {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(BwdBars) <= 128, "barrier block must fit its 128-byte region");
 
 // Dl_i = dO_i . O_i (fp32 over the stored O and dO); one warp per row.
 template <int D, bool O_F32>
@@ -141,12 +144,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = BwdCfg<D>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-  const int tile = blockIdx.x;  // (b * H + h) * nb + kb
-  const int bh = tile / p.nb;
-  const int kb = tile - bh * p.nb;
-  const int c0 = p.col_ptr[tile];
-  const int n = p.col_ptr[tile + 1] - c0;
-  const int krow0 = bh * p.S + kb * kBlock;  // first key row of the tile
+  const int tile = blockIdx.x;  // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk
+  const int kvbh = tile / p.nb;
+  const int kb = tile - kvbh * p.nb;
+  const int g = p.kv_group;     // query heads reading this K/V head
+  const int hkv = p.H / g;      // K/V heads per batch entry
+  const int bh0 = (kvbh / hkv) * p.H + (kvbh % hkv) * g;  // its first query head b*H + hk*g
+  const int krow0 = kvbh * p.S + kb * kBlock;             // first key row of the tile
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  // The CTA walks the transposed lists of the group's query heads one after
+  // the other: head bh0 + i contributes entries [g_st[i], g_st[i+1]) of the
+  // walk, starting at row_idx[g_c0[i]].
+  int* g_c0 = reinterpret_cast<int*>(smem_raw + (base - raw) + C::kGrpOff);
+  int* g_st = g_c0 + kMaxKvGroup;
+  if (tid < g) {
+    const int t = (bh0 + tid) * p.nb + kb;
+    g_c0[tid] = p.col_ptr[t];
+    g_st[tid + 1] = p.col_ptr[t + 1] - p.col_ptr[t];
+  }
+  __syncthreads();
+  if (tid == 0) {
+    g_st[0] = 0;
+    for (int i = 0; i < g; ++i) g_st[i + 1] += g_st[i];
+  }
+  __syncthreads();
+  const int n = g_st[g];
+  // entry j of the walk: query head (b*H + h) and query block
+  auto entry = [&](int j, int& bhq, int& qbj) {
+    int gi = 0;
+    while (gi + 1 < g && g_st[gi + 1] <= j) ++gi;
+    bhq = bh0 + gi;
+    qbj = p.row_idx[g_c0[gi] + (j - g_st[gi])];
+  };
   if (n <= 0) {  // no live query block: dK = dV = 0
     float4* dk4 = reinterpret_cast<float4*>(p.dk + (size_t)krow0 * D);
     float4* dv4 = reinterpret_cast<float4*>(p.dv + (size_t)krow0 * D);
@@ -156,10 +188,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     return;
   }
-  // The plan's list must hold valid query blocks; anything else is an internal error.
-  bool bad = n > p.nb;
+  // The plan's lists must hold valid query blocks; anything else is an internal error.
+  bool bad = n > p.nb * g;
+  for (int gi = 0; !bad && gi < g; ++gi) bad = g_st[gi + 1] - g_st[gi] > p.nb;
   for (int i = tid; !bad && i < n; i += kBwdThreads) {
-    const int qb = p.row_idx[c0 + i];
+    int bhq = 0, qb = 0;
+    entry(i, bhq, qb);
     bad = qb < 0 || qb >= p.nb || (p.causal && qb < kb);
   }
   if (__syncthreads_or(bad)) {
@@ -167,9 +201,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return;
   }
 
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw + (base - raw) + C::kBarOff);
   float* sL = reinterpret_cast<float*>(smem_raw + (base - raw) + C::kVecOff);  // LSE log2 e
   float* sD = sL + kBlock;                                                     // Dl
@@ -210,7 +241,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto load_qd = [&](int i) {
     const int b = i & 1;
     const uint32_t bar = smem_u32(&bars->qd_full[b]);
-    const int row = bh * p.S + p.row_idx[c0 + i] * kBlock;
+    int bhq = 0, qbi = 0;
+    entry(i, bhq, qbi);
+    const int row = bhq * p.S + qbi * kBlock;
     mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
     load_tile(&tm_q, base + C::kQOff + b * C::kTileBytes, bar, row);
     load_tile(&tm_do, base + C::kdOOff + b * C::kTileBytes, bar, row);
@@ -230,14 +263,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // the first half
   float lse_next = 0.f, dl_next = 0.f;
   if (half == 0) {
-    const int qrow = bh * p.S + p.row_idx[c0] * kBlock + r;
+    int bhq = 0, qbi = 0;
+    entry(0, bhq, qbi);
+    const int qrow = bhq * p.S + qbi * kBlock + r;
     lse_next = p.lse[qrow] * kLog2e;
     dl_next = p.dl[qrow];
   }
 
   bool ok = true;
   for (int j = 0; j < n; ++j) {
-    const int qb = p.row_idx[c0 + j];
+    int bhj = 0, qb = 0;  // (the head only matters for the rows loaded ahead)
+    entry(j, bhj, qb);
     const int b = j & 1;
     if (half == 0) {
       sL[r] = lse_next;
@@ -248,7 +284,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (tid == 0) load_qd(j + 1);
       n_issued = j + 2;
       if (half == 0) {
-        const int qrow = bh * p.S + p.row_idx[c0 + j + 1] * kBlock + r;
+        int bhq = 0, qbi = 0;
+        entry(j + 1, bhq, qbi);
+        const int qrow = bhq * p.S + qbi * kBlock + r;
         lse_next = p.lse[qrow] * kLog2e;
         dl_next = p.dl[qrow];
       }
@@ -464,6 +502,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int r0 = p.row_ptr[tile];
   const int n = p.row_ptr[tile + 1] - r0;
   const int qrow0 = bh * p.S + qb * kBlock;  // first query row of the tile
+  const int kvbh =  // the K/V head it attends with
+      p.kv_group > 1 ? (bh / p.H) * (p.H / p.kv_group) + (bh % p.H) / p.kv_group : bh;
   if (n <= 0) {  // no live key block: dQ = 0
     float4* dq4 = reinterpret_cast<float4*>(p.dq + (size_t)qrow0 * D);
     for (int i = tid; i < kBlock * D / 4; i += kBwdThreads) dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -520,7 +560,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto load_kv = [&](int i) {  // K and V of key block number i into buffer i % 2 (thread 0)
     const int b = i & 1;
     const uint32_t bar = smem_u32(&bars->kv_full[b]);
-    const int row = bh * p.S + p.col_idx[r0 + i] * kBlock;
+    const int row = kvbh * p.S + p.col_idx[r0 + i] * kBlock;
     mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
     load_tile(&tm_k, base + C::kKOff + b * C::kTileBytes, bar, row);
     load_tile(&tm_v, base + C::kVOff + b * C::kTileBytes, bar, row);

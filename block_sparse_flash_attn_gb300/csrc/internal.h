@@ -77,6 +77,8 @@ struct BwdParams {
   float scale;
   float scale_log2;  // scale * log2(e), signed
   unsigned long long timeout_ns;
+  int H = 1;         // query heads; kv_group query heads share one K/V head
+  int kv_group = 1;
 };
 
 constexpr unsigned long long kDefaultWaitTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait

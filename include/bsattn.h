@@ -167,6 +167,18 @@ bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void
                          void* stream);
 
 /*
+ * bsattn_bwd_gqa -- bsattn_bwd for grouped-query attention (as bsattn_fwd_gqa):
+ * k, v, dk, dv are [B][Hkv][S][D]; dK and dV of a K/V head sum the gradients
+ * of all H / Hkv query heads that attend with it.  H / Hkv <= 64.
+ * Errors: as bsattn_bwd; INVALID_ARG when H % Hkv != 0, UNSUPPORTED when
+ * H / Hkv > 64.
+ */
+bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                             const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
+                             float* dk, float* dv, int B, int H, int Hkv, int S, int D,
+                             float scale, void* stream);
+
+/*
  * bsattn_fwd_gqa -- bsattn_fwd with grouped-query attention: K and V have Hkv
  * heads and query head h of a batch entry attends with K/V head h / (H / Hkv)
  * (Hkv = 1: multi-query attention; Hkv = H: bsattn_fwd).  The result equals

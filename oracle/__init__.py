@@ -180,4 +180,4 @@ def attention_gqa(q, k, v, mask, scale: float, causal: bool = False, rows=None):
         mask = np.ascontiguousarray(np.broadcast_to(mask, (B, H) + mask.shape[2:]))
     return attention(q, k_rep, v_rep, mask, scale, causal, rows=rows)
 
-from .backward import BWD_MUTATIONS, attention_bwd, csc, set_bwd_mutation  # noqa: E402,F401
+from .backward import BWD_MUTATIONS, attention_bwd, attention_bwd_gqa, csc, set_bwd_mutation  # noqa: E402,F401,E501

@@ -166,3 +166,35 @@ def csc(mask, causal: bool = False):
                         rows.append(qb)
                 col_ptr.append(len(rows))
     return np.asarray(col_ptr, dtype=np.int32), np.asarray(rows, dtype=np.int32)
+
+
+def attention_bwd_gqa(q, k, v, do, mask, scale: float, causal: bool = False,
+                      bounds: bool = False):
+    """Gradients for grouped-query attention, fp64: q, do [B][H][S][D]; k, v
+    [B][Hkv][S][D] (query head h attends with K/V head h // (H // Hkv)); mask
+    [B][H][nb][nb] or [B][1][nb][nb] shared by the heads.
+
+    The gradients of attention on K and V with each head repeated H // Hkv
+    times (attention_bwd), with dK and dV of each K/V head summed over the
+    query heads of its group (the chain rule through the repetition); with
+    bounds=True the per-element bounds are summed the same way."""
+    q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
+    B, H, S, D = q.shape
+    Hkv = k.shape[1]
+    if H % Hkv:
+        raise ValueError("H must be a multiple of the K/V heads")
+    g = H // Hkv
+    k_rep, v_rep = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    mask = np.asarray(mask, dtype=np.uint8)
+    if mask.shape[1] == 1 and H > 1:
+        mask = np.broadcast_to(mask, (B, H) + mask.shape[2:])
+    res = attention_bwd(q, k_rep, v_rep, do, mask, scale, causal, bounds=bounds)
+
+    def fold(x):
+        return x.reshape(B, Hkv, g, S, D).sum(axis=2)
+
+    if bounds:
+        (dq, dk, dv), (bq, bk, bv) = res
+        return (dq, fold(dk), fold(dv)), (bq, fold(bk), fold(bv))
+    dq, dk, dv = res
+    return dq, fold(dk), fold(dv)

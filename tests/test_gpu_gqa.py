@@ -90,3 +90,27 @@ def test_shared_mask_plan_fwd_bwd(bs):
     ref, bound = oracle.attention_bwd(qb, kb, vb, gb, full, np.float32(scale), causal, bounds=True)
     for got, r, b, nm in zip((dq, dk, dv), ref, bound, ("dQ", "dK", "dV")):
         _check(got, r, b, f"shared mask {nm}")
+
+
+@pytest.mark.parametrize("Hkv,D,causal", [(1, 128, True), (2, 64, False), (4, 128, False)])
+def test_gqa_gradients(bs, Hkv, D, causal):
+    """dQ, and dK, dV summed over each K/V head's group, against the oracle
+    (O and LSE from the oracle, per-element bound as in test_gpu_bwd.py)."""
+    import torch
+    B, H, S = 1, 8, 1024
+    scale = D ** -0.5
+    qb = workloads.custom(800 + Hkv, B, H, S, D)[0]
+    _, kb, vb = workloads.custom(900 + Hkv, B, Hkv, S, D)
+    gb = workloads.upstream_grad(950 + Hkv, B, H, S, D)
+    mask = _mask_iid(30 + Hkv, B, H, S // 128, 0.5, diag=True)
+    O_ref, L_ref = oracle.attention_gqa(qb, kb, vb, mask, np.float32(scale), causal)
+    p = bs.plan(torch.from_numpy(mask).cuda(), causal=causal)
+    dq, dk, dv = bs.bwd(to_dev(qb), to_dev(kb), to_dev(vb), to_dev(_bf16_bits(O_ref)),
+                        torch.from_numpy(L_ref.astype(np.float32)).cuda(), to_dev(gb), p, scale)
+    bs.plan_status(p)
+    p.close()
+    assert dk.shape == (B, Hkv, S, D) and dv.shape == (B, Hkv, S, D)
+    ref, bound = oracle.attention_bwd_gqa(qb, kb, vb, gb, mask, np.float32(scale), causal,
+                                          bounds=True)
+    for got, r, b, nm in zip((dq, dk, dv), ref, bound, ("dQ", "dK", "dV")):
+        _check(got, r, b, f"gqa {Hkv} {nm}")

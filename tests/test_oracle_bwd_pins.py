@@ -157,3 +157,23 @@ def test_planted_mistakes_are_caught(m):
         assert not _all_pins_pass(), f"mutation {m} ({ob.BWD_MUTATIONS[m]}) passed every pin"
     finally:
         ob.set_bwd_mutation(0)
+
+
+@pytest.mark.parametrize("Hkv,causal", [(1, False), (2, True)])
+def test_gqa_gradients_against_torch_autograd(Hkv, causal):
+    """Grouped-query gradients against torch float64 autograd of SDPA with enable_gqa."""
+    torch = pytest.importorskip("torch")
+    B, H, S, D = 1, 4, 256, 8
+    q, G = _rand(80, (B, H, S, D)), _rand(81, (B, H, S, D))
+    k, v = _rand(82, (B, Hkv, S, D)), _rand(83, (B, Hkv, S, D))
+    t = [torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v)]
+    try:
+        o = torch.nn.functional.scaled_dot_product_attention(t[0], t[1], t[2], is_causal=causal,
+                                                             scale=0.3, enable_gqa=True)
+    except TypeError:
+        pytest.skip("torch without enable_gqa")
+    (o * torch.tensor(G)).sum().backward()
+    mask = np.ones((B, 1, S // 128, S // 128), np.uint8)
+    got = oracle.attention_bwd_gqa(q, k, v, G, mask, 0.3, causal)
+    for a, x in zip(got, t):
+        assert np.max(np.abs(a - x.grad.numpy())) < 1e-10
