@@ -391,8 +391,9 @@ BWD_METRIC = "bs-attn bwd effective TFLOP/s (live blocks)"
 
 
 def run_bwd(args):
-    """Backward pass: one step = one bsattn_bwd call (the dO.O row term and the
-    gradient kernel) on the workload, inputs resident, L2 flushed before each."""
+    """Backward pass: one step = one bsattn_bwd call (the dO.O row term, the
+    dK/dV kernel and the dQ kernel) on the workload, inputs resident, L2
+    flushed before each."""
     import torch
     import torch.distributed as dist
 
@@ -485,12 +486,13 @@ def run_bwd(args):
                        "l2": "flushed (512 MB write) before every timed step",
                        "parallelism": f"replicas x{world} (independent problems, no collective)"},
             "e2e": None,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": 3 * args.steps,  # row term, dK/dV and dQ kernels
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"],
                          "unit": UNIT, "frac": achieved / peaks["bf16"], "traffic": None,
                          "peak_source": f"bf16 dense burst, {peaks['source']}",
                          "frac_of_spec_2250": achieved / 2250.0,
-                         "kernel": "bsattn_bwd_kernel (with the dO.O row-term kernel)",
+                         "kernel": "bsattn_bwd_kernel + bsattn_bwd_dq_kernel + row term "
+                                   "(whole step)",
                          "ms_per_launch": ms_mean},
             "cpu_baseline": cpu,
             "clocks": clk,
