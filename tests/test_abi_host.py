@@ -95,3 +95,26 @@ def test_kernel_source_is_tcgen05_tma():
         assert needle in src
     from block_sparse_flash_attn_gb300 import _build
     assert "arch=compute_103a,code=sm_103a" in " ".join(_build.ARCH)
+
+
+def test_backward_and_gqa_reject_missing_plan(lib):
+    """The entry points added for the backward pass and grouped-query attention
+    check the plan handle before anything else."""
+    import block_sparse_flash_attn_gb300 as bs
+    vp = ctypes.c_void_p
+    fake = vp(0x10000)
+    f = ctypes.c_float(0.1)
+    assert lib.bsattn_bwd(fake, fake, fake, fake, fake, fake, vp(0), fake, fake, fake,
+                          1, 1, 128, 128, f, vp(0)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_bwd_gqa(fake, fake, fake, fake, fake, fake, vp(0), fake, fake, fake,
+                              1, 4, 2, 128, 128, f, vp(0)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_fwd_gqa(fake, fake, fake, vp(0), fake, fake, 1, 4, 2, 128, 128, f,
+                              vp(0)) == bs.ERR_INVALID_ARG
+    cp, ri, n = vp(), vp(), ctypes.c_int64()
+    assert lib.bsattn_plan_csc(vp(0), ctypes.byref(cp), ctypes.byref(ri), ctypes.byref(n)) == \
+        bs.ERR_INVALID_ARG
+    # the shared-mask flag is accepted by the argument check; an unknown bit is not
+    out = vp()
+    assert lib.bsattn_plan(vp(0), 1, 4, 128, bs.MASK_SHARED_HEADS, vp(0), ctypes.byref(out)) == \
+        bs.ERR_INVALID_ARG  # (null mask)
+    assert lib.bsattn_plan(fake, 1, 4, 128, 16, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
