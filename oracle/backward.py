@@ -75,7 +75,7 @@ def allowed_matrix(mask_bh: np.ndarray, S: int, causal: bool) -> np.ndarray:
     return allowed
 
 
-def _head(q, k, v, do, allowed, scale, bounds):
+def _head(q, k, v, do, allowed, scale, bounds, o_bf16=True, acc_mult=1):
     """One (batch, head): the formulas of the module docstring, in order."""
     s = scale * (q @ k.T)
     s = np.where(allowed, s, -np.inf)
@@ -98,27 +98,82 @@ def _head(q, k, v, do, allowed, scale, bounds):
     dv = (P if _mutation == 2 else P.T) @ do
     if not bounds:
         return dq, dk, dv, None
-    # Per-element error bounds of a kernel that rounds P and dS to bf16 (relative
-    # 2^-9 each) and forms Dl from a bf16-rounded O (relative 2^-9 per product).
-    u = 2.0 ** -9
-    E = np.abs(do * O).sum(axis=1)                   # sum_d |dO_id O_id|
-    dS_w = np.abs(dS) + P * E[:, None]               # weight of the dS error
-    b = (u * abs(scale) * (dS_w @ np.abs(k)),
-         u * abs(scale) * (dS_w.T @ np.abs(q)),
-         u * (np.abs(P).T @ np.abs(do)))
-    return dq, dk, dv, b
+    return dq, dk, dv, _bounds(q, k, v, do, allowed, scale, s, P, O, dP, dS, m, l, o_bf16,
+                               acc_mult)
+
+
+# Error model of a kernel that computes the gradients this way (it is the
+# arithmetic of the CUDA backward pass, stated here so the bound can be
+# checked by reading):
+#   * Q, K, V, dO are bf16 inputs, used exactly;
+#   * S = Q K^T and dP = dO V^T come from the tensor core in fp32 (products
+#     exact, D additions);
+#   * P is recomputed as 2^(S scale log2 e - LSE log2 e) in fp32 with a
+#     hardware exp2 approximation, from the given fp32 LSE;
+#   * Dl = dO . O in fp32 over the given O (bf16 or fp32);
+#   * dS = P (dP - Dl) in fp32;
+#   * P and dS are rounded to bf16 (round to nearest) as tensor-core operands;
+#   * dV = P^T dO, dK = dS^T Q, dQ = dS K accumulate in fp32 over every live
+#     row (dV, dK) or key (dQ), then dK and dQ are multiplied by scale.
+U_BF16 = 2.0 ** -8    # unit roundoff of bf16 (8 significant bits, round to nearest)
+U_F32 = 2.0 ** -24    # unit roundoff of fp32
+ADD_F32 = 2.0 ** -23  # one fp32 addition that may truncate instead of rounding
+# Relative error of the hardware exp2 approximation: a deliberately loose
+# bound (the approximation is accurate to a few fp32 ulps, ~2^-22); any value
+# in between changes the bound by less than 1 %.
+EXP2_REL = 2.0 ** -16
+LOG2E = 1.0 / np.log(2.0)
+# P below fp32's normal range is flushed to zero by the kernel's exp2; each
+# such P is off by at most 2^-126, which this absolute term covers for any
+# sum of up to 2^20 of them times |values| <= 2^6.
+ABS_FLOOR = 2.0 ** -100
+
+
+def _bounds(q, k, v, do, allowed, scale, s, P, O, dP, dS, m, l, o_bf16, acc_mult):
+    """Per-element bounds on |kernel - exact| for (dQ, dK, dV) of one head,
+    first order in the roundings of the error model above, times (1 + 2^-7)
+    for the neglected products of two rounding errors."""
+    D = q.shape[1]
+    aq, ak, av, ado = np.abs(q), np.abs(k), np.abs(v), np.abs(do)
+    sl = abs(scale) * LOG2E
+    # error of the exponent x = S sl - LSE log2 e: the S product (D additions),
+    # the fused multiply-add and the fp32 LSE (stored and converted)
+    live = allowed.any(axis=1)
+    lse2 = np.where(live, (m + np.log(np.where(live, l, 1.0))) * LOG2E, 0.0)
+    x_abs = np.where(allowed, np.abs(s) * LOG2E, 0.0)
+    dx = sl * D * ADD_F32 * (aq @ ak.T) + 4 * U_F32 * (x_abs + np.abs(lse2)[:, None])
+    eps_p = np.where(allowed, np.log(2.0) * dx + EXP2_REL, 0.0)   # relative error of P
+    # dP (D additions) and Dl (O's storage rounding and D additions)
+    u_o = U_BF16 if o_bf16 else U_F32
+    E = np.abs(do * O).sum(axis=1)
+    ddp = D * ADD_F32 * (ado @ av.T)
+    ddl = (u_o + D * ADD_F32) * E
+    # dS before and after its bf16 rounding
+    ads = np.abs(dS)
+    dds = (U_BF16 + eps_p + 2 * U_F32) * ads + P * (ddp + ddl[:, None])
+    # accumulation lengths: live rows per key (dV, dK), live keys per row (dQ)
+    n_col = acc_mult * allowed.sum(axis=0).astype(np.float64)
+    n_row = allowed.sum(axis=1).astype(np.float64)
+    g_col = n_col * ADD_F32
+    g_row = n_row * ADD_F32
+    bv = (U_BF16 + g_col[:, None]) * (P.T @ ado) + (eps_p * P).T @ ado
+    bk = abs(scale) * (dds.T @ aq + (g_col + U_F32)[:, None] * (ads.T @ aq))
+    bq = abs(scale) * (dds @ ak + (g_row + U_F32)[:, None] * (ads @ ak))
+    slack = 1.0 + 2.0 ** -7
+    return tuple(slack * b + ABS_FLOOR for b in (bq, bk, bv))
 
 
 def attention_bwd(q, k, v, do, mask, scale: float, causal: bool = False, heads=None,
-                  bounds: bool = False):
+                  bounds: bool = False, o_bf16: bool = True, acc_mult: int = 1):
     """Gradients (dQ, dK, dV) of exact block-sparse attention, fp64.
 
     q, k, v, do: [B][H][S][D] as bf16 bit patterns (uint16) or float64.
     mask: uint8 [B][H][S/128][S/128].  heads: iterable of (b, h) to compute,
     or None for all.  Returns float64 arrays [B][H][S][D] (heads not computed
     are NaN); with bounds=True also a tuple of per-element error bounds
-    (same shapes) for a kernel computing in the precision described in
-    ``_head``.
+    (same shapes) for a kernel computing with the error model of ``_bounds``
+    (o_bf16: the O it is given was rounded to bf16, else to fp32;
+    acc_mult: dK and dV rows accumulate over that many heads' live rows).
     """
     q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
     mask = np.asarray(mask, dtype=np.uint8)
@@ -136,7 +191,8 @@ def attention_bwd(q, k, v, do, mask, scale: float, causal: bool = False, heads=N
         heads = [(b, h) for b in range(B) for h in range(H)]
     for b, h in heads:
         allowed = allowed_matrix(mask[b, h], S, causal)
-        dq, dk, dv, bb = _head(q[b, h], k[b, h], v[b, h], do[b, h], allowed, float(scale), bounds)
+        dq, dk, dv, bb = _head(q[b, h], k[b, h], v[b, h], do[b, h], allowed, float(scale), bounds,
+                               o_bf16=o_bf16, acc_mult=acc_mult)
         out[0][b, h], out[1][b, h], out[2][b, h] = dq, dk, dv
         if bounds:
             for t in range(3):
@@ -169,7 +225,7 @@ def csc(mask, causal: bool = False):
 
 
 def attention_bwd_gqa(q, k, v, do, mask, scale: float, causal: bool = False,
-                      bounds: bool = False):
+                      bounds: bool = False, o_bf16: bool = True):
     """Gradients for grouped-query attention, fp64: q, do [B][H][S][D]; k, v
     [B][Hkv][S][D] (query head h attends with K/V head h // (H // Hkv)); mask
     [B][H][nb][nb] or [B][1][nb][nb] shared by the heads.
@@ -177,7 +233,9 @@ def attention_bwd_gqa(q, k, v, do, mask, scale: float, causal: bool = False,
     The gradients of attention on K and V with each head repeated H // Hkv
     times (attention_bwd), with dK and dV of each K/V head summed over the
     query heads of its group (the chain rule through the repetition); with
-    bounds=True the per-element bounds are summed the same way."""
+    bounds=True the per-element bounds are summed the same way, each with the
+    accumulation length of the whole group (the kernel adds all g heads' terms
+    into one fp32 sum)."""
     q, k, v, do = (_as_f64(x) for x in (q, k, v, do))
     B, H, S, D = q.shape
     Hkv = k.shape[1]
@@ -188,7 +246,8 @@ def attention_bwd_gqa(q, k, v, do, mask, scale: float, causal: bool = False,
     mask = np.asarray(mask, dtype=np.uint8)
     if mask.shape[1] == 1 and H > 1:
         mask = np.broadcast_to(mask, (B, H) + mask.shape[2:])
-    res = attention_bwd(q, k_rep, v_rep, do, mask, scale, causal, bounds=bounds)
+    res = attention_bwd(q, k_rep, v_rep, do, mask, scale, causal, bounds=bounds, o_bf16=o_bf16,
+                        acc_mult=g)
 
     def fold(x):
         return x.reshape(B, Hkv, g, S, D).sum(axis=2)

@@ -177,3 +177,48 @@ def test_gqa_gradients_against_torch_autograd(Hkv, causal):
     got = oracle.attention_bwd_gqa(q, k, v, G, mask, 0.3, causal)
     for a, x in zip(got, t):
         assert np.max(np.abs(a - x.grad.numpy())) < 1e-10
+
+
+def _bf16_round(x):
+    """Round float32 values to bf16 (nearest, ties to even), returned as float32."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("o_bf16", [True, False])
+@pytest.mark.parametrize("case", range(4))
+def test_error_bounds_cover_a_reduced_precision_emulation(case, o_bf16):
+    """The per-element bounds hold for a numpy emulation of the error model
+    they describe (fp32 products and sums, P from the fp32 LSE with a float32
+    exp2, bf16-rounded P and dS as product operands, O given rounded), and
+    are not vacuous: the worst element uses a sizeable part of its bound."""
+    B, H, S, D, mask, causal, scale = _cases()[case]
+    f32 = np.float32
+    q, k, v, do = (_bf16_round(_rand(60 + case * 4 + i, (B, H, S, D))).astype(np.float64)
+                   for i in range(4))
+    O, L = oracle.attention(q, k, v, mask, scale, causal)
+    (dq, dk, dv), bounds = ob.attention_bwd(q, k, v, do, mask, scale, causal, bounds=True,
+                                            o_bf16=o_bf16)
+    ratios = []
+    for b in range(B):
+        for h in range(H):
+            allowed = ob.allowed_matrix(mask[b, h], S, causal)
+            live = allowed.any(axis=1)
+            qq, kk, vv, gg = (x[b, h].astype(f32) for x in (q, k, v, do))
+            sl = f32(scale / np.log(2.0))
+            l2 = np.where(live, L[b, h] / np.log(2.0), 0.0).astype(f32)
+            s = qq @ kk.T
+            p = np.where(allowed, np.exp2(s * sl - l2[:, None]), f32(0)).astype(f32)
+            o_in = _bf16_round(O[b, h].astype(f32)) if o_bf16 else O[b, h].astype(f32)
+            dl = (gg * o_in).sum(axis=1, dtype=f32)
+            dp = gg @ vv.T
+            ds = (p * (dp - dl[:, None])).astype(f32)
+            pb, dsb = _bf16_round(p), _bf16_round(ds)
+            got = (f32(scale) * (dsb @ kk), f32(scale) * (dsb.T @ qq), pb.T @ gg)
+            for g, ref, bd in zip(got, (dq, dk, dv), bounds):
+                err = np.abs(g.astype(np.float64) - ref[b, h])
+                assert np.all(err <= bd[b, h])
+                ratios.append(float(np.max(err / bd[b, h])))
+    print("max err / bound", max(ratios))
+    assert max(ratios) > 0.02, ratios
