@@ -149,13 +149,6 @@ def csr(mask, causal: bool = False):
     return row_ptr, col_idx[:nnz]
 
 
-def flops_live(mask, D: int, causal: bool = False) -> int:
-    """Work the method does, counted over live blocks: 4*128*128*D per block."""
-    row_ptr, _ = csr(mask, causal)
-    return int(row_ptr[-1]) * 4 * BLOCK * BLOCK * D
-
-
-
 def attention_gqa(q, k, v, mask, scale: float, causal: bool = False, rows=None):
     """Grouped-query attention, fp64: q [B][H][S][D], k and v [B][Hkv][S][D]
     with H % Hkv == 0; query head h attends with K/V head h // (H // Hkv).
