@@ -28,6 +28,7 @@ BLOCK = 128
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_INTERNAL = range(7)
 ERR_SCRATCH_LIMIT = 7
+ERR_RANGE = 8
 CAUSAL, OUT_F32, MASK_SHARED_HEADS = 1, 2, 4
 
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
@@ -311,11 +312,40 @@ def fwd_noalloc(q, k, v, mask, causal: bool = False, scale: float | None = None,
     live in the library's fixed 16 MiB device array (see bsattn_fwd_noalloc in
     include/bsattn.h for the limit and the sharing rules).  Output tensors are
     allocated here by torch only when not passed in.
+
+    Every tensor is checked before the call (the C entry point sees only raw
+    pointers and cannot tell a host tensor or a short buffer from a good one):
+    q, k, v contiguous bf16 [B, H, S, D] of one shape; mask contiguous uint8
+    [B, H, S/128, S/128]; out and lse of the output dtype and shape; all on
+    one CUDA device.
     """
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be a bf16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one shape [B, H, S, D]")
     B, H, S, D = q.shape
+    if S % BLOCK:
+        raise ValueError("S must be a multiple of 128")
+    nb = S // BLOCK
+    if not isinstance(mask, torch.Tensor) or mask.dtype != torch.uint8:
+        raise TypeError("mask must be a uint8 tensor")
+    if tuple(mask.shape) != (B, H, nb, nb) or not mask.is_contiguous():
+        raise ValueError(f"mask must be contiguous [B, H, S/128, S/128] = {(B, H, nb, nb)}")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     odt = torch.float32 if out_f32 else torch.bfloat16
+    if out is not None and (out.dtype != odt or tuple(out.shape) != (B, H, S, D)
+                            or not out.is_contiguous()):
+        raise ValueError("out must be contiguous [B, H, S, D] of the output dtype")
+    if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, S)
+                            or not lse.is_contiguous()):
+        raise ValueError("lse must be contiguous fp32 [B, H, S]")
+    for name, t in (("q", q), ("k", k), ("v", v), ("mask", mask), ("out", out), ("lse", lse)):
+        if t is not None and (not t.is_cuda or t.device != q.device):
+            raise TypeError(f"{name} must be on q's CUDA device")
     if out is None:
         out = torch.empty((B, H, S, D), dtype=odt, device=q.device)
     if lse is None:

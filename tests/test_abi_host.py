@@ -118,3 +118,34 @@ def test_backward_and_gqa_reject_missing_plan(lib):
     assert lib.bsattn_plan(vp(0), 1, 4, 128, bs.MASK_SHARED_HEADS, vp(0), ctypes.byref(out)) == \
         bs.ERR_INVALID_ARG  # (null mask)
     assert lib.bsattn_plan(fake, 1, 4, 128, 16, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+
+
+def test_noalloc_wrapper_rejects_bad_tensors_before_any_call(monkeypatch):
+    """The allocation-free wrapper checks every tensor itself (the C entry point
+    sees raw pointers only): a host mask, a K of another shape, a mask of the
+    wrong block shape and a non-contiguous Q are rejected before the library is
+    even loaded."""
+    import torch
+
+    import block_sparse_flash_attn_gb300 as bs
+
+    def no_load():
+        raise AssertionError("the library must not be reached")
+
+    monkeypatch.setattr(bs, "load", no_load)
+    B, H, S, D = 1, 2, 256, 64
+    q = torch.zeros((B, H, S, D), dtype=torch.bfloat16)
+    mask = torch.ones((B, H, 2, 2), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="one shape"):
+        bs.fwd_noalloc(q, q[:, :1].contiguous(), q, mask)
+    with pytest.raises(ValueError, match="mask"):
+        bs.fwd_noalloc(q, q, q, torch.ones((B, H, 3, 3), dtype=torch.uint8))
+    with pytest.raises(TypeError, match="mask"):
+        bs.fwd_noalloc(q, q, q, mask.float())
+    with pytest.raises(ValueError, match="contiguous"):
+        bs.fwd_noalloc(q.transpose(2, 3), q, q, mask)
+    with pytest.raises(ValueError, match="lse"):
+        bs.fwd_noalloc(q, q, q, mask, lse=torch.zeros((B, H, S + 1)))
+    # right shapes and dtypes, but host tensors (a host mask among them)
+    with pytest.raises(TypeError, match="CUDA device"):
+        bs.fwd_noalloc(q, q, q, mask)

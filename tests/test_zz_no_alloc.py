@@ -2,7 +2,8 @@
 memory (a framework that owns the device memory pool, a plug-in that may not
 allocate once running, a loop that cannot absorb cudaMalloc's device-wide
 synchronisation).  Its plan and scratch live in the library's fixed device
-array, so it must give the same O and LSE as bsattn_plan + bsattn_fwd.
+array; it must match the fp64 oracle at the forward tolerance, and give
+the same O and LSE as bsattn_plan + bsattn_fwd.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.  It builds the library itself
@@ -13,6 +14,7 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workloads
 from _util import compare, to_dev
 
@@ -41,24 +43,33 @@ def _case(seed, B, H, S, D, p, causal):
     return q, k, v, mask, causal
 
 
-def _call_noalloc(bs, q, k, v, mask_d, causal, out_f32, scale):
+def _outputs(q, out_f32):
     import torch
-    lib = bs.load()
     B, H, S, D = q.shape
     out = torch.empty((B, H, S, D), dtype=torch.float32 if out_f32 else torch.bfloat16,
                       device="cuda")
     lse = torch.empty((B, H, S), dtype=torch.float32, device="cuda")
-    flags = (bs.CAUSAL if causal else 0) | (bs.OUT_F32 if out_f32 else 0)
+    return out, lse
+
+
+def _call_noalloc(bs, q, k, v, mask_d, causal, scale, out, lse):
+    import torch
+    lib = bs.load()
+    B, H, S, D = q.shape
+    flags = (bs.CAUSAL if causal else 0) | (bs.OUT_F32 if out.dtype == torch.float32 else 0)
     vp = ctypes.c_void_p
     st = lib.bsattn_fwd_noalloc(vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()),
                                 vp(mask_d.data_ptr()), vp(out.data_ptr()), vp(lse.data_ptr()),
                                 B, H, S, D, ctypes.c_float(scale), flags,
                                 vp(torch.cuda.current_stream().cuda_stream))
     assert st == bs.OK, bs.status_string(st)
-    return out, lse
 
 
-def test_noalloc_matches_plan_and_fwd_on_two_calls(bs):
+def test_noalloc_matches_oracle_and_plan_fwd_on_two_calls(bs):
+    """Two calls in a row through the C ABI: each is checked against the fp64
+    oracle and against bsattn_plan + bsattn_fwd, at the forward tolerance.
+    The second call must also leave the device's free memory unchanged (it
+    allocates nothing), and the Python wrapper must give the same result."""
     import torch
     cases = [_case(501, 2, 4, 1024, 128, 0.4, True), _case(502, 1, 3, 512, 64, 0.6, False)]
     for i, (qb, kb, vb, mask, causal) in enumerate(cases):
@@ -66,17 +77,33 @@ def test_noalloc_matches_plan_and_fwd_on_two_calls(bs):
         q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
         mask_d = torch.from_numpy(mask).cuda()
         scale = qb.shape[-1] ** -0.5
-        # existing entry points
+        O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(scale), causal)
+        # the existing entry points
         p = bs.plan(mask_d, causal=causal, out_f32=out_f32)
-        o_ref, l_ref = bs.fwd(q, k, v, p, scale)
+        o_pf, l_pf = bs.fwd(q, k, v, p, scale)
         bs.plan_status(p)
         p.close()
-        # the allocation-free entry point, through the C ABI
-        o, l = _call_noalloc(bs, q, k, v, mask_d, causal, out_f32, scale)
-        ok, rep = compare(o.float().cpu().numpy(), l.cpu().numpy(),
-                          o_ref.float().cpu().numpy().astype(np.float64),
-                          l_ref.cpu().numpy().astype(np.float64), out_bf16=not out_f32)
-        assert ok, (i, rep)
+        o_pf = o_pf.float().cpu().numpy().astype(np.float64)
+        l_pf = l_pf.cpu().numpy().astype(np.float64)
+        out, lse = _outputs(q, out_f32)
+        for call in range(2):
+            torch.cuda.synchronize()
+            free0 = torch.cuda.mem_get_info()[0]
+            out.fill_(float("nan"))
+            lse.fill_(float("nan"))
+            _call_noalloc(bs, q, k, v, mask_d, causal, scale, out, lse)
+            torch.cuda.synchronize()
+            if call == 1:  # after one warm call (lazy module loading is done)
+                assert torch.cuda.mem_get_info()[0] == free0, "device memory was allocated"
+            o = out.float().cpu().numpy()
+            l = lse.cpu().numpy()
+            ok, rep = compare(o, l, O_ref, L_ref, out_bf16=not out_f32)
+            assert ok, ("oracle", i, call, rep)
+            ok, rep = compare(o, l, o_pf, l_pf, out_bf16=not out_f32)
+            assert ok, ("plan+fwd", i, call, rep)
+        o_w, l_w = bs.fwd_noalloc(q, k, v, mask_d, causal=causal, scale=scale, out_f32=out_f32)
+        torch.cuda.synchronize()
+        assert torch.equal(o_w, out) and torch.equal(l_w, lse)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(bs):
