@@ -102,6 +102,32 @@ def normal_f64(seed: int, stream: int, shape, mult: float = 1.0) -> np.ndarray:
     return out.reshape(shape)
 
 
+# e4m3 (the OCP 8-bit format: sign, 4 exponent bits with bias 7, 3 mantissa
+# bits, no infinities, 0x7F / 0xFF NaN): the 127 non-negative finite values,
+# indexed by their code 0x00..0x7E, for rounding inputs to the format.
+_E4M3_POS = np.array([(m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 ** (e - 7)
+                      for e in range(16) for m in range(8)][:127])
+
+
+def e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round values to e4m3 (nearest, ties to the even code; beyond +-448
+    saturates to +-448; NaN -> 0x7F); returns the uint8 bit patterns."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), _E4M3_POS[-1])
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x) & (code != 0), code | 0x80, code)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def normal_e4m3(seed: int, stream: int, shape, mult: float = 1.0) -> np.ndarray:
+    """N(0,1)*mult (the same draws as normal_f64) rounded to e4m3; uint8 bits."""
+    return e4m3_bits(normal_f64(seed, stream, shape, mult))
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns to float32 (for display/tests)."""
     return (bits.astype(np.uint32) << 16).view(np.float32)
