@@ -175,3 +175,4 @@ def attention_gqa(q, k, v, mask, scale: float, causal: bool = False, rows=None):
 
 from .backward import BWD_MUTATIONS, attention_bwd, attention_bwd_gqa, csc, set_bwd_mutation  # noqa: E402,F401,E501
 from .fp8 import attention_fp8, decode_e4m3  # noqa: E402,F401
+from .keyblocks import attention_kb, csr_kb  # noqa: E402,F401
