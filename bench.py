@@ -6,15 +6,21 @@ Prints ONE JSON line (rank 0):
            (query block, key block) pair; diagonal causal blocks count in
            full), with its fraction of the bf16 dense tensor peak
   value    whole-job throughput with inputs resident in HBM: sum over ranks of
-           live flop / max over ranks of the mean per-step kernel time
+           live flop / max over ranks of the mean per-step kernel time, on the
+           headline workload (default: the random 10 % mask at S = 65536, the
+           largest of the five workloads)
   e2e      the same metric through the public API with host buffers
            (HostPipeline): each step copies Q, K, V from pinned host memory to
            the device, runs the forward and copies O and LSE back, all inside
            the timed region; the copies of one piece of the (batch, head)
            range overlap the forward of another
-  roofline the forward kernel against the tensor-core peak: achieved =
-           live flop per launch / average launch time (CUDA events on the
-           launching stream)
+  roofline the forward kernel against its binding roofline: the larger of
+           live flop / bf16 tensor peak and algorithmic bytes / HBM peak;
+           achieved = that work per launch / average launch time (CUDA events
+           on the launching stream); traffic = measured DRAM bytes per launch
+           from the committed ncu capture of the same kernel source, else null
+  per_config  every one of the five workloads timed the same way for at least
+           --config-seconds each (bf16 O), with its own roofline and clocks
   cpu_baseline  the fp64 CPU oracle timed on a bounded sample of the workload
 
 A step is one forward pass (the only kernel of the hot path; the plan is built
@@ -28,6 +34,7 @@ tensors (see workloads/).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -54,10 +61,14 @@ L2_FLUSH_BYTES = 512 << 20
 E2E_PIECE_BYTES = 24 << 20
 E2E_MAX_PIECES = 8  # each piece costs a plan, a launch and five copies of host time
 
-# DRAM traffic of one forward launch (dram__bytes_read.sum + dram__bytes_write.sum)
-# of the current forward kernel, from the ncu capture summarised in
-# profiles/bsattn_fwd_kernel-causal-s4096-d128.md; workloads not captured: None.
-TRAFFIC_BYTES = {"w2_bf16": 308_948_736 + 48_557_312}
+# Measured DRAM traffic per forward launch: a table under profiles/ written
+# from ncu captures (dram__bytes_read.sum + dram__bytes_write.sum), one line
+# per (workload, output dtype) with the hash of the kernel source captured.
+# A line counts only while the kernel source still has that hash.
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "bsattn_fwd_kernel-dram-traffic.txt")
+KERNEL_SOURCES = [os.path.join(ROOT, "block_sparse_flash_attn_gb300", "csrc", f)
+                  for f in ("fwd_sm103.cu", "ptx.cuh", "internal.h")]
+HEADLINE_WORKLOAD = 4  # the largest single-GPU workload (B=1 H=32 S=65536 D=128)
 
 
 def parse_args(argv=None):
@@ -65,13 +76,26 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", type=int, default=HEADLINE_WORKLOAD,
+                    choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--out-f32", action="store_true", help="write O as fp32 (default bf16)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=5, help="0 skips the end-to-end leg")
+    ap.add_argument("--configs", default="all",
+                    help="workloads timed for per_config: 'all', 'none' or a list like 2,5")
+    ap.add_argument("--config-seconds", type=float, default=1.0,
+                    help="minimum timed seconds per per_config workload")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workloads with this many heads instead (a smaller case of the "
+                         "same kernel, e.g. for an ncu capture)")
+    ap.add_argument("--in-dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="e4m3: FP8 Q, K, V (the same normal draws rounded to e4m3; head_dim "
+                         "128 workloads only)")
+    ap.add_argument("--key-block", type=int, default=128, choices=[128, 64],
+                    help="64: the workloads' masks at 64-key granularity (plans with key_block=64)")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
                     help="fwd (default: the forward hot path) or bwd (gradients dQ, dK, dV)")
     return ap.parse_args(argv)
@@ -82,25 +106,29 @@ def parse_args(argv=None):
 # ----------------------------------------------------------------------------
 
 def live_blocks(mask: np.ndarray, causal: bool) -> int:
+    """Live (query block, key block) pairs; the key blocks are 128 keys, or 64
+    when the mask has twice as many key blocks as query blocks."""
     m = mask.astype(bool)
     if causal:
-        nb = mask.shape[-1]
-        m = m & np.tril(np.ones((nb, nb), dtype=bool))
+        nbq, nbk = mask.shape[-2:]
+        kdiv = nbk // nbq
+        m = m & (np.arange(nbk)[None, :] < kdiv * (np.arange(nbq)[:, None] + 1))
     return int(np.count_nonzero(m))
 
 
-def flop_per_block(D: int) -> int:
-    return 4 * 128 * 128 * D
+def flop_per_block(D: int, key_block: int = 128) -> int:
+    return 4 * 128 * key_block * D
 
 
 def row_live_blocks(mask: np.ndarray, causal: bool, rows: np.ndarray, S: int) -> np.ndarray:
     """Live key blocks seen by each flat row id (b*H+h)*S+i."""
-    B, H, nb, _ = mask.shape
+    B, H, nb, nbk = mask.shape
+    kdiv = nbk // nb
     bh, i = np.divmod(rows, S)
     qb = i // 128
-    m = mask.reshape(B * H, nb, nb)[bh, qb].astype(bool)
+    m = mask.reshape(B * H, nb, nbk)[bh, qb].astype(bool)
     if causal:
-        m = m & (np.arange(nb)[None, :] <= qb[:, None])
+        m = m & (np.arange(nbk)[None, :] < kdiv * (qb[:, None] + 1))
     return m.sum(axis=1)
 
 
@@ -131,6 +159,69 @@ def read_peaks():
     except Exception:  # noqa: BLE001 - absent or unreadable file
         return {"bf16": FALLBACK_BF16_TFLOPS, "bf16_sustained": 1700.0, "hbm": FALLBACK_HBM_GBS,
                 "source": "fallback"}
+
+
+def algorithmic_bytes(mask: np.ndarray, causal: bool, S: int, D: int, out_bytes: int,
+                      in_bytes: int = 2) -> int:
+    """HBM bytes one forward launch cannot avoid: Q rows of tiles with a live
+    block, K and V rows of key blocks some tile uses (bf16), O and LSE of every
+    row written once, and the plan entries the kernel reads (int32)."""
+    B, H, nb, nbk = mask.shape
+    kdiv = nbk // nb
+    m = mask.astype(bool)
+    if causal:
+        m = m & (np.arange(nbk)[None, :] < kdiv * (np.arange(nb)[:, None] + 1))
+    q_tiles = int(m.any(axis=3).sum())
+    kv_blocks = int(m.any(axis=2).sum())
+    rows = B * H * S
+    plan_words = int(m.sum()) + B * H * nb + 1 + q_tiles
+    return (q_tiles * 128 + 2 * kv_blocks * (128 // kdiv)) * D * in_bytes + \
+        rows * D * out_bytes + rows * 4 + 4 * plan_words
+
+
+def roofline(flop: float, nbytes: float, ms: float, peaks: dict, traffic) -> dict:
+    """The binding roofline of one launch: the larger of flop / tensor peak and
+    algorithmic bytes / HBM peak sets the unit; frac = achieved / peak."""
+    t_tensor = flop / (peaks["bf16"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm"] * 1e9)
+    if t_tensor >= t_hbm:
+        achieved = flop / (ms * 1e-3) / 1e12
+        r = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+             "peak_source": f"bf16 dense burst, {peaks['source']}"}
+    else:
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+             "peak_source": f"HBM copy bandwidth, {peaks['source']}"}
+    r.update(frac=r["achieved"] / r["peak"], traffic=traffic, algorithmic_bytes=nbytes,
+             flop=flop, t_floor_us={"tensor": 1e6 * t_tensor, "hbm": 1e6 * t_hbm},
+             tflops=flop / (ms * 1e-3) / 1e12, frac_of_spec_2250=flop / (ms * 1e-3) / 1e12 / 2250.0,
+             kernel="bsattn_fwd_kernel", ms_per_launch=ms)
+    return r
+
+
+def kernel_source_sha16() -> str:
+    """Hash of the forward kernel's source files (which traffic figures apply)."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload_id: int, out_f32: bool):
+    """DRAM bytes per launch from the committed capture table, if it was taken
+    on the current kernel source; else None."""
+    want = (str(workload_id), "f32" if out_f32 else "bf16", kernel_source_sha16())
+    try:
+        with open(TRAFFIC_TABLE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 5 and not line.startswith("#") and tuple(parts[:3]) == want:
+                    return int(parts[3]) + int(parts[4])
+    except OSError:
+        pass
+    return None
 
 
 # ----------------------------------------------------------------------------
@@ -197,18 +288,22 @@ def oracle_sample_rate(w, q, k, v, mask, target_s: float, seed: int = 0):
     """Time the oracle on random rows of the workload; returns (TFLOP/s, rows, seconds)."""
     import oracle
     S, D = w.S, w.D
+    kdiv = mask.shape[3] // mask.shape[2]
     total_rows = q.shape[0] * q.shape[1] * S
     rng = np.random.default_rng(seed)
     n = 64
     while True:
         rows = np.sort(rng.choice(total_rows, size=min(n, total_rows), replace=False))
         t0 = time.perf_counter()
-        oracle.attention(q, k, v, mask, w.scale, w.causal, rows=rows)
+        if kdiv == 1:
+            oracle.attention(q, k, v, mask, w.scale, w.causal, rows=rows)
+        else:
+            oracle.attention_kb(q, k, v, mask, w.scale, w.causal, key_block=64, rows=rows)
         dt = time.perf_counter() - t0
         if dt >= 0.25 * target_s or n >= total_rows:
             break
         n = int(min(total_rows, n * max(2.0, 0.5 * target_s / max(dt, 1e-3))))
-    flop = float(row_live_blocks(mask, w.causal, rows, S).sum()) * 128 * 4 * D
+    flop = float(row_live_blocks(mask, w.causal, rows, S).sum()) * (128 // kdiv) * 4 * D
     return flop / dt / 1e12, len(rows), dt
 
 
@@ -250,6 +345,19 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def _workload_list(spec: str, headline: int):
+    """per_config workloads in run order, the headline's last (its tensors are
+    then reused for the headline's own timed steps)."""
+    if spec == "none":
+        ids = []
+    elif spec == "all":
+        ids = sorted(workloads.WORKLOADS)
+    else:
+        ids = sorted({int(x) for x in spec.split(",") if x.strip()})
+    ids = [i for i in ids if i != headline]
+    return ids + [headline]
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -267,98 +375,160 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     _build.build()
     bsattn.load()
-
-    w = workloads.WORKLOADS[args.workload]
-    # weak scaling: every rank runs its own full-size problem (independent heads)
-    qb, kb, vb = (workloads.normal_bf16(w.data_seed + 100 * rank, s, (w.B, w.H, w.S, w.D), w.mult)
-                  for s in (workloads.STREAM_Q, workloads.STREAM_K, workloads.STREAM_V))
-    mask = workloads.make_mask(w)
-    nlive = live_blocks(mask, w.causal)
-    flop = nlive * flop_per_block(w.D)
-
-    def to_dev(bits):
-        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
-
-    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
-    mask_d = torch.from_numpy(mask).to(dev)
-    plan = bsattn.plan(mask_d, causal=w.causal, out_f32=args.out_f32)
-    o, lse = bsattn.fwd(q, k, v, plan, w.scale)
-    bsattn.plan_status(plan)
+    peaks = read_peaks()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    launches = 0
 
+    fp8 = args.in_dtype == "e4m3"
+    fwd_call = bsattn.fwd_fp8 if fp8 else bsattn.fwd
+    if fp8:  # S = Q K^T at the e4m3 rate (2x bf16), P V in fp16 (1x): half the flop each
+        peaks = dict(peaks, bf16=peaks["bf16"] * 4.0 / 3.0,
+                     source=f"{peaks['source']} bf16 x 4/3 (e4m3 S, fp16 PV)")
+
+    def to_dev(bits):
+        if fp8:
+            return torch.from_numpy(bits).to(dev).view(torch.float8_e4m3fn)
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def traffic_key(wid):
+        return f"{wid}" + ("-kb64" if args.key_block == 64 else "") + ("-e4m3" if fp8 else "")
+
+    def timed(q, k, v, plan, scale, o, lse, steps):
+        """steps forward launches, each timed by CUDA events on the launching
+        stream after an L2 flush; barrier + synchronize on both sides."""
+        nonlocal launches
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        wall0 = time.perf_counter()
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            fwd_call(q, k, v, plan, scale, out=o, lse=lse)
+            e.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        launches += steps
+        return [s.elapsed_time(e) for s, e in ev], time.perf_counter() - wall0
+
+    def setup(wid, out_f32):
+        w = workloads.WORKLOADS[wid]
+        if args.heads:
+            w = dataclasses.replace(w, H=args.heads)
+        # weak scaling: every rank runs its own full-size problem (independent heads)
+        gen = workloads.normal_e4m3 if fp8 else workloads.normal_bf16
+        bits = tuple(gen(w.data_seed + 100 * rank, st, (w.B, w.H, w.S, w.D), w.mult)
+                     for st in (workloads.STREAM_Q, workloads.STREAM_K, workloads.STREAM_V))
+        mask = workloads.make_mask(w) if args.key_block == 128 else workloads.make_mask_kb64(w)
+        q, k, v = (to_dev(b) for b in bits)
+        mask_d = torch.from_numpy(mask).to(dev)
+        plan = bsattn.plan(mask_d, causal=w.causal, out_f32=out_f32, key_block=args.key_block)
+        o, lse = fwd_call(q, k, v, plan, w.scale)
+        bsattn.plan_status(plan)
+        return w, bits, mask, mask_d, q, k, v, plan, o, lse
+
+    # ---- per_config: every workload for at least --config-seconds; the
+    # headline workload last, its clock record running on into the headline steps
+    per_config = {}
+    head = None
+    head_clock = None
+    if fp8 and workloads.WORKLOADS[args.workload].D != 128:
+        raise SystemExit("--in-dtype e4m3 takes a head_dim 128 workload (2, 3 or 4)")
+    for wid in _workload_list(args.configs, args.workload):
+        if fp8 and workloads.WORKLOADS[wid].D != 128:
+            continue  # e4m3 inputs at head_dim 128 only
+        is_head = wid == args.workload
+        out_f32 = args.out_f32 if is_head else False
+        w, bits, mask, mask_d, q, k, v, plan, o, lse = setup(wid, out_f32)
+        for _ in range(max(3, args.warmup)):
+            flush.zero_()
+            fwd_call(q, k, v, plan, w.scale, out=o, lse=lse)
+        est, _ = timed(q, k, v, plan, w.scale, o, lse, 3)
+        est_ms = statistics.mean(est)
+        steps_c = int(min(4000, max(args.steps, np.ceil(1e3 * args.config_seconds /
+                                                         max(est_ms, 1e-3)))))
+        clocks = ClockSampler(local)
+        clocks.start()
+        ms, wall = timed(q, k, v, plan, w.scale, o, lse, steps_c)
+        bsattn.plan_status(plan)
+        nlive = live_blocks(mask, w.causal)
+        flop = nlive * flop_per_block(w.D, args.key_block)
+        ms_max = max_over_ranks(statistics.mean(ms), dev)
+        nbytes = algorithmic_bytes(mask, w.causal, w.S, w.D, 4 if out_f32 else 2,
+                                   1 if fp8 else 2)
+        entry = {"workload": f"{w.id}:{w.name}", "out_dtype": "f32" if out_f32 else "bf16",
+                 "steps": steps_c, "ms_per_step": ms_max,
+                 "value": whole_job_tflops(flop, world, ms_max), "unit": UNIT,
+                 "wall_s_timed_region": wall,
+                 "roofline": roofline(flop, nbytes, statistics.mean(ms), peaks,
+                                      measured_traffic(traffic_key(w.id), out_f32))}
+        if is_head:
+            head = (w, bits, mask, mask_d, q, k, v, plan, o, lse, nlive, flop, nbytes)
+            head_clock = clocks
+        else:
+            entry["clocks"] = clocks.stop()
+            plan.close()
+            del q, k, v, o, lse, mask_d
+        per_config[str(wid)] = entry
+
+    # ---- headline: exactly --steps timed steps after --warmup untimed ones
+    w, bits, mask, mask_d, q, k, v, plan, o, lse, nlive, flop, nbytes = head
     for _ in range(args.warmup):
         flush.zero_()
-        bsattn.fwd(q, k, v, plan, w.scale, out=o, lse=lse)
+        fwd_call(q, k, v, plan, w.scale, out=o, lse=lse)
     torch.cuda.synchronize()
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for s, e in ev:
-        flush.zero_()
-        s.record(stream)
-        bsattn.fwd(q, k, v, plan, w.scale, out=o, lse=lse)
-        e.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    wall = time.perf_counter() - wall0
-    clk = clocks.stop()
+    ms, wall = timed(q, k, v, plan, w.scale, o, lse, args.steps)
+    head_launches = args.steps
+    clk = head_clock.stop()
+    if str(w.id) in per_config:
+        per_config[str(w.id)]["clocks"] = clk
     bsattn.plan_status(plan)
-    ms = [s.elapsed_time(e) for s, e in ev]
     ms_mean = statistics.mean(ms)
     ms_max = max_over_ranks(ms_mean, dev)
     value = whole_job_tflops(flop, world, ms_max)
 
-    # end to end through the public API with pinned host buffers
-    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
-                  for x in (qb, kb, vb))
-    ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
-    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
-
-    # the public host-buffer path: per piece of the (batch, head) range, the
-    # upload, the forward and the download run on their own streams, overlapped
-    pieces = min(w.B * w.H, E2E_MAX_PIECES, max(4, -(-h2d // E2E_PIECE_BYTES)))
-    pipe = bsattn.HostPipeline(mask_d, w.D, causal=w.causal, out_f32=args.out_f32,
-                               chunks=pieces)
-
-    def e2e_step():
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    # the host pipeline takes bf16 inputs and 128-key blocks
+    if args.e2e_steps > 0 and args.key_block == 128 and not fp8:
+        qb, kb, vb = bits
+        hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+                      for x in (qb, kb, vb))
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+        d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+        # the public host-buffer path: per piece of the (batch, head) range, the
+        # upload, the forward and the download run on their own streams, overlapped
+        pieces = min(w.B * w.H, E2E_MAX_PIECES, max(4, -(-h2d // E2E_PIECE_BYTES)))
+        pipe = bsattn.HostPipeline(mask_d, w.D, causal=w.causal, out_f32=args.out_f32,
+                                   chunks=pieces)
         pipe.run(hq, hk, hv, ho, hl, w.scale, stream=stream)
-
-    e2e_step()
-    torch.cuda.synchronize()
-    pipe.status()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    pipe.status()
-    pipe.close()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
-    e2e_value = whole_job_tflops(flop, world, e2e_ms)
-
-    peaks = read_peaks()
-    achieved = flop / (ms_mean * 1e-3) / 1e12
-    key = f"w{w.id}_{'f32' if args.out_f32 else 'bf16'}"
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16"], "unit": UNIT,
-                "frac": achieved / peaks["bf16"], "traffic": TRAFFIC_BYTES.get(key),
-                "peak_source": f"bf16 dense burst, {peaks['source']}",
-                "frac_of_spec_2250": achieved / 2250.0,
-                "kernel": "bsattn_fwd_kernel", "ms_per_launch": ms_mean}
+        torch.cuda.synchronize()
+        pipe.status()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            pipe.run(hq, hk, hv, ho, hl, w.scale, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        pipe.status()
+        pipe.close()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, dev)
+        e2e = {"value": whole_job_tflops(flop, world, e2e_ms), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+               "pieces": pieces}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, nrows, dt = oracle_sample_rate(w, qb, kb, vb, mask, args.cpu_seconds)
+        if fp8:  # the oracle on the decoded inputs (the same fp64 work)
+            import oracle
+            bits = tuple(np.ascontiguousarray(oracle.decode_e4m3(b)) for b in bits)
+        rate, nrows, dt = oracle_sample_rate(w, *bits, mask, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                "sample": f"{nrows} random query rows of workload {w.id} ({dt:.1f} s, fp64)"}
 
@@ -366,20 +536,27 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+            "data": "synthetic",
             "config": {"workload": f"{w.id}:{w.name}", "shape": w.describe(),
                        "out_dtype": "f32" if args.out_f32 else "bf16",
+                       "key_block": args.key_block, "in_dtype": args.in_dtype,
                        "live_blocks": nlive, "flop_per_step": flop,
                        "l2": "flushed (512 MB write) before every timed step",
                        "parallelism": f"replicas x{world} (independent problems, no collective)"},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
-            "roofline": roofline,
+            "e2e": e2e,
+            "gpu_launches": head_launches,
+            "roofline": roofline(flop, nbytes, ms_mean, peaks,
+                                 measured_traffic(traffic_key(w.id), args.out_f32)),
             "cpu_baseline": cpu,
             "clocks": clk,
+            "clocks_note": "sampled from the start of this workload's per_config timing "
+                           "through the end of the headline steps",
             "wall_s_timed_region": wall,
             "pct_of_peak": 100.0 * value / world / peaks["bf16"],
+            "kernel_source_sha16": kernel_source_sha16(),
+            "per_config": per_config,
+            "gpu_launches_all_timed_regions": launches,
         }
         print(json.dumps(line), flush=True)
     plan.close()

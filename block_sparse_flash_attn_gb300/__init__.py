@@ -29,13 +29,14 @@ BLOCK = 128
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_OOM, ERR_TIMEOUT, ERR_INTERNAL = range(7)
 ERR_SCRATCH_LIMIT = 7
 ERR_RANGE = 8
-CAUSAL, OUT_F32, MASK_SHARED_HEADS = 1, 2, 4
+CAUSAL, OUT_F32, MASK_SHARED_HEADS, KEY_BLOCK_64 = 1, 2, 4, 8
 
 EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd",
            "bsattn_plan_status", "bsattn_plan_free", "bsattn_status_string", "bsattn_version",
            "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
            "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free",
-           "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa", "bsattn_bwd_gqa"]
+           "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa", "bsattn_bwd_gqa",
+           "bsattn_fwd_fp8"]
 
 
 class BsattnError(RuntimeError):
@@ -48,7 +49,9 @@ _lib = None
 
 
 def lib_path() -> str:
-    return _build.LIB
+    """The library this process loads: _build.LIB, or the build named by the
+    BSATTN_LIBRARY environment variable (the tuner's per-setting builds)."""
+    return os.environ.get("BSATTN_LIBRARY") or _build.LIB
 
 
 def load():
@@ -56,10 +59,11 @@ def load():
     global _lib
     if _lib is not None:
         return _lib
-    if not os.path.exists(_build.LIB):
-        raise RuntimeError(f"{_build.LIB} is not built; run block_sparse_flash_attn_gb300._build.build()"
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built; run block_sparse_flash_attn_gb300._build.build()"
                            " (or __graft_entry__.build()) first -- there is no fallback path")
-    lib = ctypes.CDLL(_build.LIB)
+    lib = ctypes.CDLL(path)
     vp, i32, i64, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint
     lib.bsattn_plan.argtypes = [vp, i32, i32, i32, u32, vp, ctypes.POINTER(vp)]
     lib.bsattn_plan.restype = i32
@@ -73,6 +77,9 @@ def load():
     lib.bsattn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
                                    vp]
     lib.bsattn_fwd_gqa.restype = i32
+    lib.bsattn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, ctypes.c_float,
+                                   ctypes.c_float, vp]
+    lib.bsattn_fwd_fp8.restype = i32
     lib.bsattn_plan_csc.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)]
     lib.bsattn_plan_csc.restype = i32
     lib.bsattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
@@ -138,10 +145,12 @@ def _view_i32(ptr, n: int) -> torch.Tensor:
 class Plan:
     """Handle to a device-side plan (CSR of live key blocks + tile schedule)."""
 
-    def __init__(self, handle: int, B: int, H: int, S: int, causal: bool, out_f32: bool):
+    def __init__(self, handle: int, B: int, H: int, S: int, causal: bool, out_f32: bool,
+                 key_block: int = BLOCK):
         self._h = ctypes.c_void_p(handle)
         self.B, self.H, self.S = B, H, S
         self.causal, self.out_f32 = causal, out_f32
+        self.key_block = key_block
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -162,18 +171,24 @@ class Plan:
 
 
 def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream=None,
-         heads: int | None = None) -> Plan:
+         heads: int | None = None, key_block: int = BLOCK) -> Plan:
     """Build the plan for a uint8 block mask [B, H, S/128, S/128] on the GPU.
 
     With heads=H and a mask of shape [B, 1, S/128, S/128], the one mask of
-    each batch entry applies to all its H heads."""
+    each batch entry applies to all its H heads.  With key_block=64 the mask
+    is [B, H, S/128, S/64]: one entry per 128-query x 64-key block (forward
+    pass only)."""
     if not (isinstance(mask, torch.Tensor) and mask.is_cuda and mask.dtype == torch.uint8):
         raise TypeError("mask must be a CUDA uint8 tensor")
-    if mask.dim() != 4 or mask.shape[2] != mask.shape[3]:
-        raise ValueError("mask must be [B, H, nb, nb]")
+    if key_block not in (BLOCK, 64):
+        raise ValueError("key_block must be 128 or 64")
+    kdiv = BLOCK // key_block
+    if mask.dim() != 4 or mask.shape[3] != kdiv * mask.shape[2]:
+        raise ValueError(f"mask must be [B, H, nb, {kdiv} * nb]")
     mask = mask.contiguous()
     B, H, nb, _ = mask.shape
-    flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0)
+    flags = (CAUSAL if causal else 0) | (OUT_F32 if out_f32 else 0) | \
+        (KEY_BLOCK_64 if key_block == 64 else 0)
     if heads is not None and heads != H:
         if H != 1:
             raise ValueError("a mask shared by the heads must have shape [B, 1, nb, nb]")
@@ -183,7 +198,7 @@ def plan(mask: torch.Tensor, causal: bool = False, out_f32: bool = False, stream
     with torch.cuda.device(mask.device):
         _check(load().bsattn_plan(ctypes.c_void_p(mask.data_ptr()), B, H, nb * BLOCK, flags,
                                   _stream_handle(stream), ctypes.byref(h)), "bsattn_plan")
-    return Plan(h.value, B, H, nb * BLOCK, causal, out_f32)
+    return Plan(h.value, B, H, nb * BLOCK, causal, out_f32, key_block)
 
 
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float | None = None,
@@ -222,6 +237,42 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, p: Plan, scale: float
                                          p.handle, vp(out.data_ptr()), vp(lse.data_ptr()), B, H,
                                          Hkv, S, D, float(scale), _stream_handle(stream)),
                    "bsattn_fwd_gqa")
+    return out, lse
+
+
+def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, v8: torch.Tensor, p: Plan,
+            scale: float | None = None, v_scale: float = 1.0, out: torch.Tensor | None = None,
+            lse: torch.Tensor | None = None, stream=None):
+    """O, LSE of block-sparse attention on e4m3 inputs: q8, k8, v8 CUDA
+    [B, H, S, 128] of torch.float8_e4m3fn (or uint8 holding e4m3 bits),
+    contiguous.  scale multiplies q.k (include the Q and K scales in it);
+    v_scale multiplies O."""
+    for t in (q8, k8, v8):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or \
+                t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+            raise TypeError("q8, k8, v8 must be CUDA float8_e4m3fn (or uint8) tensors")
+        if not t.is_contiguous():
+            raise ValueError("q8, k8, v8 must be contiguous")
+    if q8.dim() != 4 or k8.shape != q8.shape or v8.shape != q8.shape:
+        raise ValueError("q8, k8, v8 must share one shape [B, H, S, D]")
+    B, H, S, D = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    odt = torch.float32 if p.out_f32 else torch.bfloat16
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=odt, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
+    if out.dtype != odt or out.shape != (B, H, S, D) or not out.is_contiguous():
+        raise ValueError("out has the wrong dtype/shape/layout for this plan")
+    if lse.dtype != torch.float32 or lse.shape != (B, H, S) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [B, H, S]")
+    vp = ctypes.c_void_p
+    with torch.cuda.device(q8.device):
+        _check(load().bsattn_fwd_fp8(vp(q8.data_ptr()), vp(k8.data_ptr()), vp(v8.data_ptr()),
+                                     p.handle, vp(out.data_ptr()), vp(lse.data_ptr()), B, H, S, D,
+                                     float(scale), float(v_scale), _stream_handle(stream)),
+               "bsattn_fwd_fp8")
     return out, lse
 
 

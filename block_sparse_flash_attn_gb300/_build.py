@@ -30,21 +30,26 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(_CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(_INC, "bsattn.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile and link libbsattn.so if any source is newer than it."""
-    if not force and not _stale():
-        return LIB
-    os.makedirs(LIBDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out: str | None = None) -> str:
+    """Compile and link libbsattn.so if any source is newer than it.
+
+    extra_flags: more nvcc flags (the tuner's -D settings of the kernels'
+    build-time parameters); out: the library path (default LIB; the tuner
+    builds each setting into its own file under LIBDIR/variants)."""
+    lib = out or LIB
+    if not force and not _stale(lib):
+        return lib
+    os.makedirs(os.path.dirname(lib), exist_ok=True)
     nvcc = _nvcc()
-    objdir = os.path.join(LIBDIR, f"obj{os.getpid()}")
+    objdir = os.path.join(os.path.dirname(lib), f"obj{os.getpid()}")
     os.makedirs(objdir, exist_ok=True)
     common = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-I", _INC, "-I", _CSRC, *extra_flags]
@@ -63,13 +68,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     shutil.rmtree(objdir, ignore_errors=True)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -17,6 +17,7 @@ using namespace bsattn;
 struct bsattn_plan_s {
   uint32_t magic = 0;
   int B = 0, H = 0, S = 0, nb = 0;
+  int kdiv = 1;  // key blocks of 128 / kdiv keys (BSATTN_KEY_BLOCK_64: 2)
   unsigned flags = 0;
   int device = 0;
   int64_t nnz = 0, n_live = 0, n_empty = 0;
@@ -67,14 +68,32 @@ void set_scale_params(FwdParams& p, float scale) {
   p.neg_scale = scale < 0.0f ? 1 : 0;
 }
 
-// 2-D view (rows = B*H*S, cols = D) of a bf16 tensor; box 64 columns x 128
-// rows (one 128-byte swizzle span), 128B swizzle.
-bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows) {
+// 2-D view (rows = B*H*S, cols = D) of a bf16 tensor; box 64 columns x
+// box_rows rows (128, or 64 for the halves of a tile of 64-key blocks; one
+// 128-byte swizzle span per row), 128B swizzle.
+bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows,
+                              int box_rows) {
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kBlock};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? BSATTN_OK : BSATTN_ERR_CUDA;
+}
+
+// 2-D view (rows = B*H*S, cols = D bytes) of an e4m3 tensor (uint8 elements);
+// box D = 128 bytes x box_rows rows, 128B swizzle: the same 128-byte rows and
+// swizzle as one 64-column box of a bf16 tile.
+bsattn_status encode_e4m3_map(CUtensorMap* m, const void* ptr, int D, long long rows,
+                              int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D};
+  cuuint32_t box[2] = {(cuuint32_t)D, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -105,14 +124,15 @@ namespace bsattn {
 
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf, int Hkv) {
+                          PreparedFwd* pf, int Hkv, bool in8, float v_scale) {
   if (!plan_ok(plan) || !pf) return BSATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
     return BSATTN_ERR_INVALID_ARG;
   if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
-  if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
+  if (in8 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !std::isfinite(v_scale)) return BSATTN_ERR_INVALID_ARG;
   if (Hkv <= 0 || H % Hkv != 0) return BSATTN_ERR_INVALID_ARG;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != plan->device) return BSATTN_ERR_INVALID_ARG;
@@ -121,9 +141,12 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   const long long rows = (long long)B * H * S;
   const long long kv_rows = (long long)B * Hkv * S;
   bsattn_status rc;
-  if ((rc = encode_bf16_map(&pf->tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&pf->tk, k, D, kv_rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&pf->tv, v, D, kv_rows)) != BSATTN_OK) return rc;
+  // K and V come in halves of 64 rows when the plan's key blocks have 64 keys
+  const int kv_box = kBlock / plan->kdiv;
+  auto encode = in8 ? encode_e4m3_map : encode_bf16_map;
+  if ((rc = encode(&pf->tq, q, D, rows, kBlock)) != BSATTN_OK) return rc;
+  if ((rc = encode(&pf->tk, k, D, kv_rows, kv_box)) != BSATTN_OK) return rc;
+  if ((rc = encode(&pf->tv, v, D, kv_rows, kv_box)) != BSATTN_OK) return rc;
 
   FwdParams& prm = pf->prm;
   prm = FwdParams{};
@@ -145,14 +168,17 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   prm.timeout_ns = kDefaultWaitTimeoutNs;
   prm.H = H;
   prm.kv_group = H / Hkv;
+  prm.kdiv = plan->kdiv;
+  prm.v_scale = v_scale;
   pf->D = D;
+  pf->in8 = in8;
   pf->out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
   pf->grid = device_sm_count(dev);
   return BSATTN_OK;
 }
 
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream) {
-  return launch_fwd(pf.D, pf.out_f32, pf.tq, pf.tk, pf.tv, pf.prm, pf.grid, stream);
+  return launch_fwd(pf.D, pf.out_f32, pf.tq, pf.tk, pf.tv, pf.prm, pf.grid, stream, pf.in8);
 }
 
 }  // namespace bsattn
@@ -171,6 +197,7 @@ const char* bsattn_status_string(bsattn_status s) {
     case BSATTN_ERR_TIMEOUT: return "device wait timed out";
     case BSATTN_ERR_INTERNAL: return "internal error detected on device";
     case BSATTN_ERR_SCRATCH_LIMIT: return "problem exceeds the no-allocation scratch size";
+    case BSATTN_ERR_RANGE: return "input value out of the supported range (D = 64: |V| <= 65504)";
   }
   return "unknown status";
 }
@@ -179,7 +206,8 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
                           void* stream, bsattn_plan_t* out_plan) {
   if (!d_mask || !out_plan) return BSATTN_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || S <= 0 || (S % kBlock) != 0) return BSATTN_ERR_INVALID_ARG;
-  if (flags & ~(unsigned)(BSATTN_CAUSAL | BSATTN_OUT_F32 | BSATTN_MASK_SHARED_HEADS))
+  if (flags & ~(unsigned)(BSATTN_CAUSAL | BSATTN_OUT_F32 | BSATTN_MASK_SHARED_HEADS |
+                          BSATTN_KEY_BLOCK_64))
     return BSATTN_ERR_INVALID_ARG;
   const int nb = S / kBlock;
   if (nb > kMaxBlocksPerRow) return BSATTN_ERR_UNSUPPORTED;
@@ -195,9 +223,11 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
   p->S = S;
   p->nb = nb;
   p->flags = flags;
+  p->kdiv = (flags & BSATTN_KEY_BLOCK_64) ? 2 : 1;
   cudaGetDevice(&p->device);
   const int causal = (flags & BSATTN_CAUSAL) ? 1 : 0;
   const int mdiv = (flags & BSATTN_MASK_SHARED_HEADS) ? H : 1;  // mask heads: H or 1
+  const int kdiv = p->kdiv;
 
   int* tmp = nullptr;  // counts[rows] | live_per_head[BH] | live_off[BH+1] | totals (2 x int64)
   const size_t tmp_ints = (size_t)rows + BH + (BH + 1) + 1 + 4;
@@ -223,7 +253,7 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
   if ((e = cudaMemsetAsync(p->dev.work, 0, sizeof(int) * kWorkWords, st)) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = plan_count_and_scan(d_mask, BH, nb, causal, d_counts, p->dev.row_ptr, d_live_off,
-                               d_totals, st, mdiv)) != cudaSuccess)
+                               d_totals, st, mdiv, kdiv)) != cudaSuccess)
     return fail(from_cuda(e));
   if ((e = cudaMemcpyAsync(h_tot, d_totals, sizeof(h_tot), cudaMemcpyDeviceToHost, st)) !=
       cudaSuccess)
@@ -245,20 +275,23 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
     return fail(from_cuda(e));
   if ((e = plan_fill_and_order(d_mask, BH, nb, causal, p->dev.row_ptr, d_live_off,
                                p->dev.col_idx, p->dev.tile_order, p->dev.empty_tiles,
-                               device_sm_count(p->device), st, mdiv)) != cudaSuccess)
+                               device_sm_count(p->device), st, mdiv, kdiv)) != cudaSuccess)
     return fail(from_cuda(e));
   // Transposed plan for the backward pass (same number of live blocks) and
-  // its per-row scratch; d_counts is free again once the CSR is built.
-  if ((e = cudaMalloc(&p->dev.col_ptr, sizeof(int) * ((size_t)rows + 1))) != cudaSuccess)
-    return fail(from_cuda(e));
-  if ((e = cudaMalloc(&p->dev.row_idx, sizeof(int) * (size_t)(p->nnz > 0 ? p->nnz : 1))) !=
-      cudaSuccess)
-    return fail(from_cuda(e));
-  if ((e = cudaMalloc(&p->dev.dl, sizeof(float) * (size_t)B * H * S)) != cudaSuccess)
-    return fail(from_cuda(e));
-  if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st,
-                    mdiv)) != cudaSuccess)
-    return fail(from_cuda(e));
+  // its per-row scratch; d_counts is free again once the CSR is built.  The
+  // backward pass takes 128-key blocks only, so plans of 64-key blocks have none.
+  if (kdiv == 1) {
+    if ((e = cudaMalloc(&p->dev.col_ptr, sizeof(int) * ((size_t)rows + 1))) != cudaSuccess)
+      return fail(from_cuda(e));
+    if ((e = cudaMalloc(&p->dev.row_idx, sizeof(int) * (size_t)(p->nnz > 0 ? p->nnz : 1))) !=
+        cudaSuccess)
+      return fail(from_cuda(e));
+    if ((e = cudaMalloc(&p->dev.dl, sizeof(float) * (size_t)B * H * S)) != cudaSuccess)
+      return fail(from_cuda(e));
+    if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st,
+                      mdiv)) != cudaSuccess)
+      return fail(from_cuda(e));
+  }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
   cudaFree(tmp);
   tmp = nullptr;
@@ -279,6 +312,7 @@ bsattn_status bsattn_plan_csr(bsattn_plan_t plan, const int32_t** d_row_ptr,
 bsattn_status bsattn_plan_csc(bsattn_plan_t plan, const int32_t** d_col_ptr,
                               const int32_t** d_row_idx, int64_t* nnz) {
   if (!plan_ok(plan) || !d_col_ptr || !d_row_idx || !nnz) return BSATTN_ERR_INVALID_ARG;
+  if (plan->kdiv != 1) return BSATTN_ERR_UNSUPPORTED;  // no transposed list for 64-key blocks
   *d_col_ptr = plan->dev.col_ptr;
   *d_row_idx = plan->dev.row_idx;
   *nnz = plan->nnz;
@@ -315,6 +349,16 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }
 
+bsattn_status bsattn_fwd_fp8(const void* q8, const void* k8, const void* v8, bsattn_plan_t plan,
+                             void* out, float* lse, int B, int H, int S, int D, float scale,
+                             float v_scale, void* stream) {
+  PreparedFwd pf;
+  const bsattn_status rc =
+      prepare_fwd(q8, k8, v8, plan, out, lse, B, H, S, D, scale, &pf, H, true, v_scale);
+  if (rc != BSATTN_OK) return rc;
+  return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
+}
+
 bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                              const float* lse, const void* dout, bsattn_plan_t plan, float* dq,
                              float* dk, float* dv, int B, int H, int Hkv, int S, int D,
@@ -326,6 +370,7 @@ bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const 
     return BSATTN_ERR_INVALID_ARG;
   if (B != plan->B || H != plan->H || S != plan->S) return BSATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return BSATTN_ERR_UNSUPPORTED;
+  if (plan->kdiv != 1) return BSATTN_ERR_UNSUPPORTED;  // gradients over 128-key blocks only
   if (!std::isfinite(scale)) return BSATTN_ERR_INVALID_ARG;
   if (Hkv <= 0 || H % Hkv != 0) return BSATTN_ERR_INVALID_ARG;
   if (H / Hkv > 64) return BSATTN_ERR_UNSUPPORTED;  // query heads per K/V head walked by one CTA
@@ -388,6 +433,7 @@ bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream) {
   const int s = words[kWorkStatus];
   if (s & kStatusInternal) return BSATTN_ERR_INTERNAL;
   if (s & kStatusTimeout) return BSATTN_ERR_TIMEOUT;
+  if (s & kStatusRange) return BSATTN_ERR_RANGE;
   return BSATTN_OK;
 }
 

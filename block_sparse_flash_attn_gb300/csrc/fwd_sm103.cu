@@ -37,25 +37,37 @@
 // into block g's buffer once O += P(g) V(g) is complete, so the scores of
 // the next blocks are computed while the softmax works on block g: the chain
 // softmax -> PV -> next S spans three blocks and hides behind the tensor
-// core's own work.  Shared memory: Q buffers and 3-stage rings of K and V
-// tiles (128 x D bf16 each, 128-byte swizzled by TMA, read by tcgen05.mma
-// through matrix descriptors): at D = 128 one Q (224 KB), at D = 64 two.
+// core's own work.  Shared memory: Q buffers and rings of K and V tiles
+// (128 x D each, 128-byte swizzled by TMA, read by tcgen05.mma through matrix
+// descriptors); see Cfg for the depths of each configuration.
+//
+// Precision: S = Q K^T in bf16 (e4m3 with FP8 inputs) with fp32 accumulation;
+// P V in bf16 at D = 128, in fp16 at D = 64 and with FP8 inputs (the four
+// epilogue warps convert each V tile to fp16 in shared memory: bf16 -> fp16
+// in place, e4m3 -> fp16 from a staging ring), so that the rounding of P, the
+// largest error term, is 2^-11 instead of 2^-8 where the logits are wide.
 //
 // The producer sees the CTA's tiles as one stream of key blocks and loads K
 // two blocks ahead of V along it; the scheduler warp loads each tile's Q as
-// soon as the Q buffer is free.  Along the same stream one MMA warp issues
-// S(g) as soon as K(g) is loaded and PV(g-3) is complete, another issues
-// PV(g) as soon as P(g) is written and V(g) loaded; a tile's first PV starts
-// a fresh O.  The commit after S(g) frees K(g)'s ring stage and is the
-// softmax's "S(g) ready" signal; the commit after PV(g) frees V(g)'s stage
-// and is "PV(g) done", which the softmax waits for only before an O rescale
-// and the epilogue warps for a tile's last block.  The next tile's first PV,
-// the one that overwrites O, waits until the epilogue warps have read O.
+// soon as the Q buffer is free.  With 64-key blocks (kdiv = 2) a block of the
+// stream is a pair of consecutive entries of the tile's list, loaded as the
+// two 64-row halves of one stage (an odd tail repeats its one entry and the
+// softmax masks the copy).  Along the stream one MMA warp issues S(g) as soon
+// as K(g) is loaded and PV(g-3) is complete, another issues PV(g) as soon as
+// P(g) is written and V(g) loaded (and converted); a tile's first PV starts a
+// fresh O.  The commit after S(g) frees K(g)'s ring stage and signals "S(g)
+// ready" (s_full); the commit after PV(g) frees V(g)'s stage and signals
+// "PV(g) done" (pv_done), which the S issuer waits for before reusing a score
+// buffer, the softmax before an O rescale and the epilogue warps for a
+// tile's last block.  The next tile's first PV, the one that overwrites O,
+// waits until the epilogue warps have read O.
 // Online softmax in base 2 with lazy rescale: the running max m only moves
 // when a block's max exceeds it by more than 8 (log2 units), so P <= 256 and
-// the O rescale is rare.  O is normalised by the row sum of the bf16-rounded
-// P that multiplied V (so the weights on V sum to one even when a single key
-// dominates a row); the LSE uses the fp32 sum of the unrounded P.
+// the O rescale is rare.  O is normalised by the row sum of the rounded P
+// that multiplied V (so the weights on V sum to one even when a single key
+// dominates a row); the LSE uses the fp32 sum of the unrounded P.  A row with
+// no allowed key (possible inside a live tile only with 64-key blocks under
+// causal) gets O = 0 and LSE = -inf.
 //
 // Every wait is bounded (globaltimer); on expiry the kernel records a timeout
 // in the status word, every role leaves its loop, outstanding TMA loads and
@@ -87,15 +99,15 @@ constexpr uint32_t kSleepNs = 200;
 // The producer asks for the next tile when its K cursor has this many blocks
 // of the current tile left: claiming a tile (four dependent global reads)
 // and loading its Q take about as long as this many blocks' MMAs.
-constexpr int kClaimAhead = 4;
+#ifndef BSATTN_CLAIM_AHEAD
+#define BSATTN_CLAIM_AHEAD 4
+#endif
+constexpr int kClaimAhead = BSATTN_CLAIM_AHEAD;
 // Launch budget 512 x 128 registers; the two role warpgroups hand part of
 // their share to the two softmax warpgroups: 256 x 208 + 256 x 48 = 512 x 128.
 constexpr int kRegsSoftmax = 208;
 constexpr int kRegsOther = 48;
 constexpr float kTau = 8.0f;
-// A row whose probabilities, formed against a stale reference, sum to more
-// than this over one block is redone with the block's max as reference.
-constexpr float kGrowSum = 4294967296.0f;  // 2^32
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: three score buffers S[0..2] (128 each; the bf16 P
 // of a block overwrites its scores) and the output accumulator O (D).
@@ -108,23 +120,47 @@ static_assert(kTmemS + kSBufs * 128 <= kTmemO && kTmemO + 128 <= kTmemCols &&
 constexpr unsigned long long kDrainNs = 200ull * 1000 * 1000;
 constexpr int kMaxDevices = 64;
 
-template <int D>
+#ifndef BSATTN_D128_QSTAGES
+#define BSATTN_D128_QSTAGES 1
+#endif
+#ifndef BSATTN_D128_KSTAGES
+#define BSATTN_D128_KSTAGES 3
+#endif
+#ifndef BSATTN_D128_VSTAGES
+#define BSATTN_D128_VSTAGES 3
+#endif
+
+// IN8: Q, K, V are e4m3 (FP8), at D = 128 only.  Q and K tiles are then 16 KB
+// (one 128-byte row per key or query), S = Q K^T runs as kind::f8f6f4 MMAs
+// (K = 32 per instruction), and each e4m3 V tile lands in its own staging
+// ring, from which the epilogue warps convert it to the fp16 V tile that the
+// P V product reads (P in fp16 as well).
+template <int D, bool IN8 = false>
 struct Cfg {
-  static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
-  static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
+  static_assert(!IN8 || D == 128, "e4m3 inputs at head_dim 128 only");
+  static constexpr bool kIn8 = IN8;
+  static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 / fp16 tile (V for P V)
+  static constexpr int kBoxes = D / 64;              // 64-column (128-byte) boxes of such a tile
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
-  // Ring depths and Q buffers: D = 128 fills 224 KB with one Q tile and
-  // three stages of each ring; D = 64 has two Q tiles and three stages.
-  static constexpr int kKStages = 3;
-  static constexpr int kVStages = 3;
-  static constexpr int kQStages = D == 128 ? 1 : 2;
+  // Q and K tiles as loaded: bf16 (kBoxes boxes), or e4m3 (one 128-byte box)
+  static constexpr int kQKBytes = IN8 ? kBlock * D : kTileBytes;
+  static constexpr int kQKBoxes = IN8 ? 1 : kBoxes;
+  // Ring depths and Q buffers: at D = 128 seven 32 KB tiles fill 224 KB
+  // (Q buffers + K stages + V stages = 7); D = 64 has two Q tiles and three
+  // stages of each ring; e4m3 has two 16 KB Q tiles, three 16 KB K stages,
+  // three 16 KB e4m3 V stages and three 32 KB fp16 V stages (224 KB).
+  static constexpr int kKStages = IN8 ? 3 : D == 128 ? BSATTN_D128_KSTAGES : 3;
+  static constexpr int kVStages = IN8 ? 3 : D == 128 ? BSATTN_D128_VSTAGES : 3;
+  static constexpr int kQStages = IN8 ? 2 : D == 128 ? BSATTN_D128_QSTAGES : 2;
+  static constexpr int kV8Stages = IN8 ? 3 : 0;  // e4m3 V staging ring
   static constexpr int kQOff = 0;
-  static constexpr int kKOff = kQStages * kTileBytes;
+  static constexpr int kKOff = kQStages * kQKBytes;
+  static constexpr int kV8Off = kKOff + kKStages * kQKBytes;
   // V region: the PV MMA's B operand (MN-major) has its 64-wide column
   // groups kVGroup bytes apart: group c of stage s sits at
   // kVOff + c * kVGroup + s * kBoxBytes.
   static constexpr int kVGroup = kVStages * kBoxBytes;
-  static constexpr int kVOff = kKOff + kKStages * kTileBytes;
+  static constexpr int kVOff = kV8Off + kV8Stages * kBoxBytes;
   // Row sum of the rounded P (the O denominator): at D = 64 the tensor core
   // accumulates it next to O, the PV MMA multiplying P by [V | ones] (N =
   // D + 16; the ones tile of each V stage sits one column group after the
@@ -132,11 +168,23 @@ struct Cfg {
   // memory columns are not free, and the softmax threads add it up.
   static constexpr bool kOnes = D == 64;
   static constexpr int kPvN = kOnes ? D + 16 : D;
+  // P V in fp16 (P and V rounded to 11 significant bits instead of bf16's 8):
+  // at D = 64 the epilogue warps convert each V tile in shared memory after
+  // its load; with e4m3 inputs they convert it into the fp16 ring; at
+  // D = 128 with bf16 inputs P V stays in bf16.
+  static constexpr bool kF16PV = D == 64 || IN8;
+  // A row's block sum above this (formed against a stale reference) makes the
+  // softmax redo the block with its max; in fp16 it also keeps every P below
+  // fp16's largest finite value: each P <= the sum <= 2^15.
+  static constexpr float kGrowSum = kF16PV ? 32768.0f : 4294967296.0f;
   static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;
   static constexpr int kBarOff = kOnesOff + (kOnes ? kVStages * kBoxBytes : 0);
   static constexpr int kSmem = kBarOff + 2048;  // barriers, tile queue, 1/l
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
-  static constexpr uint32_t kIdescO = idesc_bf16_f32(128, kPvN, true);
+  // S = Q K^T: bf16 (kind::f16, K = 16 per MMA) or e4m3 (kind::f8f6f4, K =
+  // 32 per MMA; e4m3 has the same format code, 0, there as f16 has in kind::f16)
+  static constexpr int kSMmas = IN8 ? 4 : D / 16;
+  static constexpr uint32_t kIdescS = idesc_f16kind_f32(128, 128, false, false, IN8);
+  static constexpr uint32_t kIdescO = idesc_f16kind_f32(128, kPvN, true, false, kF16PV);
 };
 
 constexpr int kSlotCols = 32;  // key blocks of a tile published with it
@@ -147,16 +195,21 @@ constexpr int kMaxStages = 3;  // deepest K / V ring of any Cfg
 struct TileInfo {
   int t;     // tile id (b*H + h)*nb + qb, or -1 when no tiles are left
   int r0;    // first CSR entry of the tile
-  int n;     // live key blocks
-  int diag;  // causal and the last live block is the diagonal one
-  int cols[kSlotCols];  // its first min(n, 32) key blocks (CSR col_idx[r0 ..])
+  int n;     // blocks of the stream: live key blocks (64-key blocks: their pairs)
+  int diag;  // causal and the last live block is the diagonal one (128-key blocks)
+  int n64;   // CSR entries of the tile (= n for 128-key blocks)
+  int last2[2];  // 64-key blocks: the key blocks of entries n64-2 and n64-1 (-1: none)
+  int cols[kSlotCols];  // its first min(n64, 32) CSR entries (col_idx[r0 ..])
 };
 
 struct __align__(16) Bars {
   uint64_t k_full[kMaxStages];   // K ring stage loaded
-  uint64_t k_empty[kMaxStages];  // S(g) complete: K stage free, S(g) ready for the softmax
+  uint64_t k_empty[kMaxStages];  // S(g) complete: K stage free
   uint64_t v_full[kMaxStages];   // V ring stage loaded
   uint64_t v_empty[kMaxStages];  // PV(g) complete: V stage free, O holds block g
+  uint64_t v_conv[kMaxStages];   // fp16 P V: the four epilogue warps converted V(g) to fp16
+  uint64_t v8_full[kMaxStages];  // e4m3 inputs: V(g) staged (TMA)
+  uint64_t v8_empty[kMaxStages]; // e4m3 inputs: V(g) converted, the staging stage is free
   uint64_t q_full[2];
   uint64_t q_empty[2];  // the tile's last S complete: Q buffer free
   // every softmax warp wrote its rows of P(g), indexed by g % kSBufs: the
@@ -164,6 +217,15 @@ struct __align__(16) Bars {
   // kSBufs) needs S(g + kSBufs), i.e. PV(g) complete, so a barrier never
   // completes a phase for a later block before its waiter saw the earlier one
   uint64_t p_full[kSBufs];
+  // S(g) complete (the softmax may read it) and PV(g) complete (S buffer g %
+  // kSBufs may take S(g + kSBufs)), indexed by g % kSBufs: a phase of these can
+  // only complete once the waiter is done with the previous one (S(g + 3)
+  // needs PV(g), which needs P(g) from the softmax; PV(g + 3) needs S(g + 3),
+  // which the S issuer has not issued while it waits for PV(g)), so their
+  // parity waits never alias, whatever the ring depths; a wait on a ring
+  // stage's own barrier could, when that ring is shallower than kSBufs.
+  uint64_t s_full[kSBufs];
+  uint64_t pv_done[kSBufs];
   uint64_t tq_full[2];  // tile queue slot published
   uint64_t tq_empty[2]; // slot read by the producer, both MMA warps, every softmax warp, epilogue leader
   uint64_t drain;       // all MMAs of both issuers complete (one commit from each)
@@ -174,13 +236,17 @@ struct __align__(16) Bars {
   uint32_t tmem_base;
   int abort_flag;
   int epi_tile[2];       // tile the epilogue warps write next (by tile parity); < 0: stop
+  int epi_n[2];          // and its live key blocks
   float inv_l[kBlock];  // D = 128: 1 / (rounded row sum) of the tile being written out
 };
 static_assert(sizeof(Bars) <= 2048, "barrier block must fit its 2 KB region");
 static_assert(Cfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(Cfg<64>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
+static_assert(Cfg<128, true>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(Cfg<128>::kKStages <= kMaxStages && Cfg<64>::kKStages <= kMaxStages &&
-                  Cfg<128>::kVStages <= kMaxStages && Cfg<64>::kVStages <= kMaxStages,
+                  Cfg<128>::kVStages <= kMaxStages && Cfg<64>::kVStages <= kMaxStages &&
+                  Cfg<128, true>::kKStages <= kMaxStages &&
+                  Cfg<128, true>::kV8Stages <= kMaxStages,
               "ring depth");
 
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
@@ -226,10 +292,10 @@ __device__ __forceinline__ bool wait_warp_idle(uint32_t bar, uint32_t parity,
 // reads (counter, tile order, CSR row pointers, column indices) and the Q
 // load are thus off the producer's and the MMA warp's path.  Ends after
 // publishing the "no tiles left" entry.
-template <int D>
+template <int D, bool IN8>
 __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars* bars,
                               uint32_t smem_base, volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.timeout_ns;
   const int rows = p.n_live + p.n_empty;
@@ -252,7 +318,7 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
     if (lane == 0) idx = atomicAdd(p.counter, 1);
     idx = __shfl_sync(0xffffffffu, idx, 0);
     const int t = idx < p.n_live ? p.tile_order[idx] : -1;
-    int r0 = 0, cnt = 0, diag = 0;
+    int r0 = 0, cnt = 0, diag = 0, l0 = -1, l1 = -1;
     if (t >= 0) {
       if (t >= rows) {
         raise_internal(abort_flag, p.status);
@@ -261,20 +327,28 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
       }
       r0 = p.row_ptr[t];
       cnt = p.row_ptr[t + 1] - r0;
-      if (cnt <= 0 || cnt > p.nb) {
+      if (cnt <= 0 || cnt > p.nb * p.kdiv) {
         raise_internal(abort_flag, p.status);
         ok = false;
         break;
       }
-      diag = (p.causal && p.col_idx[r0 + cnt - 1] == t % p.nb) ? 1 : 0;
-      if (lane < cnt) bars->tq[e].cols[lane] = p.col_idx[r0 + lane];
+      if (p.kdiv == 1) {
+        diag = (p.causal && p.col_idx[r0 + cnt - 1] == t % p.nb) ? 1 : 0;
+      } else {
+        l0 = cnt >= 2 ? p.col_idx[r0 + cnt - 2] : -1;
+        l1 = p.col_idx[r0 + cnt - 1];
+      }
+      if (lane < cnt && lane < kSlotCols) bars->tq[e].cols[lane] = p.col_idx[r0 + lane];
     }
     if (lane == 0) {
       volatile TileInfo* slot = &bars->tq[e];
       slot->t = t;
       slot->r0 = r0;
-      slot->n = cnt;
+      slot->n = p.kdiv == 1 ? cnt : (cnt + 1) / 2;
       slot->diag = diag;
+      slot->n64 = cnt;
+      slot->last2[0] = l0;
+      slot->last2[1] = l1;
     }
     __syncwarp();  // every lane's writes to the slot precede the arrive
     if (lane == 0) mbar_arrive(smem_u32(&bars->tq_full[e]));
@@ -292,10 +366,10 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
       const int bh = t / p.nb;
       const int row = bh * p.S + (t - bh * p.nb) * kBlock;
       const uint32_t full = smem_u32(&bars->q_full[qs]);
-      const uint32_t dst = smem_base + C::kQOff + qs * C::kTileBytes;
-      mbar_arrive_expect_tx(full, C::kTileBytes);
+      const uint32_t dst = smem_base + C::kQOff + qs * C::kQKBytes;
+      mbar_arrive_expect_tx(full, C::kQKBytes);
 #pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c)
+      for (int c = 0; c < C::kQKBoxes; ++c)
         tma_load_2d(dst + c * C::kBoxBytes, tm_q, full, c * 64, row);
     }
     __syncwarp();
@@ -312,7 +386,7 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
 // it read.  Returns false when the wait failed.
 __device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& p,
                                           volatile int* abort_flag, int& t, int& r0, int& n,
-                                          int& col, uint32_t sleep_ns = 0) {
+                                          int& col, uint32_t sleep_ns = 0, int* n64 = nullptr) {
   const int lane = threadIdx.x & 31;
   const int e = tqc & 1;
   const uint32_t bar = smem_u32(&bars->tq_full[e]);
@@ -324,7 +398,9 @@ __device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& 
   t = slot->t;
   r0 = slot->r0;
   n = slot->n;
-  col = (t >= 0 && lane < n && lane < kSlotCols) ? slot->cols[lane] : 0;
+  const int ne = slot->n64;
+  if (n64) *n64 = ne;
+  col = (t >= 0 && lane < ne && lane < kSlotCols) ? slot->cols[lane] : 0;
   __syncwarp();
   if (lane == 0) mbar_arrive(smem_u32(&bars->tq_empty[e]));
   __syncwarp();
@@ -339,31 +415,41 @@ __device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& 
 // ring is loaded in its consumption order.  When the K cursor has
 // kClaimAhead blocks of its tile left (or enters a shorter tile) it asks the
 // scheduler for the next tile.
-template <int D>
+template <int D, bool IN8>
 __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, Bars* bars,
                              uint32_t smem_base, volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.timeout_ns;
   int kc = 0, vc = 0, tqc = 0;  // K / V tiles loaded, tiles taken
   bool ok = true, more = true;
   int k_ask = 0;  // K cursor's remaining-block count at which to ask for the next tile
-  // K cursor: position in its tile; `k_col` holds, in lane i, the key block
-  // of the tile's entry 32 * (k_j / 32) + i.
-  int k_rem = 0, k_j = 0, k_r0 = 0, k_hrow = 0, k_col = 0;
-  // key rows of blocks whose K is loaded and V not yet (at most two)
-  int f0 = 0, f1 = 0, nf = 0;
+  // K cursor: position in its tile (stream blocks); `k_col` holds, in lane i,
+  // the key block of the tile's CSR entry 32 * (e / 32) + i, e the cursor's
+  // first entry (64-key blocks: stream block j is entries 2j and 2j + 1).
+  int k_rem = 0, k_j = 0, k_r0 = 0, k_hrow = 0, k_col = 0, k_n64 = 0;
+  // key rows of blocks whose K is loaded and V not yet (at most two); with
+  // 64-key blocks, the rows of the block's two halves
+  int f0 = 0, f1 = 0, g0 = 0, g1 = 0, nf = 0;
+  const bool halves = p.kdiv == 2;
+  constexpr uint32_t kHalfBytes = 64 * 128;  // 64 rows of a 128-byte-row box
 
   // One TMA tile (128 rows x D) into a buffer, completion on `full`, after
-  // `empty` says the buffer's previous contents were consumed.
+  // `empty` says the buffer's previous contents were consumed; with 64-key
+  // blocks as two 64-row halves from rows `row` and `row2` (the tensor map's
+  // box is then 64 rows high).
+  // `nbox` boxes of 128-byte rows, `bytes` in all (bf16: D / 64 boxes; e4m3: one).
   auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t box_stride, uint32_t full,
-                       uint32_t empty, uint32_t empty_parity, int row) -> bool {
+                       uint32_t empty, uint32_t empty_parity, int row, int row2, int nbox,
+                       uint32_t bytes) -> bool {
     if (!wait_warp(empty, empty_parity, abort_flag, p.status, lim)) return false;
     if (elect_one()) {
-      mbar_arrive_expect_tx(full, C::kTileBytes);
-#pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * box_stride, tm, full, c * 64, row);
+      mbar_arrive_expect_tx(full, bytes);
+      for (int c = 0; c < nbox; ++c) {
+        tma_load_2d(dst + c * box_stride, tm, full, c * 64, row);
+        if (halves) tma_load_2d(dst + c * box_stride + kHalfBytes, tm, full, c * 64, row2);
+      }
     }
     __syncwarp();
     return true;
@@ -372,7 +458,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     if (k_rem == 0) {
       if (!more) return true;
       int t = 0;
-      if (!take_tile(bars, tqc, p, abort_flag, t, k_r0, k_rem, k_col)) return false;
+      if (!take_tile(bars, tqc, p, abort_flag, t, k_r0, k_rem, k_col, 0, &k_n64)) return false;
       ++tqc;
       if (t < 0) {
         more = false;
@@ -386,19 +472,29 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
       k_hrow = kvbh * p.S;
       k_j = 0;
       k_ask = k_rem - 1 < kClaimAhead ? k_rem - 1 : kClaimAhead;
-    } else if ((k_j & 31) == 0) {  // next 32 entries of the tile's CSR list
-      k_col = (lane < k_rem) ? p.col_idx[k_r0 + k_j + lane] : 0;
+    } else {
+      const int e = halves ? 2 * k_j : k_j;
+      if ((e & 31) == 0)  // next 32 entries of the tile's CSR list
+        k_col = (lane < k_n64 - e) ? p.col_idx[k_r0 + e + lane] : 0;
     }
-    const int kb = __shfl_sync(0xffffffffu, k_col, k_j & 31);
-    if (kb < 0 || kb >= p.nb) {
+    const int e = halves ? 2 * k_j : k_j;
+    const int kb = __shfl_sync(0xffffffffu, k_col, e & 31);
+    // the second half: the next entry, or (odd tail) the first half again,
+    // whose scores the softmax masks
+    int kb2 = kb;
+    if (halves && e + 1 < k_n64) kb2 = __shfl_sync(0xffffffffu, k_col, (e + 1) & 31);
+    const int nbk = p.nb * p.kdiv;
+    if (kb < 0 || kb >= nbk || kb2 < 0 || kb2 >= nbk) {
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int row = k_hrow + kb * kBlock;
+    const int krows = kBlock / p.kdiv;
+    const int row = k_hrow + kb * krows, row2 = k_hrow + kb2 * krows;
     const int st = kc % C::kKStages;
-    if (!load_tile(tm_k, smem_base + C::kKOff + st * C::kTileBytes, C::kBoxBytes,
+    if (!load_tile(tm_k, smem_base + C::kKOff + st * C::kQKBytes, C::kBoxBytes,
                    smem_u32(&bars->k_full[st]), smem_u32(&bars->k_empty[st]),
-                   ((uint32_t)(kc / C::kKStages) & 1u) ^ 1u, row))
+                   ((uint32_t)(kc / C::kKStages) & 1u) ^ 1u, row, row2, C::kQKBoxes,
+                   C::kQKBytes))
       return false;
     ++kc;
     ++k_j;
@@ -407,16 +503,31 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
       if (elect_one()) mbar_arrive(smem_u32(&bars->req));
       __syncwarp();
     }
-    if (nf == 0) f0 = row; else f1 = row;
+    if (nf == 0) {
+      f0 = row;
+      g0 = row2;
+    } else {
+      f1 = row;
+      g1 = row2;
+    }
     ++nf;
     return true;
   };
-  auto load_v = [&](int row) -> bool {
-    const int st = vc % C::kVStages;
-    if (!load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
-                   smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]),
-                   ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u, row))
-      return false;
+  auto load_v = [&](int row, int row2) -> bool {
+    if constexpr (C::kIn8) {  // into the e4m3 staging ring, free once converted
+      const int st = vc % C::kV8Stages;
+      if (!load_tile(tm_v, smem_base + C::kV8Off + st * C::kBoxBytes, C::kBoxBytes,
+                     smem_u32(&bars->v8_full[st]), smem_u32(&bars->v8_empty[st]),
+                     ((uint32_t)(vc / C::kV8Stages) & 1u) ^ 1u, row, row2, 1, C::kBoxBytes))
+        return false;
+    } else {
+      const int st = vc % C::kVStages;
+      if (!load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
+                     smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]),
+                     ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u, row, row2, C::kBoxes,
+                     C::kTileBytes))
+        return false;
+    }
     ++vc;
     return true;
   };
@@ -424,18 +535,24 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   ok = next_k();
   if (ok) ok = next_k();
   while (ok && nf > 0) {
-    const int row = f0;
+    const int row = f0, row2 = g0;
     f0 = f1;
+    g0 = g1;
     --nf;
-    ok = load_v(row);
+    ok = load_v(row, row2);
     if (ok) ok = next_k();
   }
   if (!ok) {
     // Let every TMA load this warp issued land before the CTA exits.
     for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
       wait_drain(smem_u32(&bars->k_full[i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
-    for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
-      wait_drain(smem_u32(&bars->v_full[i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
+    if constexpr (C::kIn8) {
+      for (int i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
+        wait_drain(smem_u32(&bars->v8_full[i % C::kV8Stages]), (uint32_t)(i / C::kV8Stages) & 1u);
+    } else {
+      for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
+        wait_drain(smem_u32(&bars->v_full[i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
+    }
   }
 }
 
@@ -456,10 +573,10 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
 // ready.  A negative scale is applied as -Q (instruction-descriptor negate
 // bit) so the softmax always sees a non-negative multiplier.  After a tile's
 // last S the Q buffer is released.
-template <int D>
+template <int D, bool IN8>
 __device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
                           volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   const uint64_t lim = p.timeout_ns;
   const uint32_t idesc_s = C::kIdescS | (p.neg_scale ? (1u << 13) : 0u);
   int kc = 0, qc = 0, tqc = 0;  // S issued, tiles' Q used, tiles taken
@@ -474,12 +591,12 @@ __device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_
                    p.status, lim))
       break;
     ++qc;
-    const uint64_t qd = smem_desc_sw128(smem_base + C::kQOff + qs * C::kTileBytes, 16, 1024);
+    const uint64_t qd = smem_desc_sw128(smem_base + C::kQOff + qs * C::kQKBytes, 16, 1024);
     for (int j = 0; j < n; ++j) {
       if (kc >= kSBufs) {  // PV(kc-3) complete: S[kc % 3] holds nothing needed any more
         const int pv = kc - kSBufs;
-        if (!wait_warp(smem_u32(&bars->v_empty[pv % C::kVStages]),
-                       (uint32_t)(pv / C::kVStages) & 1u, abort_flag, p.status, lim)) {
+        if (!wait_warp(smem_u32(&bars->pv_done[pv % kSBufs]), (uint32_t)(pv / kSBufs) & 1u,
+                       abort_flag, p.status, lim)) {
           ok = false;
           break;
         }
@@ -493,14 +610,20 @@ __device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_
       tc_fence_after();
       if (elect_one()) {
         // descriptors advance by adding the byte offset >> 4 to the start-address field
-        const uint64_t kd = smem_desc_sw128(smem_base + C::kKOff + st * C::kTileBytes, 16, 1024);
+        const uint64_t kd = smem_desc_sw128(smem_base + C::kKOff + st * C::kQKBytes, 16, 1024);
+        // 32 bytes of K per MMA (16 bf16 or 32 e4m3), a new 64-column box every 4
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < C::kSMmas; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tmem + kTmemS + (kc % kSBufs) * 128, qd + off, kd + off, idesc_s,
-                 kk > 0 ? 1u : 0u);
+          if constexpr (C::kIn8)
+            mma_ss_f8(tmem + kTmemS + (kc % kSBufs) * 128, qd + off, kd + off, idesc_s,
+                      kk > 0 ? 1u : 0u);
+          else
+            mma_ss(tmem + kTmemS + (kc % kSBufs) * 128, qd + off, kd + off, idesc_s,
+                   kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars->k_empty[st]));
+        mma_commit(smem_u32(&bars->s_full[kc % kSBufs]));
         if (j == n - 1) mma_commit(smem_u32(&bars->q_empty[qs]));  // the tile's last S: Q free
       }
       __syncwarp();
@@ -519,10 +642,10 @@ __device__ void run_mma_s(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_
 // groups 1024 bytes apart, 64-wide column groups kVGroup apart.  A tile's
 // first PV starts a fresh O.  The commit frees V's ring stage and tells the
 // softmax and the S issuer that PV(g) is done.
-template <int D>
+template <int D, bool IN8>
 __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32_t smem_base,
                            volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   const uint64_t lim = p.timeout_ns;
   int vc = 0, tqc = 0, ntile = 0;  // PV issued, tiles taken, tiles started
   bool ok = true;
@@ -545,8 +668,9 @@ __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32
         break;
       }
       const int st = vc % C::kVStages;
-      if (!wait_warp(smem_u32(&bars->v_full[st]), (uint32_t)(vc / C::kVStages) & 1u, abort_flag,
-                     p.status, lim)) {
+      // V(vc) loaded (fp16 P V: and converted to fp16 by the epilogue warps)
+      if (!wait_warp(smem_u32(C::kF16PV ? &bars->v_conv[st] : &bars->v_full[st]),
+                     (uint32_t)(vc / C::kVStages) & 1u, abort_flag, p.status, lim)) {
         ok = false;
         break;
       }
@@ -562,6 +686,7 @@ __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32
                  (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(smem_u32(&bars->v_empty[st]));
+        mma_commit(smem_u32(&bars->pv_done[vc % kSBufs]));
       }
       __syncwarp();
       ++vc;
@@ -592,25 +717,78 @@ __device__ void write_empty_tiles(const FwdParams& p) {
   }
 }
 
+// 2^x for a pair of fp32 x on the FMA and integer pipes, without the MUFU
+// unit: Cody-Waite range reduction x = n + f with n = round(x)
+// and f in [-1/2, 1/2] (rounding by adding 1.5 * 2^23), 2^f by a cubic fitted
+// for least maximum relative error on [-1/2, 1/2] (Lawson's iteration; error
+// <= 7.5e-5, far below the bf16 rounding of P), and 2^n added to the exponent
+// field (the integer n sits in the low bits of x + 1.5 * 2^23).  x is clamped
+// to [-126, 126]: below, 2^x is negligible next to the row's largest term
+// (>= 2^-8; a masked score, -inf, gives 2^-126 instead of 0, which no fp32
+// sum of such terms can register); above, the result stays huge, so the
+// caller's block-sum test still sees it.
+// Measured on GB300: every split tried (6 to 16 of 32 pairs) is slower than
+// none (the exponential phase is not bound by the MUFU rate there), so the
+// default is 0 and the polynomial path is a tuning option.
+#ifndef BSATTN_EXP2_POLY_PAIRS
+#define BSATTN_EXP2_POLY_PAIRS 0
+#endif
+constexpr int kPolyPairs = BSATTN_EXP2_POLY_PAIRS;  // of each 32 pairs per half row
+constexpr float kExp2C0 = 0.99992808f, kExp2C1 = 0.69326102f, kExp2C2 = 0.24261111f,
+                kExp2C3 = 0.05517149f;
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+
+__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float& y0, float& y1) {
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  x0 = fminf(fmaxf(x0, -126.0f), 126.0f);
+  x1 = fminf(fmaxf(x1, -126.0f), 126.0f);
+  const uint64_t xc = f2_pack(x0, x1);
+  const uint64_t t = f2_add(xc, f2_pack(kRoundMagic, kRoundMagic));   // magic + round(x)
+  const uint64_t nf = f2_add(t, f2_pack(-kRoundMagic, -kRoundMagic));  // round(x), exact
+  const uint64_t f = f2_fma(nf, f2_pack(-1.0f, -1.0f), xc);            // x - round(x), exact
+  uint64_t p = f2_fma(f2_pack(kExp2C3, kExp2C3), f, f2_pack(kExp2C2, kExp2C2));
+  p = f2_fma(p, f, f2_pack(kExp2C1, kExp2C1));
+  p = f2_fma(p, f, f2_pack(kExp2C0, kExp2C0));
+  float p0, p1, t0, t1;
+  f2_unpack(p, p0, p1);
+  f2_unpack(t, t0, t1);
+  y0 = __uint_as_float(__float_as_uint(p0) + (__float_as_uint(t0) << 23));
+  y1 = __uint_as_float(__float_as_uint(p1) + (__float_as_uint(t1) << 23));
+}
+
 // Probabilities of one 64-column half row: p = 2^(s*sl - m), rounded to bf16
-// pairs into pr[] (the A operand of the PV product).  Accumulates the row sum
+// (F16: fp16) pairs into pr[] (the A operand of the PV product).  POLY of the 32 pairs,
+// spread evenly, take their exponentials from exp2_poly_pair, the others from
+// the MUFU unit.  Accumulates the row sum
 // of the fp32 p (for the LSE) in a2, two partial sums in one f32x2 pair, and,
 // when ROUNDED, r32 of the bf16-rounded p that multiply V (the O denominator,
 // so that the weights on V sum to one even when a single key dominates a
 // row), again in two partial sums.  sl2 = (sl, sl), nm2 = (-m, -m).
-template <bool ROUNDED>
+template <bool ROUNDED, int POLY, bool F16>
 __device__ __forceinline__ void softmax_exp64(const uint32_t* sr, uint32_t* pr, uint64_t sl2,
                                               uint64_t nm2, uint64_t& a2, float (&r32)[2]) {
 #pragma unroll
   for (int q = 0; q < 32; ++q) {
-    float x0, x1;
-    f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])), sl2, nm2),
-              x0, x1);
-    const float p0 = ex2_approx(x0);
-    const float p1 = ex2_approx(x1);
-    pr[q] = pack_bf16x2(p0, p1);
+    const uint64_t x2 =
+        f2_fma(f2_pack(__uint_as_float(sr[2 * q]), __uint_as_float(sr[2 * q + 1])), sl2, nm2);
+    float p0, p1;
+    if (((q + 1) * POLY) / 32 != (q * POLY) / 32) {
+      exp2_poly_pair(x2, p0, p1);
+    } else {
+      float x0, x1;
+      f2_unpack(x2, x0, x1);
+      p0 = ex2_approx(x0);
+      p1 = ex2_approx(x1);
+    }
+    pr[q] = F16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
     a2 = f2_add(a2, f2_pack(p0, p1));
-    if (ROUNDED) add_bf16x2_f32(r32[0], r32[1], pr[q]);
+    if (ROUNDED) {
+      if (F16)
+        add_f16x2_f32(r32[0], r32[1], pr[q]);
+      else
+        add_bf16x2_f32(r32[0], r32[1], pr[q]);
+    }
   }
 }
 
@@ -627,10 +805,10 @@ __device__ __forceinline__ float row_max64(const uint32_t* sr) {
   return fmaxf(max3(a[0], a[1], a[2]), max3(max3(a[3], a[4], a[5]), a[6], a[7]));
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool IN8>
 __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   constexpr int DH = D / 2;            // O columns owned by this thread
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -655,10 +833,12 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int e = tq_cnt & 1;
     const uint32_t ph = (uint32_t)(tq_cnt >> 1) & 1u;
     if (!wait_warp(smem_u32(&bars->tq_full[e]), ph, abort_flag, p.status, lim)) return;
-    const volatile int* slot = reinterpret_cast<const volatile int*>(&bars->tq[e]);
-    const int t = slot[0];
-    const int n = slot[2];
-    const int diag_last = slot[3];
+    const volatile TileInfo* slot = &bars->tq[e];
+    const int t = slot->t;
+    const int n = slot->n;
+    const int diag_last = slot->diag;
+    const int n64 = slot->n64;
+    const int last_a = slot->last2[0], last_b = slot->last2[1];
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars->tq_empty[e]));
     ++tq_cnt;
@@ -671,43 +851,83 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     float r32[2] = {0.f, 0.f};  // and bf16-rounded p
     for (int jb = 0; jb < n; ++jb, ++g) {
       const int b = g % kSBufs;  // P barrier of this block
-      // S(g) ready = its commit released K(g)'s stage
-      if (!wait_warp(smem_u32(&bars->k_empty[g % C::kKStages]), (uint32_t)(g / C::kKStages) & 1u,
+      // S(g) ready
+      if (!wait_warp(smem_u32(&bars->s_full[g % kSBufs]), (uint32_t)(g / kSBufs) & 1u,
                      abort_flag, p.status, lim))
         return;
       tc_fence_after();
       const uint32_t tS = tmem + kTmemS + (g % kSBufs) * 128 + lane_off;  // S buffer of this block
-      uint32_t sr[64];
-      tmem_ld16x2_32<64>(tS + 0, sr + 0);
-      tmem_ld16x2_32<64>(tS + 32, sr + 32);
-      tmem_wait_ld();
-      reg_fence(sr, 64);
-      const bool diag = diag_last && jb == n - 1;
-      if (diag) {  // causal diagonal tile: key c is allowed for query row r iff c <= r
-#pragma unroll
-        for (int c = 0; c < 64; ++c) sr[c] = (ch * 64 + c > r) ? kNegInf : sr[c];
+      // Keys c (0..63) of this thread's half of the block with c > klim are
+      // masked: the causal diagonal of 128-key blocks (key 64 ch + c allowed
+      // for query row r iff it is <= r); with 64-key blocks in pairs, the
+      // missing second half of an odd tail (all masked) and, under causal,
+      // the halves among the tile's last two entries that reach past the
+      // tile's first query (key 64 kb + c allowed iff <= 128 qb + r).
+      const bool diag = diag_last && jb == n - 1;  // warp-uniform
+      int klim = diag ? r - 64 * ch : 63;
+      bool masked = diag;
+      if (p.kdiv == 2) {
+        const int e64 = 2 * jb + ch;
+        if (e64 >= n64) {
+          klim = -1;
+        } else if (p.causal && e64 >= n64 - 2) {
+          const int kb = e64 == n64 - 1 ? last_b : last_a;
+          klim = min(63, qb * kBlock + r - kb * 64);
+        }
+        masked = __any_sync(0xffffffffu, klim < 63);
       }
-      // After a tile's first block the probabilities are formed against the
-      // current reference m without a max pass (any common reference gives
-      // the exact softmax).  Only when a row's sum over the block shows that
-      // its scores rose far above m (kGrowSum) -- or on the tile's first
-      // block, where m = -inf -- is the block redone with its max, by the
-      // lazy rule, as the new reference.
       uint32_t pr[32];
       uint64_t b2 = 0;  // this block's sums
       float br32[2] = {0.f, 0.f};
-      bool redo = jb == 0;
+      // This thread's 64 scores of the block, masked as above.
+      auto load_scores = [&](uint32_t (&sr)[64]) {
+        tmem_ld16x2_32<64>(tS + 0, sr + 0);
+        tmem_ld16x2_32<64>(tS + 32, sr + 32);
+        tmem_wait_ld();
+        reg_fence(sr, 64);
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sr[c] = (c > klim) ? kNegInf : sr[c];
+        }
+      };
+      // Masked scores need exact zeros, which the MUFU exponential gives.
+      auto exp_pass = [&](const uint32_t (&sr)[64], float mref) {
+        if constexpr (kPolyPairs == 0) {
+          softmax_exp64<!C::kOnes, 0, C::kF16PV>(sr, pr, sl2, f2_pack(-mref, -mref), b2, br32);
+        } else {
+          if (masked)
+            softmax_exp64<!C::kOnes, 0, C::kF16PV>(sr, pr, sl2, f2_pack(-mref, -mref), b2, br32);
+          else
+            softmax_exp64<!C::kOnes, kPolyPairs, C::kF16PV>(sr, pr, sl2, f2_pack(-mref, -mref),
+                                                            b2, br32);
+        }
+      };
+      // After a tile's first block the probabilities are formed against the
+      // current reference m without a max pass (any common reference gives
+      // the exact softmax).  Only when a row's sum over the block shows that
+      // its scores rose far above m (C::kGrowSum) -- or on the tile's first
+      // block, where m = -inf -- is the block redone with its max, by the
+      // lazy rule, as the new reference.  The redo reads the scores again
+      // from tensor memory (P has not overwritten them yet), so the scores
+      // need not stay in registers past the first pass.
+      // A row with no allowed key so far (m = -inf: possible with 64-key
+      // blocks under causal) always takes the redo path, with reference 0.
+      bool redo = jb == 0 || (p.kdiv == 2 && __any_sync(0xffffffffu, m == __uint_as_float(kNegInf)));
       if (!redo) {
-        softmax_exp64<!C::kOnes>(sr, pr, sl2, f2_pack(-m, -m), b2, br32);
+        uint32_t sr[64];
+        load_scores(sr);
+        exp_pass(sr, m);
         float b0, b1;
         f2_unpack(b2, b0, b1);
         float bs = b0 + b1;
         bs += __shfl_xor_sync(0xffffffffu, bs, 16);  // the other half of the row
-        redo = __any_sync(0xffffffffu, !(bs <= kGrowSum));  // also catches inf / NaN
+        redo = __any_sync(0xffffffffu, !(bs <= C::kGrowSum));  // also catches inf / NaN
       }
       bool need = false;
       float f = 1.f;
       if (redo) {
+        uint32_t sr[64];
+        load_scores(sr);
         float mx = row_max64(sr);
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
         const float xm = mx * sl;
@@ -721,7 +941,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         }
         b2 = 0;
         br32[0] = br32[1] = 0.f;
-        softmax_exp64<!C::kOnes>(sr, pr, sl2, f2_pack(-m, -m), b2, br32);
+        exp_pass(sr, (p.kdiv == 2 && m == __uint_as_float(kNegInf)) ? 0.f : m);
       }
       a2 = f2_add(a2, b2);
       r32[0] += br32[0];
@@ -778,7 +998,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     if constexpr (!C::kOnes) {
       float l = r32[0] + r32[1];  // sum of the rounded P: the O denominator
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (ch == 0) bars->inv_l[r] = 1.0f / l;
+      if (ch == 0) bars->inv_l[r] = l > 0.f ? 1.0f / l : 0.f;  // no allowed key: O = 0
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&bars->epi_full));
@@ -800,10 +1020,74 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
 // shared memory and a named barrier, where the other three warps wait
 // without issuing.  The leader reaches the barrier on every path, with a
 // negative tile to stop, so the four warps always leave together.
+// One tile's O, this thread's row: read O from tensor memory 16 columns at a
+// time, divide by the row's rounded sum and store it.  Each thread writes its
+// own row: 32-byte stores (one full sector each) when the output is 32-byte
+// aligned, else 16-byte ones.
 template <int D, bool OUT_F32>
+__device__ __forceinline__ void write_o_row(const FwdParams& p, const Bars* bars, uint32_t tO,
+                                            int r, int t) {
+  using C = Cfg<D>;
+  float inv_l = 0.f;
+  if constexpr (!C::kOnes) inv_l = bars->inv_l[r];
+  if constexpr (C::kOnes) {  // rounded row sum accumulated by the tensor core in column D
+    uint32_t rs[1];
+    tmem_ld32_1(tO + D, rs);
+    tmem_wait_ld();
+    reg_fence(rs, 1);
+    const float l = __uint_as_float(rs[0]);
+    inv_l = l > 0.f ? 1.0f / l : 0.f;  // no allowed key in the row: O = 0
+  }
+  inv_l *= p.v_scale;  // 1, or the scale of e4m3 V (attention is linear in V)
+  const int bh = t / p.nb;
+  const size_t row = (size_t)bh * p.S + (size_t)(t - bh * p.nb) * kBlock + r;
+  const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+#pragma unroll
+  for (int c0 = 0; c0 < D; c0 += 16) {
+    uint32_t orr[16];
+    tmem_ld32_16(tO + c0, orr);
+    tmem_wait_ld();
+    reg_fence(orr, 16);
+    if constexpr (OUT_F32) {
+      float* dst = reinterpret_cast<float*>(p.out) + row * D + c0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * inv_l);
+      if (wide) {
+        st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(orr));
+        st_global_v8(dst + 8, *reinterpret_cast<const uint32_t(*)[8]>(orr + 8));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          st_global_v4(dst + i, orr[i], orr[i + 1], orr[i + 2], orr[i + 3]);
+      }
+    } else {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + c0;
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
+                            __uint_as_float(orr[2 * i + 1]) * inv_l);
+      if (wide) {
+        st_global_v8(dst, pk);
+      } else {
+        st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
+        st_global_v4(dst + 8, pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
+  }
+}
+
+// For each tile the softmax hands over: wait for its last PV, write O (one
+// thread per query row = TMEM lane); then release O for the next tile's first
+// PV.  Only the leader warp takes tiles and waits (sleeping between tests);
+// it passes the tile on through shared memory and a named barrier, where the
+// other three warps wait without issuing.  The leader reaches the barrier on
+// every path, with a negative tile to stop, so the four warps always leave
+// together.
+template <int D, bool OUT_F32, bool IN8>
 __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
                              volatile int* abort_flag) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r = (warp & 3) * 32 + lane;  // query row of the tile = TMEM lane
@@ -831,53 +1115,7 @@ __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
     const int t = *reinterpret_cast<volatile int*>(&bars->epi_tile[ntile & 1]);
     if (t < 0) return;
     tc_fence_after();
-    float inv_l = 0.f;
-    if constexpr (!C::kOnes) inv_l = bars->inv_l[r];
-    if constexpr (C::kOnes) {  // rounded row sum accumulated by the tensor core in column D
-      uint32_t rs[1];
-      tmem_ld32_1(tO + D, rs);
-      tmem_wait_ld();
-      reg_fence(rs, 1);
-      inv_l = 1.0f / __uint_as_float(rs[0]);
-    }
-    const int bh = t / p.nb;
-    const size_t row = (size_t)bh * p.S + (size_t)(t - bh * p.nb) * kBlock + r;
-    // Each thread writes its own row: 32-byte stores (one full sector each)
-    // when the output is 32-byte aligned, else 16-byte ones.
-    const bool wide = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      uint32_t orr[16];
-      tmem_ld32_16(tO + c0, orr);
-      tmem_wait_ld();
-      reg_fence(orr, 16);
-      if constexpr (OUT_F32) {
-        float* dst = reinterpret_cast<float*>(p.out) + row * D + c0;
-        uint32_t v[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = __float_as_uint(__uint_as_float(orr[i]) * inv_l);
-        if (wide) {
-          st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(v));
-          st_global_v8(dst + 8, *reinterpret_cast<const uint32_t(*)[8]>(v + 8));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) st_global_v4(dst + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
-        }
-      } else {
-        uint16_t* dst = reinterpret_cast<uint16_t*>(p.out) + row * D + c0;
-        uint32_t pk[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          pk[i] = pack_bf16x2(__uint_as_float(orr[2 * i]) * inv_l,
-                              __uint_as_float(orr[2 * i + 1]) * inv_l);
-        if (wide) {
-          st_global_v8(dst, pk);
-        } else {
-          st_global_v4(dst, pk[0], pk[1], pk[2], pk[3]);
-          st_global_v4(dst + 8, pk[4], pk[5], pk[6], pk[7]);
-        }
-      }
-    }
+    write_o_row<D, OUT_F32>(p, bars, tO, r, t);
     tc_fence_before();
     __syncwarp();  // every lane's reads of O are complete
     if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
@@ -885,12 +1123,213 @@ __device__ void run_epilogue(const FwdParams& p, Bars* bars, uint32_t tmem,
   }
 }
 
-template <int D, bool OUT_F32>
+// This warp's quarter of one V tile (128 keys x 64 columns, one 16 KB
+// 128-byte-swizzled box) converted from bf16 to fp16 in place: the layout
+// does not change, element by element.  bf16 converts to fp16 exactly for
+// 2^-14 <= |v| <= 65504 (below, to fp16's subnormals, off by < 2^-25);
+// `rmax` collects, per 16-bit half, the largest fp16 exponent field seen, so
+// that an infinity or NaN (a |v| too large for fp16, or a non-finite v) can
+// be reported.
+__device__ __forceinline__ void convert_v_quarter(uint32_t stage, int wq, int lane,
+                                                  uint32_t& rmax) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t a = stage + (uint32_t)((wq * 256 + i * 32 + lane) * 16);
+    uint32_t w[4];
+    ld_shared_v4(a, w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      w[j] = pack_f16x2(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u));
+      rmax = max_u16x2(rmax, w[j] & 0x7C007C00u);
+    }
+    st_shared_v4(a, w[0], w[1], w[2], w[3]);
+  }
+}
+
+// This warp's quarter of one e4m3 V tile (128 keys x 128 columns, one 16 KB
+// box of 128-byte rows, 128-byte swizzled as TMA wrote it) converted to the
+// fp16 V tile of the P V product (two 64-column boxes `group` bytes apart,
+// 128-byte swizzled as the MMA's descriptor reads them).  e4m3 converts to
+// fp16 exactly; `rmax` collects the fp16 exponent fields as in
+// convert_v_quarter (an e4m3 NaN becomes an fp16 NaN and is reported).
+__device__ __forceinline__ void convert_v8_quarter(uint32_t src, uint32_t dst, uint32_t group,
+                                                   int wq, int lane, uint32_t& rmax) {
+#pragma unroll 1  // one chunk at a time: these warps run with few registers
+  for (int i = 0; i < 8; ++i) {
+    const int idx = wq * 256 + i * 32 + lane;
+    const uint32_t r = (uint32_t)idx >> 3, c = (uint32_t)idx & 7u;  // key row, 16-byte chunk
+    uint32_t w[4];
+    ld_shared_v4(src + r * 128u + ((c ^ (r & 7u)) << 4), w);
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      e4m3x4_to_f16x4(w[j], h[2 * j], h[2 * j + 1]);
+      rmax = max_u16x2(rmax, h[2 * j] & 0x7C007C00u);
+      rmax = max_u16x2(rmax, h[2 * j + 1] & 0x7C007C00u);
+    }
+    // columns 16c .. 16c+15 -> box c / 4, its 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1
+    const uint32_t box = dst + (c >> 2) * group + r * 128u;
+    const uint32_t j0 = 2u * (c & 3u);
+    st_shared_v4(box + ((j0 ^ (r & 7u)) << 4), h[0], h[1], h[2], h[3]);
+    st_shared_v4(box + (((j0 + 1u) ^ (r & 7u)) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
+
+// The epilogue warps when P V runs in fp16 (D = 64, or e4m3 inputs): besides
+// writing each tile's O (as run_epilogue does), they convert every V tile of
+// the CTA's block stream to fp16 after its load, each warp a quarter, and
+// announce it on v_conv (four arrivals): in place at D = 64; with e4m3 inputs
+// from the staging ring into the fp16 ring, once the fp16 stage's previous
+// tile has been multiplied (its PV complete), freeing the staging stage.  Blocks are converted in stream order.  Before a
+// tile's O is written, all of the tile's V tiles are converted (its PVs need
+// them); while waiting for the tile's last PV, a warp also converts the next
+// tiles' V tiles as soon as they are loaded, so the next tile's first PV does
+// not wait for the conversion after O is released.  Each warp decides alone
+// when its rows of O can be written (the softmax's hand-over and the last PV
+// are both complete), so no barrier joins them there.
+template <int D, bool OUT_F32, bool IN8>
+__device__ void run_epilogue_convert(const FwdParams& p, Bars* bars, uint32_t tmem,
+                                     uint32_t smem_base, volatile int* abort_flag) {
+  using C = Cfg<D, IN8>;
+  static_assert(C::kBoxes == 1 || C::kIn8, "one 64-column box per bf16 V tile");
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int wq = warp & 3;
+  const int r = wq * 32 + lane;  // query row of the tile = TMEM lane
+  const uint32_t tO = tmem + kTmemO + ((uint32_t)(wq * 32) << 16);
+  const uint64_t lim = p.timeout_ns;
+  int tqc = 0;    // (leader) tiles taken
+  int known = 0;  // blocks of the stream in the tiles seen so far
+  int cg = 0;     // blocks whose V this warp has converted
+  int ntile = 0;  // tiles taken
+  uint32_t rmax = 0;
+  bool ok = true;  // false once a wait of this warp failed
+  auto convert_next = [&]() {
+    const int st = cg % C::kVStages;
+    if constexpr (C::kIn8) {
+      const int s8 = cg % C::kV8Stages;
+      convert_v8_quarter(smem_base + C::kV8Off + s8 * C::kBoxBytes,
+                         smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup, wq, lane, rmax);
+      fence_proxy_async_smem();  // the tensor core reads what these generic stores wrote
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&bars->v_conv[st]));
+        mbar_arrive(smem_u32(&bars->v8_empty[s8]));
+      }
+    } else {
+      convert_v_quarter(smem_base + C::kVOff + st * C::kBoxBytes, wq, lane, rmax);
+      fence_proxy_async_smem();  // the tensor core reads what these generic stores wrote
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->v_conv[st]));
+    }
+    ++cg;
+  };
+  // V(g) can be converted: loaded (e4m3: staged, and the fp16 stage's
+  // previous tile multiplied).  Non-blocking, warp-uniform.
+  auto v_loaded = [&](int g) -> bool {
+    bool rdy = false;
+    if (lane == 0) {
+      if constexpr (C::kIn8)
+        rdy = mbar_test_wait(smem_u32(&bars->v8_full[g % C::kV8Stages]),
+                             (uint32_t)(g / C::kV8Stages) & 1u) &&
+              (g < C::kVStages ||
+               mbar_test_wait(smem_u32(&bars->v_empty[(g - C::kVStages) % C::kVStages]),
+                              (uint32_t)((g - C::kVStages) / C::kVStages) & 1u));
+      else
+        rdy = mbar_test_wait(smem_u32(&bars->v_full[g % C::kVStages]),
+                             (uint32_t)(g / C::kVStages) & 1u);
+    }
+    return __shfl_sync(0xffffffffu, rdy, 0);
+  };
+  // The same, waiting (bounded) until it holds.
+  auto wait_v = [&](int g) -> bool {
+    if constexpr (C::kIn8) {
+      if (!wait_warp(smem_u32(&bars->v8_full[g % C::kV8Stages]), (uint32_t)(g / C::kV8Stages) & 1u,
+                     abort_flag, p.status, lim))
+        return false;
+      return g < C::kVStages ||
+             wait_warp(smem_u32(&bars->v_empty[(g - C::kVStages) % C::kVStages]),
+                       (uint32_t)((g - C::kVStages) / C::kVStages) & 1u, abort_flag, p.status, lim);
+    } else {
+      return wait_warp(smem_u32(&bars->v_full[g % C::kVStages]), (uint32_t)(g / C::kVStages) & 1u,
+                       abort_flag, p.status, lim);
+    }
+  };
+  // Every warp reaches the named barrier once per tile taken, on every path:
+  // a warp whose wait failed (abort flag raised) skips the rest of each
+  // iteration, and the leader's next take_tile then fails too and publishes
+  // the stop value, so the four warps always leave together.
+  for (;;) {
+    if (warp == kWarpEpi0) {
+      int t = 0, r0 = 0, n = 0, col = 0;
+      const bool got = ok && take_tile(bars, tqc, p, abort_flag, t, r0, n, col, kSleepNs);
+      ++tqc;
+      if (lane == 0) {
+        bars->epi_tile[ntile & 1] = got ? t : -1;
+        bars->epi_n[ntile & 1] = n;
+      }
+    }
+    named_bar_sync(kEpiBarrier, kEpiWarps * 32);
+    const int t = *reinterpret_cast<volatile int*>(&bars->epi_tile[ntile & 1]);
+    const int n = *reinterpret_cast<volatile int*>(&bars->epi_n[ntile & 1]);
+    ++ntile;
+    if (t < 0) break;
+    if (!ok) continue;
+    known += n;
+    // the tile's V tiles (those not converted ahead already)
+    while (cg < known) {
+      if (!wait_v(cg)) {
+        ok = false;
+        break;
+      }
+      convert_next();
+    }
+    if (!ok) continue;
+    // wait for the softmax's hand-over and the tile's last PV; meanwhile
+    // convert the following V tiles as they arrive
+    const int gl = known - 1;
+    const uint32_t tpar = (uint32_t)(ntile - 1) & 1u;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      bool rdy = false;
+      if (lane == 0)
+        rdy = mbar_test_wait(smem_u32(&bars->epi_full), tpar) &&
+              mbar_test_wait(smem_u32(&bars->v_empty[gl % C::kVStages]),
+                             (uint32_t)(gl / C::kVStages) & 1u);
+      if (__shfl_sync(0xffffffffu, rdy, 0)) break;
+      if (v_loaded(cg)) {
+        convert_next();
+        continue;
+      }
+      if (*abort_flag || globaltimer_ns() - t0 > lim) {
+        if (lane == 0 && !*abort_flag) {
+          *abort_flag = 1;
+          atomicOr(p.status, kStatusTimeout);
+        }
+        ok = false;
+        break;
+      }
+      __nanosleep(kSleepNs);
+    }
+    __syncwarp();
+    if (!ok) continue;
+    tc_fence_after();
+    write_o_row<D, OUT_F32>(p, bars, tO, r, t);
+    tc_fence_before();
+    __syncwarp();  // every lane's reads of O are complete
+    if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
+  }
+  // A V entry that is not finite in fp16 (|v| > 65504, or inf / NaN) was converted.
+  const bool bad = (rmax & 0xFFFFu) == 0x7C00u || (rmax >> 16) == 0x7C00u;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusRange);
+}
+
+template <int D, bool OUT_F32, bool IN8>
 __global__ void __launch_bounds__(kThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, IN8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles want 1024-byte alignment
@@ -906,13 +1345,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::kVStages; ++i) {
       mbar_init(smem_u32(&bars->v_full[i]), 1);
       mbar_init(smem_u32(&bars->v_empty[i]), 1);
+      mbar_init(smem_u32(&bars->v_conv[i]), kEpiWarps);  // one arrival per epilogue warp
+    }
+    for (int i = 0; i < C::kV8Stages; ++i) {
+      mbar_init(smem_u32(&bars->v8_full[i]), 1);
+      mbar_init(smem_u32(&bars->v8_empty[i]), kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->q_full[i]), 1);
       mbar_init(smem_u32(&bars->q_empty[i]), 1);
     }
     // the softmax warps arrive once per warp (elected lane, after __syncwarp)
-    for (int i = 0; i < kSBufs; ++i) mbar_init(smem_u32(&bars->p_full[i]), kSoftmaxWarps);
+    for (int i = 0; i < kSBufs; ++i) {
+      mbar_init(smem_u32(&bars->p_full[i]), kSoftmaxWarps);
+      mbar_init(smem_u32(&bars->s_full[i]), 1);
+      mbar_init(smem_u32(&bars->pv_done[i]), 1);
+    }
     mbar_init(smem_u32(&bars->drain), 2);
     mbar_init(smem_u32(&bars->req), 1);
     mbar_init(smem_u32(&bars->epi_full), kSoftmaxWarps);
@@ -928,10 +1376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&bars->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  if constexpr (C::kOnes) {  // bf16 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
+  if constexpr (C::kOnes) {  // 1.0 tiles read by the PV MMA (generic-proxy writes, then a proxy fence)
+    constexpr uint32_t one2 = C::kF16PV ? 0x3C003C00u : 0x3F803F80u;  // fp16 / bf16 pairs of 1.0
     uint4* ones = reinterpret_cast<uint4*>(smem_raw + (base - raw) + C::kOnesOff);
     for (int i = threadIdx.x; i < C::kVStages * C::kBoxBytes / 16; i += kThreads)
-      ones[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+      ones[i] = make_uint4(one2, one2, one2, one2);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == kWarpLoad && lane == 0) {
@@ -948,18 +1397,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kSoftmaxThreads / 32) {
     regs_dec<kRegsOther>();
     if (warp == kWarpLoad)
-      run_producer<D>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
+      run_producer<D, IN8>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
     else if (warp == kWarpMmaS)
-      run_mma_s<D>(p, bars, tmem, base, abort_flag);
+      run_mma_s<D, IN8>(p, bars, tmem, base, abort_flag);
     else if (warp == kWarpMmaPV)
-      run_mma_pv<D>(p, bars, tmem, base, abort_flag);
-    else if (warp >= kWarpEpi0)
-      run_epilogue<D, OUT_F32>(p, bars, tmem, abort_flag);
+      run_mma_pv<D, IN8>(p, bars, tmem, base, abort_flag);
+    else if (warp >= kWarpEpi0) {
+      if constexpr (C::kF16PV)
+        run_epilogue_convert<D, OUT_F32, IN8>(p, bars, tmem, base, abort_flag);
+      else
+        run_epilogue<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
+    }
     else if (warp == kWarpSched)
-      run_scheduler<D>(&tm_q, p, bars, base, abort_flag);
+      run_scheduler<D, IN8>(&tm_q, p, bars, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, OUT_F32>(p, bars, tmem, abort_flag);
+    run_softmax<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
   }
   __syncwarp();  // reconverge each warp before the CTA-wide barrier
 
@@ -995,10 +1448,10 @@ __global__ void selftest_wait_kernel(unsigned long long timeout_ns, int* status)
   __syncthreads();
 }
 
-template <int D, bool OUT_F32>
+template <int D, bool OUT_F32, bool IN8>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream) {
-  const size_t smem = Cfg<D>::kSmem + 1024;
+  const size_t smem = Cfg<D, IN8>::kSmem + 1024;
   // The shared-memory opt-in is set once per device (it costs host time on
   // every call otherwise); a failed attempt is retried on the next call.
   static std::atomic<bool> opted_in[kMaxDevices];
@@ -1006,12 +1459,12 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32>,
+    e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32, IN8>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_fwd_kernel<D, OUT_F32><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  bsattn_fwd_kernel<D, OUT_F32, IN8><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -1022,13 +1475,19 @@ size_t fwd_smem_bytes(int D) {
 }
 
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream) {
-  if (D == 64) {
-    return out_f32 ? launch_one<64, true>(tq, tk, tv, p, grid, stream)
-                   : launch_one<64, false>(tq, tk, tv, p, grid, stream);
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream,
+                       bool in8) {
+  if (in8) {
+    if (D != 128) return cudaErrorInvalidValue;
+    return out_f32 ? launch_one<128, true, true>(tq, tk, tv, p, grid, stream)
+                   : launch_one<128, false, true>(tq, tk, tv, p, grid, stream);
   }
-  return out_f32 ? launch_one<128, true>(tq, tk, tv, p, grid, stream)
-                 : launch_one<128, false>(tq, tk, tv, p, grid, stream);
+  if (D == 64) {
+    return out_f32 ? launch_one<64, true, false>(tq, tk, tv, p, grid, stream)
+                   : launch_one<64, false, false>(tq, tk, tv, p, grid, stream);
+  }
+  return out_f32 ? launch_one<128, true, false>(tq, tk, tv, p, grid, stream)
+                 : launch_one<128, false, false>(tq, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,

@@ -15,7 +15,9 @@ constexpr int kMaxBlocksPerRow = 4096;
 constexpr uint32_t kPlanMagic = 0x42535041u;  // "BSPA"
 
 // Status bits written by kernels into the caller's status word.
-enum : int { kStatusTimeout = 1, kStatusInternal = 2 };
+// kStatusRange: an input value the kernel's arithmetic cannot hold (see
+// BSATTN_ERR_RANGE).
+enum : int { kStatusTimeout = 1, kStatusInternal = 2, kStatusRange = 4 };
 
 // Device workspace words owned by a plan.
 enum : int { kWorkCounter = 0, kWorkStatus = 1, kWorkDone = 2, kWorkWords = 4 };
@@ -57,6 +59,12 @@ struct FwdParams {
   // query head
   int H = 1;
   int kv_group = 1;
+  // multiplies O (the scale of e4m3 V; 1 for bf16 inputs)
+  float v_scale = 1.0f;
+  // key blocks of 128 / kdiv keys: 2 = 64-key blocks, which the kernel runs in
+  // pairs (two consecutive entries of a tile's list fill one 128-key stage;
+  // the K and V tensor maps then have 64-row boxes)
+  int kdiv = 1;
 };
 
 // Everything the backward kernel needs besides its four tensor maps.
@@ -89,7 +97,10 @@ bool get_tensor_map_encoder();
 int device_sm_count(int dev);
 bool aligned16(const void* p);
 bsattn_status from_cuda(cudaError_t e);
-bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows);
+bsattn_status encode_bf16_map(CUtensorMap* m, const void* ptr, int D, long long rows,
+                              int box_rows = kBlock);
+bsattn_status encode_e4m3_map(CUtensorMap* m, const void* ptr, int D, long long rows,
+                              int box_rows = kBlock);
 
 // One forward launch with everything resolved: tensor maps, kernel
 // parameters, grid.  prepare_fwd checks the arguments exactly as bsattn_fwd
@@ -99,24 +110,29 @@ struct PreparedFwd {
   FwdParams prm;
   int D = 0;
   bool out_f32 = false;
+  bool in8 = false;
   int grid = 0;
 };
 // Hkv: K/V heads (H % Hkv == 0; Hkv == H for plain multi-head attention).
+// in8: q, k, v are e4m3 (D = 128); v_scale multiplies O.
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf, int Hkv);
+                          PreparedFwd* pf, int Hkv, bool in8 = false, float v_scale = 1.0f);
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream);
 
 // plan.cu
 // mdiv: head (b*H + h) reads mask (b*H + h) / mdiv (1: a mask per head; H: one
 // mask per batch entry shared by its heads)
+// kdiv: key blocks of 128 / kdiv keys (1: 128-key blocks, the mask is
+// [nb][nb] per head; 2: 64-key blocks, [nb][2 nb]); the CSR then lists 64-key
+// blocks, and the schedule counts a tile's length in pairs of them.
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,
-                                cudaStream_t stream, int mdiv = 1);
+                                cudaStream_t stream, int mdiv = 1, int kdiv = 1);
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
                                 int* d_tile_order, int* d_empty_tiles, int nsm,
-                                cudaStream_t stream, int mdiv = 1);
+                                cudaStream_t stream, int mdiv = 1, int kdiv = 1);
 // Transposed plan (per key block, the ascending live query blocks); d_counts
 // is scratch of R ints.
 cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
@@ -125,8 +141,10 @@ cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_c
 int schedule_chunk_heads(int nb);
 
 // fwd_sm103.cu
+// in8: Q, K, V are e4m3 (D = 128 only; the tensor maps are of uint8 elements)
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream);
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream,
+                       bool in8 = false);
 size_t fwd_smem_bytes(int D);
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
                                  cudaStream_t stream);

@@ -176,5 +176,6 @@ extern "C" bsattn_status bsattn_fwd_noalloc(const void* q, const void* k, const 
     return from_cuda(e);
   if (status & kStatusInternal) return BSATTN_ERR_INTERNAL;
   if (status & kStatusTimeout) return BSATTN_ERR_TIMEOUT;
+  if (status & kStatusRange) return BSATTN_ERR_RANGE;
   return BSATTN_OK;
 }

@@ -29,23 +29,33 @@ namespace {
 constexpr int kScanThreads = 1024;
 // Key blocks of K/V per schedule chunk: 768 blocks of 128 keys x D=128 bf16
 // K and V = 48 MB, well inside the 126 MB L2.
-constexpr int kChunkKeyBlocks = 768;
+#ifndef BSATTN_SCHED_CHUNK_BLOCKS
+#define BSATTN_SCHED_CHUNK_BLOCKS 768
+#endif
+constexpr int kChunkKeyBlocks = BSATTN_SCHED_CHUNK_BLOCKS;
 
-__device__ __forceinline__ bool block_live(const uint8_t* mask_row, int kb, int qb, int causal) {
-  return mask_row[kb] != 0 && (!causal || kb <= qb);
+// Key blocks are 128 / kdiv keys (kdiv = 1: 128, kdiv = 2: 64); a query
+// block qb (128 queries) has kdiv * nb key blocks per mask row.  Under causal
+// a key block is kept when its first key is <= the tile's last query, i.e.
+// kb < (qb + 1) * kdiv.
+__device__ __forceinline__ bool block_live(const uint8_t* mask_row, int kb, int qb, int causal,
+                                           int kdiv) {
+  return mask_row[kb] != 0 && (!causal || kb < (qb + 1) * kdiv);
 }
 
 // One warp per CSR row: number of live key blocks.  Also counts, per head, the
 // rows with at least one live block.
-__global__ void count_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int causal,
-                             int mdiv, int* __restrict__ counts, int* __restrict__ live_per_head) {
+__global__ void count_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int kdiv,
+                             int causal, int mdiv, int* __restrict__ counts,
+                             int* __restrict__ live_per_head) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int qb = warp % nb;
-  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nb;
+  const int nbk = nb * kdiv;
+  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nbk;
   int c = 0;
-  for (int kb = lane; kb < nb; kb += 32) c += block_live(mrow, kb, qb, causal) ? 1 : 0;
+  for (int kb = lane; kb < nbk; kb += 32) c += block_live(mrow, kb, qb, causal, kdiv) ? 1 : 0;
   c = __reduce_add_sync(0xffffffffu, c);
   if (lane == 0) {
     counts[warp] = c;
@@ -96,17 +106,19 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 // One warp per CSR row: write the live kb in ascending order.
-__global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int causal,
-                            int mdiv, const int* __restrict__ row_ptr, int* __restrict__ col_idx) {
+__global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, int kdiv,
+                            int causal, int mdiv, const int* __restrict__ row_ptr,
+                            int* __restrict__ col_idx) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int qb = warp % nb;
-  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nb;
+  const int nbk = nb * kdiv;
+  const uint8_t* mrow = mask + ((size_t)(warp / nb / mdiv) * nb + qb) * nbk;
   int base = row_ptr[warp];
-  for (int kb0 = 0; kb0 < nb; kb0 += 32) {
+  for (int kb0 = 0; kb0 < nbk; kb0 += 32) {
     const int kb = kb0 + lane;
-    const bool live = kb < nb && block_live(mrow, kb, qb, causal);
+    const bool live = kb < nbk && block_live(mrow, kb, qb, causal, kdiv);
     const unsigned bal = __ballot_sync(0xffffffffu, live);
     if (live) col_idx[base + __popc(bal & ((1u << lane) - 1u))] = kb;
     base += __popc(bal);
@@ -123,10 +135,13 @@ __global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, 
 // run long after every other SM has finished.  Chunk k's slice of tile_order
 // therefore holds its own short enough tiles plus the long tiles of chunk
 // k+1, and starts at (live tiles of chunks < k) + (tiles moved out of chunk
-// k).  Empty tiles are listed head by head, qb ascending.
+// k).  Empty tiles are listed head by head, qb ascending.  With kdiv = 2
+// (64-key blocks, run in pairs) a tile's length is its pairs,
+// ceil(live blocks / 2), and a chunk's blocks count in pairs likewise.
 __global__ void __launch_bounds__(1024)
     order_kernel(const int* __restrict__ row_ptr, const int* __restrict__ live_off, int BH, int nb,
-                 int kh, int nsm, int* __restrict__ tile_order, int* __restrict__ empty_tiles) {
+                 int kdiv, int kh, int nsm, int* __restrict__ tile_order,
+                 int* __restrict__ empty_tiles) {
   extern __shared__ uint32_t keys[];
   __shared__ int n_in, n_moved;
   const int k = blockIdx.x;
@@ -135,9 +150,10 @@ __global__ void __launch_bounds__(1024)
   const int h2 = min(BH, h1 + kh);  // next chunk's heads [h1, h2)
   // a count above thr is "long" in its chunk
   const long long thr_own =
-      (long long)(row_ptr[h1 * nb] - row_ptr[h0 * nb]) / (2ll * nsm);
+      (long long)(row_ptr[h1 * nb] - row_ptr[h0 * nb]) / kdiv / (2ll * nsm);
   const long long thr_next =
-      (h2 > h1) ? (long long)(row_ptr[h2 * nb] - row_ptr[h1 * nb]) / (2ll * nsm) : (1ll << 40);
+      (h2 > h1) ? (long long)(row_ptr[h2 * nb] - row_ptr[h1 * nb]) / kdiv / (2ll * nsm)
+                : (1ll << 40);
   const int own = (h1 - h0) * nb;
   const int pool = (h2 - h0) * nb;
   int n2 = 1;
@@ -151,7 +167,7 @@ __global__ void __launch_bounds__(1024)
     uint32_t key = 0xFFFFFFFFu;
     if (i < pool) {
       const int r = h0 * nb + i;
-      const int cnt = row_ptr[r + 1] - row_ptr[r];
+      const int cnt = (row_ptr[r + 1] - row_ptr[r] + kdiv - 1) / kdiv;  // blocks, or pairs
       bool in;
       if (i < own) {
         const bool moved = k > 0 && cnt > thr_own;
@@ -250,14 +266,14 @@ __global__ void csc_fill_kernel(const uint8_t* __restrict__ mask, int cols, int 
 
 cudaError_t plan_count_and_scan(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
                                 int* d_row_ptr, int* d_live_off, int* d_totals,
-                                cudaStream_t stream, int mdiv) {
+                                cudaStream_t stream, int mdiv, int kdiv) {
   const int rows = BH * nb;
   int* live_per_head = d_counts + rows;  // caller sized d_counts as rows + BH
   cudaError_t e = cudaMemsetAsync(live_per_head, 0, sizeof(int) * BH, stream);
   if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, mdiv,
+  count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, kdiv, causal, mdiv,
                                                           d_counts, live_per_head);
   scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, rows, live_per_head, BH, d_row_ptr,
                                               d_live_off, reinterpret_cast<long long*>(d_totals));
@@ -269,18 +285,18 @@ int schedule_chunk_heads(int nb) { return nb >= kChunkKeyBlocks ? 1 : kChunkKeyB
 cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causal,
                                 const int* d_row_ptr, const int* d_live_off, int* d_col_idx,
                                 int* d_tile_order, int* d_empty_tiles, int nsm,
-                                cudaStream_t stream, int mdiv) {
+                                cudaStream_t stream, int mdiv, int kdiv) {
   const int rows = BH * nb;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, causal, mdiv,
+  fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, rows, nb, kdiv, causal, mdiv,
                                                          d_row_ptr, d_col_idx);
   const int kh = schedule_chunk_heads(nb);
   const int chunks = (BH + kh - 1) / kh;
   int n2 = 1;
   while (n2 < 2 * kh * nb) n2 <<= 1;
   order_kernel<<<chunks, 1024, sizeof(uint32_t) * n2, stream>>>(
-      d_row_ptr, d_live_off, BH, nb, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles);
+      d_row_ptr, d_live_off, BH, nb, kdiv, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles);
   return cudaGetLastError();
 }
 

@@ -180,6 +180,18 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], 8-bit floating-point operands (kind::f8f6f4;
+// the operand formats are in the instruction descriptor)
+__device__ __forceinline__ void mma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem]
 __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -214,15 +226,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, dense.
-// [4,6) D format (1 = f32), [7,10) A format (1 = bf16), [10,13) B format
-// (1 = bf16), bit 15 A major (1 = MN), bit 16 B major (1 = MN), [17,23) N>>3,
-// [24,29) M>>4.
+// Instruction descriptor, kind::f16: bf16 x bf16 (or f16 x f16) -> fp32, dense.
+// [4,6) D format (1 = f32), [7,10) A format (0 = f16, 1 = bf16), [10,13) B
+// format (same codes; A and B must have the same type), bit 15 A major
+// (1 = MN), bit 16 B major (1 = MN), [17,23) N>>3, [24,29) M>>4.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool b_mn_major,
+                                                         bool a_mn_major, bool ab_f16) {
+  return (1u << 4) | ((ab_f16 ? 0u : 1u) << 7) | ((ab_f16 ? 0u : 1u) << 10) |
+         ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major,
                                                       bool a_mn_major = false) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
-         ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+  return idesc_f16kind_f32(M, N, b_mn_major, a_mn_major, false);
 }
 
 // tcgen05.ld / st, shape 32x32b: thread t of the warp reads/writes TMEM lane
@@ -391,9 +407,42 @@ __device__ __forceinline__ void add_bf16x2_f32(float& d0, float& d1, uint32_t pa
       : "r"(pair));
 }
 
+// d0 += low fp16 of `pair`, d1 += high fp16 of `pair` (exact widening, one fp32
+// rounding each).
+__device__ __forceinline__ void add_f16x2_f32(float& d0, float& d1, uint32_t pair) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "r"(pair));
+}
+
+// Four e4m3 values (bytes 0..3 of `w`) to fp16, exactly: `lo` gets bytes 0, 1,
+// `hi` bytes 2, 3 (the lower byte in the lower half).
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Pack two floats to f16x2 with round-to-nearest-even (+-inf beyond +-65504):
+// `lo` in bits 0..15.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Per 16-bit half: unsigned maximum.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
 
@@ -408,6 +457,13 @@ __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, ui
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
                "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void ld_shared_v4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr)
                : "memory");
 }
 

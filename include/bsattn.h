@@ -36,6 +36,10 @@
  *    [B][H][S] fp32; the mask is uint8 [B][H][S/128][S/128], nonzero = live.
  *  - Supported: D in {64, 128}; S a positive multiple of 128 with S/128 <= 4096;
  *    B*H*S < 2^31; Q, K, V bf16; O bf16 (default) or fp32 (BSATTN_OUT_F32).
+ *  - Arithmetic: S = Q K^T on the tensor core in bf16 with fp32 accumulation;
+ *    the probabilities P and the product P V in bf16 at D = 128, in fp16 at
+ *    D = 64 (V converted exactly from bf16; |V| above 65504, or a non-finite
+ *    V, is reported as BSATTN_ERR_RANGE), fp32 accumulation; softmax in fp32.
  */
 #ifndef BSATTN_H_
 #define BSATTN_H_
@@ -54,7 +58,11 @@ typedef enum {
   BSATTN_ERR_OOM = 4,          /* device or host allocation failed */
   BSATTN_ERR_TIMEOUT = 5,      /* a kernel gave up waiting (bounded wait ran out) */
   BSATTN_ERR_INTERNAL = 6,     /* a kernel detected an inconsistent state */
-  BSATTN_ERR_SCRATCH_LIMIT = 7 /* problem too large for bsattn_fwd_noalloc's fixed scratch */
+  BSATTN_ERR_SCRATCH_LIMIT = 7, /* problem too large for bsattn_fwd_noalloc's fixed scratch */
+  BSATTN_ERR_RANGE = 8         /* an input value outside what the kernel's arithmetic holds:
+                                  at D = 64 the forward pass multiplies P by V in fp16, so
+                                  every V entry must be finite with |v| <= 65504; reported
+                                  after the launch, by the status calls */
 } bsattn_status;
 
 /* Opaque plan: the per-query-tile list of live key blocks and the tile order. */
@@ -64,8 +72,11 @@ typedef struct bsattn_plan_s* bsattn_plan_t;
 enum {
   BSATTN_CAUSAL = 1u,   /* also require key j <= query i (element level, inclusive) */
   BSATTN_OUT_F32 = 2u,  /* bsattn_fwd writes O as fp32 instead of bf16 */
-  BSATTN_MASK_SHARED_HEADS = 4u  /* bsattn_plan only: d_mask is [B][1][S/128][S/128],
+  BSATTN_MASK_SHARED_HEADS = 4u, /* bsattn_plan only: d_mask is [B][1][S/128][S/128],
                                     one mask per batch entry for all its H heads */
+  BSATTN_KEY_BLOCK_64 = 8u       /* bsattn_plan only: key blocks of 64 keys; d_mask is
+                                    [B][H][S/128][S/64] (one entry per 128-query x
+                                    64-key block); forward pass only */
 };
 
 /*
@@ -193,8 +204,36 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
                              void* out, float* lse, int B, int H, int Hkv, int S, int D,
                              float scale, void* stream);
 
+/*
+ * bsattn_fwd_fp8 -- the forward pass on FP8 (e4m3) Q, K, V.
+ *
+ * "JAX Pallas and Blackwell", section "What the Tutorial Covers": Blackwell's
+ * tensor cores take FP8 operands with fp32 accumulation.  Here S = Q K^T runs
+ * on e4m3 operands (the OCP 8-bit format: sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits) with fp32 accumulation; each e4m3 V tile is converted to
+ * fp16 in shared memory (exactly) and P V runs in fp16, fp32 accumulation.
+ * The result is the attention of bsattn_fwd on the decoded values:
+ *
+ *   O = v_scale * softmax(scale * Q K^T + mask) V,  LSE as bsattn_fwd.
+ *
+ * FP8 tensors usually carry scales (value = scale_t * decoded bits): pass
+ * scale = softmax scale * q_scale * k_scale, and v_scale = V's scale.
+ *
+ *   q8, k8, v8 device e4m3 [B][H][S][D] (one byte per element), 16-byte aligned.
+ *   plan       from bsattn_plan (any flags bsattn_fwd takes, 64-key blocks too).
+ *   out, lse   as bsattn_fwd.
+ *   D          128 (UNSUPPORTED otherwise).
+ *   scale, v_scale  finite.
+ * Errors: as bsattn_fwd; a NaN entry of V (e4m3 0x7F / 0xFF) is reported as
+ * BSATTN_ERR_RANGE by the status calls.
+ */
+bsattn_status bsattn_fwd_fp8(const void* q8, const void* k8, const void* v8, bsattn_plan_t plan,
+                             void* out, float* lse, int B, int H, int S, int D, float scale,
+                             float v_scale, void* stream);
+
 /* Wait for `stream`, then report and clear the device-side status of the
-   plan's kernels: OK, TIMEOUT or INTERNAL (or CUDA if the wait failed). */
+   plan's kernels: OK, TIMEOUT, INTERNAL or RANGE (or CUDA if the wait
+   failed). */
 bsattn_status bsattn_plan_status(bsattn_plan_t plan, void* stream);
 
 /* Release the plan (waits for the device first).  NULL is ignored. */

@@ -22,7 +22,7 @@ def lib():
 def _declared():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(bsattn_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(bsattn_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -57,7 +57,7 @@ def test_plan_rejects_bad_arguments_without_a_device(lib):
     assert lib.bsattn_plan(fake, 1, 1, 100, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
     assert lib.bsattn_plan(fake, 0, 1, 128, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
     assert lib.bsattn_plan(fake, 1, -2, 128, 0, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
-    assert lib.bsattn_plan(fake, 1, 1, 128, 8, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 1, 128, 16, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
     assert lib.bsattn_plan(fake, 1, 1, 128 * 4097, 0, vp(0), ctypes.byref(out)) == bs.ERR_UNSUPPORTED
     assert lib.bsattn_plan(fake, 1024, 1024, 4096, 0, vp(0), ctypes.byref(out)) == bs.ERR_UNSUPPORTED
     assert out.value is None
@@ -117,7 +117,7 @@ def test_backward_and_gqa_reject_missing_plan(lib):
     out = vp()
     assert lib.bsattn_plan(vp(0), 1, 4, 128, bs.MASK_SHARED_HEADS, vp(0), ctypes.byref(out)) == \
         bs.ERR_INVALID_ARG  # (null mask)
-    assert lib.bsattn_plan(fake, 1, 4, 128, 16, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
+    assert lib.bsattn_plan(fake, 1, 4, 128, 32, vp(0), ctypes.byref(out)) == bs.ERR_INVALID_ARG
 
 
 def test_noalloc_wrapper_rejects_bad_tensors_before_any_call(monkeypatch):

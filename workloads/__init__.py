@@ -111,14 +111,18 @@ _E4M3_POS = np.array([(m / 8.0) * 2.0 ** -6 if e == 0 else (1 + m / 8.0) * 2.0 *
 
 def e4m3_bits(x: np.ndarray) -> np.ndarray:
     """Round values to e4m3 (nearest, ties to the even code; beyond +-448
-    saturates to +-448; NaN -> 0x7F); returns the uint8 bit patterns."""
+    saturates to +-448; NaN -> 0x7F); returns the uint8 bit patterns.
+
+    A value a = |x| in [2^E, 2^(E+1)) (E >= -6) has e4m3 steps of 2^(E-3):
+    q = rint(a / 2^(E-3)) in [8, 16] (16 carries into the next binade), code
+    = (E + 7) * 8 + q - 8; below 2^-6 the steps are 2^-9 (subnormals)."""
     x = np.asarray(x, dtype=np.float64)
-    a = np.minimum(np.abs(x), _E4M3_POS[-1])
-    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)
-    lo = np.clip(hi - 1, 0, 126)
-    d_lo, d_hi = a - _E4M3_POS[lo], _E4M3_POS[hi] - a
-    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
-    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    a = np.minimum(np.abs(np.nan_to_num(x)), _E4M3_POS[-1])
+    _, e = np.frexp(a)                      # a = f * 2^e, f in [0.5, 1)
+    E = np.maximum(e.astype(np.int64) - 1, -6)
+    q = np.rint(np.ldexp(a, -(E - 3))).astype(np.int64)   # ties to even, like the format
+    code = np.where(a < 2.0 ** -6, q, (E + 7) * 8 + q - 8)
+    code = np.minimum(code, 0x7E).astype(np.uint8)
     code = np.where(np.signbit(x) & (code != 0), code | 0x80, code)
     return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
 
@@ -236,6 +240,29 @@ def make_mask(w: Workload, B: int | None = None, H: int | None = None) -> np.nda
     if w.mask_kind == "ones":
         return mask_ones(B, H, nb)
     raise ValueError(w.mask_kind)
+
+
+STREAM_MASK_IID64 = 12
+
+
+def make_mask_kb64(w: Workload, B: int | None = None, H: int | None = None) -> np.ndarray:
+    """The workload's mask at 64-key granularity, uint8 [B][H][S/128][S/64]:
+    the iid masks drawn afresh per (128-query, 64-key) block with the same
+    density, the two 64-key halves of each diagonal block live; the
+    structured masks (causal, BigBird, dense) with every 128-key entry
+    repeated over its two halves (the same pattern, finer grid)."""
+    B = w.B if B is None else B
+    H = w.H if H is None else H
+    nb = w.nb
+    if w.mask_kind in ("iid50", "iid10"):
+        p = 0.5 if w.mask_kind == "iid50" else 0.1
+        u = uniform(w.mask_seed, STREAM_MASK_IID64, B * H * nb * 2 * nb).reshape(B, H, nb, 2 * nb)
+        m = (u < p).astype(np.uint8)
+        idx = np.arange(nb)
+        m[:, :, idx, 2 * idx] = 1
+        m[:, :, idx, 2 * idx + 1] = 1
+        return m
+    return np.repeat(make_mask(w, B, H), 2, axis=3)
 
 
 def make_qkv(w: Workload, B: int | None = None, H: int | None = None):
