@@ -292,10 +292,11 @@ __device__ __forceinline__ bool wait_warp_idle(uint32_t bar, uint32_t parity,
 // reads (counter, tile order, CSR row pointers, column indices) and the Q
 // load are thus off the producer's and the MMA warp's path.  Ends after
 // publishing the "no tiles left" entry.
-template <int D, bool IN8>
+template <int D, bool IN8, bool KB64>
 __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars* bars,
                               uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D, IN8>;
+  constexpr int kKdiv = KB64 ? 2 : 1;  // 128 / kKdiv keys per key block
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.timeout_ns;
   const int rows = p.n_live + p.n_empty;
@@ -327,12 +328,12 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
       }
       r0 = p.row_ptr[t];
       cnt = p.row_ptr[t + 1] - r0;
-      if (cnt <= 0 || cnt > p.nb * p.kdiv) {
+      if (cnt <= 0 || cnt > p.nb * kKdiv) {
         raise_internal(abort_flag, p.status);
         ok = false;
         break;
       }
-      if (p.kdiv == 1) {
+      if constexpr (!KB64) {
         diag = (p.causal && p.col_idx[r0 + cnt - 1] == t % p.nb) ? 1 : 0;
       } else {
         l0 = cnt >= 2 ? p.col_idx[r0 + cnt - 2] : -1;
@@ -344,7 +345,7 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
       volatile TileInfo* slot = &bars->tq[e];
       slot->t = t;
       slot->r0 = r0;
-      slot->n = p.kdiv == 1 ? cnt : (cnt + 1) / 2;
+      slot->n = KB64 ? (cnt + 1) / 2 : cnt;
       slot->diag = diag;
       slot->n64 = cnt;
       slot->last2[0] = l0;
@@ -415,11 +416,12 @@ __device__ __forceinline__ bool take_tile(Bars* bars, int tqc, const FwdParams& 
 // ring is loaded in its consumption order.  When the K cursor has
 // kClaimAhead blocks of its tile left (or enters a shorter tile) it asks the
 // scheduler for the next tile.
-template <int D, bool IN8>
+template <int D, bool IN8, bool KB64>
 __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                              const CUtensorMap* tm_v, const FwdParams& p, Bars* bars,
                              uint32_t smem_base, volatile int* abort_flag) {
   using C = Cfg<D, IN8>;
+  constexpr int kKdiv = KB64 ? 2 : 1;  // 128 / kKdiv keys per key block
   const int lane = threadIdx.x & 31;
   const uint64_t lim = p.timeout_ns;
   int kc = 0, vc = 0, tqc = 0;  // K / V tiles loaded, tiles taken
@@ -432,7 +434,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
   // key rows of blocks whose K is loaded and V not yet (at most two); with
   // 64-key blocks, the rows of the block's two halves
   int f0 = 0, f1 = 0, g0 = 0, g1 = 0, nf = 0;
-  const bool halves = p.kdiv == 2;
+  constexpr bool halves = KB64;
   constexpr uint32_t kHalfBytes = 64 * 128;  // 64 rows of a 128-byte-row box
 
   // One TMA tile (128 rows x D) into a buffer, completion on `full`, after
@@ -448,7 +450,7 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
       mbar_arrive_expect_tx(full, bytes);
       for (int c = 0; c < nbox; ++c) {
         tma_load_2d(dst + c * box_stride, tm, full, c * 64, row);
-        if (halves) tma_load_2d(dst + c * box_stride + kHalfBytes, tm, full, c * 64, row2);
+        if constexpr (halves) tma_load_2d(dst + c * box_stride + kHalfBytes, tm, full, c * 64, row2);
       }
     }
     __syncwarp();
@@ -483,12 +485,12 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     // whose scores the softmax masks
     int kb2 = kb;
     if (halves && e + 1 < k_n64) kb2 = __shfl_sync(0xffffffffu, k_col, (e + 1) & 31);
-    const int nbk = p.nb * p.kdiv;
+    const int nbk = p.nb * kKdiv;
     if (kb < 0 || kb >= nbk || kb2 < 0 || kb2 >= nbk) {
       raise_internal(abort_flag, p.status);
       return false;
     }
-    const int krows = kBlock / p.kdiv;
+    const int krows = kBlock / kKdiv;
     const int row = k_hrow + kb * krows, row2 = k_hrow + kb2 * krows;
     const int st = kc % C::kKStages;
     if (!load_tile(tm_k, smem_base + C::kKOff + st * C::kQKBytes, C::kBoxBytes,
@@ -805,7 +807,7 @@ __device__ __forceinline__ float row_max64(const uint32_t* sr) {
   return fmaxf(max3(a[0], a[1], a[2]), max3(max3(a[3], a[4], a[5]), a[6], a[7]));
 }
 
-template <int D, bool OUT_F32, bool IN8>
+template <int D, bool OUT_F32, bool IN8, bool KB64>
 __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
                             volatile int* abort_flag) {
   using C = Cfg<D, IN8>;
@@ -866,7 +868,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       const bool diag = diag_last && jb == n - 1;  // warp-uniform
       int klim = diag ? r - 64 * ch : 63;
       bool masked = diag;
-      if (p.kdiv == 2) {
+      if constexpr (KB64) {
         const int e64 = 2 * jb + ch;
         if (e64 >= n64) {
           klim = -1;
@@ -912,7 +914,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       // need not stay in registers past the first pass.
       // A row with no allowed key so far (m = -inf: possible with 64-key
       // blocks under causal) always takes the redo path, with reference 0.
-      bool redo = jb == 0 || (p.kdiv == 2 && __any_sync(0xffffffffu, m == __uint_as_float(kNegInf)));
+      bool redo = jb == 0 || (KB64 && __any_sync(0xffffffffu, m == __uint_as_float(kNegInf)));
       if (!redo) {
         uint32_t sr[64];
         load_scores(sr);
@@ -941,7 +943,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         }
         b2 = 0;
         br32[0] = br32[1] = 0.f;
-        exp_pass(sr, (p.kdiv == 2 && m == __uint_as_float(kNegInf)) ? 0.f : m);
+        exp_pass(sr, (KB64 && m == __uint_as_float(kNegInf)) ? 0.f : m);
       }
       a2 = f2_add(a2, b2);
       r32[0] += br32[0];
@@ -1150,28 +1152,39 @@ __device__ __forceinline__ void convert_v_quarter(uint32_t stage, int wq, int la
 // box of 128-byte rows, 128-byte swizzled as TMA wrote it) converted to the
 // fp16 V tile of the P V product (two 64-column boxes `group` bytes apart,
 // 128-byte swizzled as the MMA's descriptor reads them).  e4m3 converts to
-// fp16 exactly; `rmax` collects the fp16 exponent fields as in
-// convert_v_quarter (an e4m3 NaN becomes an fp16 NaN and is reported).
+// fp16 exactly.  Two 16-byte chunks are loaded at once (their latencies
+// overlap), then each is converted and stored (measured on the e4m3 random
+// 10 % workload: one chunk at a time 1077 TFLOP/s, two 1338, four 1309,
+// eight 1326).  `nan8` collects, per byte,
+// bit 7 set for an e4m3 NaN (0x7F / 0xFF: the 7 low bits all ones, so that
+// adding 1 to them carries into bit 7).
 __device__ __forceinline__ void convert_v8_quarter(uint32_t src, uint32_t dst, uint32_t group,
-                                                   int wq, int lane, uint32_t& rmax) {
-#pragma unroll 1  // one chunk at a time: these warps run with few registers
-  for (int i = 0; i < 8; ++i) {
-    const int idx = wq * 256 + i * 32 + lane;
-    const uint32_t r = (uint32_t)idx >> 3, c = (uint32_t)idx & 7u;  // key row, 16-byte chunk
-    uint32_t w[4];
-    ld_shared_v4(src + r * 128u + ((c ^ (r & 7u)) << 4), w);
-    uint32_t h[8];
+                                                   int wq, int lane, uint32_t& nan8) {
+#pragma unroll 1
+  for (int i0 = 0; i0 < 8; i0 += 2) {
+    uint32_t w[2][4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      e4m3x4_to_f16x4(w[j], h[2 * j], h[2 * j + 1]);
-      rmax = max_u16x2(rmax, h[2 * j] & 0x7C007C00u);
-      rmax = max_u16x2(rmax, h[2 * j + 1] & 0x7C007C00u);
+    for (int j = 0; j < 2; ++j) {
+      const int idx = wq * 256 + (i0 + j) * 32 + lane;
+      const uint32_t r = (uint32_t)idx >> 3, c = (uint32_t)idx & 7u;  // key row, 16-byte chunk
+      ld_shared_v4(src + r * 128u + ((c ^ (r & 7u)) << 4), w[j]);
     }
-    // columns 16c .. 16c+15 -> box c / 4, its 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1
-    const uint32_t box = dst + (c >> 2) * group + r * 128u;
-    const uint32_t j0 = 2u * (c & 3u);
-    st_shared_v4(box + ((j0 ^ (r & 7u)) << 4), h[0], h[1], h[2], h[3]);
-    st_shared_v4(box + (((j0 + 1u) ^ (r & 7u)) << 4), h[4], h[5], h[6], h[7]);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int idx = wq * 256 + (i0 + j) * 32 + lane;
+      const uint32_t r = (uint32_t)idx >> 3, c = (uint32_t)idx & 7u;
+      uint32_t h[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        nan8 |= ((w[j][e] & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u;
+        e4m3x4_to_f16x4(w[j][e], h[2 * e], h[2 * e + 1]);
+      }
+      // columns 16c .. 16c+15 -> box c / 4, its 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1
+      const uint32_t box = dst + (c >> 2) * group + r * 128u;
+      const uint32_t j0 = 2u * (c & 3u);
+      st_shared_v4(box + ((j0 ^ (r & 7u)) << 4), h[0], h[1], h[2], h[3]);
+      st_shared_v4(box + (((j0 + 1u) ^ (r & 7u)) << 4), h[4], h[5], h[6], h[7]);
+    }
   }
 }
 
@@ -1202,14 +1215,15 @@ __device__ void run_epilogue_convert(const FwdParams& p, Bars* bars, uint32_t tm
   int known = 0;  // blocks of the stream in the tiles seen so far
   int cg = 0;     // blocks whose V this warp has converted
   int ntile = 0;  // tiles taken
-  uint32_t rmax = 0;
-  bool ok = true;  // false once a wait of this warp failed
+  uint32_t rmax = 0;  // D = 64: per half, the largest fp16 exponent field converted
+  uint32_t nan8 = 0;  // e4m3: NaN bytes seen
+  bool ok = true;     // false once a wait of this warp failed
   auto convert_next = [&]() {
     const int st = cg % C::kVStages;
     if constexpr (C::kIn8) {
       const int s8 = cg % C::kV8Stages;
       convert_v8_quarter(smem_base + C::kV8Off + s8 * C::kBoxBytes,
-                         smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup, wq, lane, rmax);
+                         smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup, wq, lane, nan8);
       fence_proxy_async_smem();  // the tensor core reads what these generic stores wrote
       __syncwarp();
       if (lane == 0) {
@@ -1320,11 +1334,11 @@ __device__ void run_epilogue_convert(const FwdParams& p, Bars* bars, uint32_t tm
     if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));
   }
   // A V entry that is not finite in fp16 (|v| > 65504, or inf / NaN) was converted.
-  const bool bad = (rmax & 0xFFFFu) == 0x7C00u || (rmax >> 16) == 0x7C00u;
+  const bool bad = (rmax & 0xFFFFu) == 0x7C00u || (rmax >> 16) == 0x7C00u || nan8 != 0u;
   if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.status, kStatusRange);
 }
 
-template <int D, bool OUT_F32, bool IN8>
+template <int D, bool OUT_F32, bool IN8, bool KB64>
 __global__ void __launch_bounds__(kThreads, 1)
     bsattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -1397,7 +1411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp >= kSoftmaxThreads / 32) {
     regs_dec<kRegsOther>();
     if (warp == kWarpLoad)
-      run_producer<D, IN8>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
+      run_producer<D, IN8, KB64>(&tm_q, &tm_k, &tm_v, p, bars, base, abort_flag);
     else if (warp == kWarpMmaS)
       run_mma_s<D, IN8>(p, bars, tmem, base, abort_flag);
     else if (warp == kWarpMmaPV)
@@ -1409,10 +1423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         run_epilogue<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
     }
     else if (warp == kWarpSched)
-      run_scheduler<D, IN8>(&tm_q, p, bars, base, abort_flag);
+      run_scheduler<D, IN8, KB64>(&tm_q, p, bars, base, abort_flag);
   } else {
     regs_inc<kRegsSoftmax>();
-    run_softmax<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
+    run_softmax<D, OUT_F32, IN8, KB64>(p, bars, tmem, abort_flag);
   }
   __syncwarp();  // reconverge each warp before the CTA-wide barrier
 
@@ -1448,7 +1462,7 @@ __global__ void selftest_wait_kernel(unsigned long long timeout_ns, int* status)
   __syncthreads();
 }
 
-template <int D, bool OUT_F32, bool IN8>
+template <int D, bool OUT_F32, bool IN8, bool KB64>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdParams& p, int grid, cudaStream_t stream) {
   const size_t smem = Cfg<D, IN8>::kSmem + 1024;
@@ -1459,12 +1473,12 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices || !opted_in[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32, IN8>,
+    e = cudaFuncSetAttribute(bsattn_fwd_kernel<D, OUT_F32, IN8, KB64>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_fwd_kernel<D, OUT_F32, IN8><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  bsattn_fwd_kernel<D, OUT_F32, IN8, KB64><<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
@@ -1474,20 +1488,30 @@ size_t fwd_smem_bytes(int D) {
   return D == 64 ? Cfg<64>::kSmem + 1024 : Cfg<128>::kSmem + 1024;
 }
 
+// The kernel is compiled per head_dim, output type, input type and key-block
+// size (64-key blocks add per-block work to the softmax and the producer that
+// 128-key plans should not pay).
+template <int D, bool IN8, bool KB64>
+cudaError_t launch_out(bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream) {
+  return out_f32 ? launch_one<D, true, IN8, KB64>(tq, tk, tv, p, grid, stream)
+                 : launch_one<D, false, IN8, KB64>(tq, tk, tv, p, grid, stream);
+}
+
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream,
                        bool in8) {
+  const bool kb64 = p.kdiv == 2;
   if (in8) {
     if (D != 128) return cudaErrorInvalidValue;
-    return out_f32 ? launch_one<128, true, true>(tq, tk, tv, p, grid, stream)
-                   : launch_one<128, false, true>(tq, tk, tv, p, grid, stream);
+    return kb64 ? launch_out<128, true, true>(out_f32, tq, tk, tv, p, grid, stream)
+                : launch_out<128, true, false>(out_f32, tq, tk, tv, p, grid, stream);
   }
-  if (D == 64) {
-    return out_f32 ? launch_one<64, true, false>(tq, tk, tv, p, grid, stream)
-                   : launch_one<64, false, false>(tq, tk, tv, p, grid, stream);
-  }
-  return out_f32 ? launch_one<128, true, false>(tq, tk, tv, p, grid, stream)
-                 : launch_one<128, false, false>(tq, tk, tv, p, grid, stream);
+  if (D == 64)
+    return kb64 ? launch_out<64, false, true>(out_f32, tq, tk, tv, p, grid, stream)
+                : launch_out<64, false, false>(out_f32, tq, tk, tv, p, grid, stream);
+  return kb64 ? launch_out<128, false, true>(out_f32, tq, tk, tv, p, grid, stream)
+              : launch_out<128, false, false>(out_f32, tq, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
