@@ -19,24 +19,30 @@
 // either were measured to bound the whole pass by L2 atomic throughput).
 //
 // bsattn_bwd_kernel (dK, dV): one CTA per key tile (128 keys of one (batch,
-// head)), 256 threads: two warps per TMEM sub-partition, each thread one key
-// row (TMEM lane) and half of the columns.  It walks the plan's transposed
-// list (the live query blocks of its key block) and keeps dV and dK in tensor
-// memory.  Per query block, with keys as TMEM lanes:
-//   S^T = K Q^T, dP^T = V dO^T                         (tcgen05, operands in smem)
+// head)), 288 threads: eight CUDA-core warps (two per TMEM sub-partition,
+// warps 4h .. 4h+3 working on half h of each query block: queries 64h ..
+// 64h+63) and one copy / MMA warp.  It walks the plan's transposed list (the
+// live query blocks of its key block) and keeps dV and dK in tensor memory.
+// Per query block and half h, with keys as TMEM lanes:
+//   S^T_h = K Q_h^T, dP^T_h = V dO_h^T                 (tcgen05, N = 64, operands in smem)
 //   P^T = 2^(S^T scale log2 e - LSE log2 e), dS^T = P^T (dP^T - Dl)   (CUDA cores)
-//   P^T (bf16) goes back to tensor memory over S^T (queries 0-63 at columns
-//   0-31, 64-127 at 64-95: each half writes inside the scores it read);
+//   P^T (bf16) goes back to tensor memory over S^T_h (queries 64h + 2c,
+//   64h + 2c + 1 in column 64h + c: each half writes inside the scores it read);
 //   dS^T (bf16) goes to shared memory
-//   dV += P^T dO   (A from tensor memory, B = dO read MN-major)
-//   dK += dS^T Q   (A = dS^T, B = Q read MN-major)
-// Q and dO are double-buffered: the next query block's tiles load while the
-// current one is processed.
+//   dV += P^T_h dO_h   (A from tensor memory, B = dO read MN-major, K = 64)
+//   dK += dS^T_h Q_h   (A = dS^T, B = Q read MN-major, K = 64)
+// Each step has a barrier per half, so the CUDA cores work on one half while
+// the tensor core computes the other half's products: half 0's P^T / dS^T
+// overlaps S^T_1 and dP^T_1, half 1's overlaps dV, dK of half 0 and the next
+// block's S^T_0, dP^T_0.  Q and dO are double-buffered: the next query
+// block's tiles load once the previous block's products are done with them.
 //
 // bsattn_bwd_dq_kernel (dQ): one CTA per query tile, walking the forward
 // plan's list of live key blocks with queries as TMEM lanes: S = Q K^T and
 // dP = dO V^T recomputed, dS = P (dP - Dl) to shared memory, dQ += dS K in
-// tensor memory (K and V double-buffered), dQ written once at the end.
+// tensor memory (K and V double-buffered), dQ written once at the end; the
+// same 288 threads and per-half pipeline as the dK/dV kernel, halves of the
+// key block (keys 64h .. 64h+63) instead of the query block.
 //
 // Every mbarrier wait is bounded; on expiry the status word records a
 // timeout and the CTA drains its copies and MMAs before it frees tensor memory.
@@ -49,7 +55,6 @@
 namespace bsattn {
 namespace {
 
-constexpr int kBwdThreads = 256;
 constexpr uint32_t kBwdTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634074f;
 constexpr int kMaxKvGroup = 64;  // query heads per K/V head the dK/dV kernel walks
@@ -64,12 +69,12 @@ struct BwdCfg {
   static constexpr int kQOff = kVOff + kTileBytes;     // two buffers
   static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // two buffers
   static constexpr int kdSOff = kdOOff + 2 * kTileBytes;  // 128 x 128 bf16: two boxes
-  static constexpr int kVecOff = kdSOff + 2 * kBoxBytes;  // LSE log2 e [128], Dl [128]
-  static constexpr int kBarOff = kVecOff + 2 * kBlock * 4;
+  static constexpr int kBarOff = kdSOff + 2 * kBoxBytes;
   static constexpr int kGrpOff = kBarOff + 128;  // per query head of the group: list start, prefix
   static constexpr int kSmem = kGrpOff + 4 * (2 * kMaxKvGroup + 1) + 124;
-  // S^T = K Q^T and dP^T = V dO^T: M = 128 keys, N = 128 queries, both K-major
-  static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 128, false);
+  // S^T = K Q^T and dP^T = V dO^T, per half of the query block: M = 128 keys,
+  // N = 64 queries, both K-major
+  static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 64, false);
   // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, B MN-major
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, true);
   // tensor-memory columns
@@ -81,16 +86,21 @@ struct BwdCfg {
 static_assert(BwdCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(BwdCfg<128>::kTdK + 128 <= kBwdTmemCols, "tensor memory exceeded");
 
+// The dK/dV kernel works on each query block in two halves h (queries
+// 64h .. 64h+63), with a barrier per half for every step, so that one half's
+// CUDA-core work overlaps the tensor core's work on the other half.
 struct __align__(8) BwdBars {
   uint64_t kv_full;      // K and V of the key tile loaded
   uint64_t qd_full[2];   // Q and dO of a query block loaded (by buffer)
-  uint64_t st_done;      // S^T and dP^T computed
-  uint64_t grad_done;    // dV and dK updated
+  uint64_t st_done[2];   // S^T and dP^T of half h computed
+  uint64_t pds_done[2];  // P^T (tensor memory) and dS^T (shared memory) of half h written
+  uint64_t grad_done[2]; // dV and dK updated with half h
   uint64_t drain;        // every MMA issued so far complete
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(BwdBars) <= 128, "barrier block must fit its 128-byte region");
+constexpr int kBwdKvThreads = 288;  // dK/dV kernel: 8 CUDA-core warps and an MMA / copy warp
 
 // Dl_i = dO_i . O_i (fp32 over the stored O and dO); one warp per row.
 template <int D, bool O_F32>
@@ -136,7 +146,7 @@ __device__ __forceinline__ void bwd_drain_wait(uint32_t bar, uint32_t parity, ui
 }
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdKvThreads, 1)
     bsattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v,
@@ -144,6 +154,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = BwdCfg<D>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kMmaWarp = 8;   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3
   const int tile = blockIdx.x;  // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk
   const int kvbh = tile / p.nb;
   const int kb = tile - kvbh * p.nb;
@@ -182,7 +194,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (n <= 0) {  // no live query block: dK = dV = 0
     float4* dk4 = reinterpret_cast<float4*>(p.dk + (size_t)krow0 * D);
     float4* dv4 = reinterpret_cast<float4*>(p.dv + (size_t)krow0 * D);
-    for (int i = tid; i < kBlock * D / 4; i += kBwdThreads) {
+    for (int i = tid; i < kBlock * D / 4; i += kBwdKvThreads) {
       dk4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       dv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -191,7 +203,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // The plan's lists must hold valid query blocks; anything else is an internal error.
   bool bad = n > p.nb * g;
   for (int gi = 0; !bad && gi < g; ++gi) bad = g_st[gi + 1] - g_st[gi] > p.nb;
-  for (int i = tid; !bad && i < n; i += kBwdThreads) {
+  for (int i = tid; !bad && i < n; i += kBwdKvThreads) {
     int bhq = 0, qb = 0;
     entry(i, bhq, qb);
     bad = qb < 0 || qb >= p.nb || (p.causal && qb < kb);
@@ -202,17 +214,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
 
   BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw + (base - raw) + C::kBarOff);
-  float* sL = reinterpret_cast<float*>(smem_raw + (base - raw) + C::kVecOff);  // LSE log2 e
-  float* sD = sL + kBlock;                                                     // Dl
   const uint64_t lim = p.timeout_ns;
   volatile int* abort_flag = &bars->abort_flag;
 
   if (tid == 0) {
     mbar_init(smem_u32(&bars->kv_full), 1);
-    mbar_init(smem_u32(&bars->qd_full[0]), 1);
-    mbar_init(smem_u32(&bars->qd_full[1]), 1);
-    mbar_init(smem_u32(&bars->st_done), 1);
-    mbar_init(smem_u32(&bars->grad_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->qd_full[i]), 1);
+      mbar_init(smem_u32(&bars->st_done[i]), 1);
+      mbar_init(smem_u32(&bars->pds_done[i]), 4);  // the half's four warps
+      mbar_init(smem_u32(&bars->grad_done[i]), 1);
+    }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -229,138 +241,175 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
-  const int r = tid & (kBlock - 1);  // TMEM lane: key row
-  const int half = tid >> 7;         // which half of the columns this thread handles
-
-  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
-#pragma unroll
-    for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
-  };
-  // Q and dO of query block number i of the list into buffer i % 2 (thread 0).
-  auto load_qd = [&](int i) {
-    const int b = i & 1;
-    const uint32_t bar = smem_u32(&bars->qd_full[b]);
-    int bhq = 0, qbi = 0;
-    entry(i, bhq, qbi);
-    const int row = bhq * p.S + qbi * kBlock;
-    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-    load_tile(&tm_q, base + C::kQOff + b * C::kTileBytes, bar, row);
-    load_tile(&tm_do, base + C::kdOOff + b * C::kTileBytes, bar, row);
-  };
-
-  int n_issued = 0, n_waited = 0;  // (thread 0 / warp 0) Q-dO loads issued and awaited
-  bool kv_waited = false;
-  if (tid == 0) {
-    const uint32_t bar = smem_u32(&bars->kv_full);
-    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-    load_tile(&tm_k, base + C::kKOff, bar, krow0);
-    load_tile(&tm_v, base + C::kVOff, bar, krow0);
-    load_qd(0);
-  }
-  n_issued = 1;
-  // LSE (log2 units) and Dl of the next query block, one row per thread of
-  // the first half
-  float lse_next = 0.f, dl_next = 0.f;
-  if (half == 0) {
-    int bhq = 0, qbi = 0;
-    entry(0, bhq, qbi);
-    const int qrow = bhq * p.S + qbi * kBlock + r;
-    lse_next = p.lse[qrow] * kLog2e;
-    dl_next = p.dl[qrow];
-  }
-
   bool ok = true;
-  for (int j = 0; j < n; ++j) {
-    int bhj = 0, qb = 0;  // (the head only matters for the rows loaded ahead)
-    entry(j, bhj, qb);
-    const int b = j & 1;
-    if (half == 0) {
-      sL[r] = lse_next;
-      sD[r] = dl_next;
-    }
-    if (j + 1 < n) {
-      // the other buffer was last read by the previous block's MMAs, which are complete
-      if (tid == 0) load_qd(j + 1);
-      n_issued = j + 2;
-      if (half == 0) {
-        int bhq = 0, qbi = 0;
-        entry(j + 1, bhq, qbi);
-        const int qrow = bhq * p.S + qbi * kBlock + r;
-        lse_next = p.lse[qrow] * kLog2e;
-        dl_next = p.dl[qrow];
-      }
-    }
-    __syncthreads();  // sL, sD written
 
-    // S^T = K Q^T and dP^T = V dO^T (keys are the TMEM lanes)
-    if (warp == 0) {
-      bool w = kv_waited || bwd_wait(smem_u32(&bars->kv_full), 0, abort_flag, p.status, lim);
-      kv_waited = kv_waited || w;
-      w = w && bwd_wait(smem_u32(&bars->qd_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
-                        lim);
-      if (w) {
-        n_waited = j + 1;
+  if (warp == kMmaWarp) {
+    // ---- copies and MMAs (elected lane): per block j, for each half h,
+    // S^T_h = K Q_h^T and dP^T_h = V dO_h^T once the half's buffers are free
+    // (dV, dK of the previous block's half h complete), then, once the CUDA
+    // cores have written P^T_h and dS^T_h, dV += P^T_h dO_h and dK += dS^T_h Q_h.
+    auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+    };
+    auto load_qd = [&](int i) {  // Q and dO of entry i into buffer i % 2
+      const int b = i & 1;
+      const uint32_t bar = smem_u32(&bars->qd_full[b]);
+      int bhq = 0, qbi = 0;
+      entry(i, bhq, qbi);
+      const int row = bhq * p.S + qbi * kBlock;
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      load_tile(&tm_q, base + C::kQOff + b * C::kTileBytes, bar, row);
+      load_tile(&tm_do, base + C::kdOOff + b * C::kTileBytes, bar, row);
+    };
+    int n_issued = 0, n_waited = 0;  // Q-dO loads issued / awaited
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&bars->kv_full);
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      load_tile(&tm_k, base + C::kKOff, bar, krow0);
+      load_tile(&tm_v, base + C::kVOff, bar, krow0);
+      load_qd(0);
+      if (n > 1) load_qd(1);
+    }
+    __syncwarp();
+    n_issued = n > 1 ? 2 : 1;
+    ok = bwd_wait(smem_u32(&bars->kv_full), 0, abort_flag, p.status, lim);
+    const bool kv_ok = ok;
+    const uint64_t kd = smem_desc_sw128(base + C::kKOff, 16, 1024);
+    const uint64_t vd = smem_desc_sw128(base + C::kVOff, 16, 1024);
+    const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
+    for (int j = 0; ok && j < n; ++j) {
+      const int b = j & 1;
+      ok = bwd_wait(smem_u32(&bars->qd_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
+                    lim);
+      if (!ok) break;
+      n_waited = j + 1;
+      for (int h = 0; ok && h < 2; ++h) {
+        if (j > 0) {  // half h of the previous block multiplied: its columns and dS^T free
+          ok = bwd_wait(smem_u32(&bars->grad_done[h]), (uint32_t)(j - 1) & 1u, abort_flag,
+                        p.status, lim);
+          if (!ok) break;
+          if (h == 1 && j + 1 < n) {  // the previous block's buffers are free: next Q, dO
+            if (elect_one()) load_qd(j + 1);
+            __syncwarp();
+            n_issued = j + 2;
+          }
+        }
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t kd = smem_desc_sw128(base + C::kKOff, 16, 1024);
-          const uint64_t vd = smem_desc_sw128(base + C::kVOff, 16, 1024);
-          const uint64_t qd = smem_desc_sw128(base + C::kQOff + b * C::kTileBytes, 16, 1024);
-          const uint64_t dd = smem_desc_sw128(base + C::kdOOff + b * C::kTileBytes, 16, 1024);
+          // queries 64h .. 64h+63: rows 64h.. of the Q and dO tiles (8 KB into each box)
+          const uint32_t rows_h = (uint32_t)h * 64u * 128u;
+          const uint64_t qd = smem_desc_sw128(base + C::kQOff + b * C::kTileBytes + rows_h, 16, 1024);
+          const uint64_t dd = smem_desc_sw128(base + C::kdOOff + b * C::kTileBytes + rows_h, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTS, kd + off, qd + off, C::kIdescT, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kTS + 64u * h, kd + off, qd + off, C::kIdescT, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTdP, vd + off, dd + off, C::kIdescT, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kTdP + 64u * h, vd + off, dd + off, C::kIdescT, kk > 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&bars->st_done));
+          mma_commit(smem_u32(&bars->st_done[h]));
         }
         __syncwarp();
       }
-      ok = w;
+      for (int h = 0; ok && h < 2; ++h) {
+        ok = bwd_wait(smem_u32(&bars->pds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint32_t qoff = base + C::kQOff + b * C::kTileBytes;
+          const uint32_t dooff = base + C::kdOOff + b * C::kTileBytes;
+          const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
+          const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * h + k4;                       // queries 16kk .. 16kk+15
+            const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
+            const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            const uint32_t pcol = 64u * h + 8u * k4;  // P^T of queries 16kk .. in bf16 pairs
+            mma_ts(tmem + C::kTdV, tmem + C::kTS + pcol, do_mn + mn, C::kIdescKV, acc);
+            mma_ss(tmem + C::kTdK, ds_k + km, q_mn + mn, C::kIdescKV, acc);
+          }
+          mma_commit(smem_u32(&bars->grad_done[h]));
+        }
+        __syncwarp();
+      }
     }
-    if (ok) ok = bwd_wait(smem_u32(&bars->st_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-
-    // P^T and dS^T, one key row (TMEM lane) and 64 queries per thread, 32 at
-    // a time.  P^T (bf16 pairs) goes over the scores this thread's half has
-    // already read: queries 64h + 2c, 64h + 2c + 1 in column 64h + c.  dS^T
-    // (bf16) goes to shared memory, 128-byte swizzled like a TMA tile: row r,
-    // 16-byte chunk c of 64-query box x at x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16).
-    {
+    // Drain: every copy issued and every MMA issued completes before tensor
+    // memory is freed and the CTA exits.
+    if (!kv_ok) bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
+    for (int i = n_waited; i < n_issued; ++i)
+      bwd_drain_wait(smem_u32(&bars->qd_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+    if (elect_one()) mma_commit(smem_u32(&bars->drain));
+    __syncwarp();
+    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
+  } else {
+    // ---- P^T and dS^T of half h (queries 64h .. 64h+63), one key row (TMEM
+    // lane) per thread, 32 queries at a time.  P^T (bf16 pairs) goes over
+    // the scores just read: queries 64h + 2c, 64h + 2c + 1 in column 64h + c.
+    // dS^T (bf16) goes to shared memory, 128-byte swizzled like a TMA tile:
+    // row r, 16-byte chunk c of 64-query box h at h * 16 KB + r * 128 +
+    // ((c ^ (r mod 8)) * 16).
+    const int h = warp >> 2;
+    const int r = tid & (kBlock - 1);  // TMEM lane: key row
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
+    const float sl = p.scale_log2;
+    const uint32_t tS = tmem + C::kTS + lane_off;
+    const uint32_t tdP = tmem + C::kTdP + lane_off;
+    const uint32_t sdS = base + C::kdSOff;
+    // LSE (log2 units) and Dl of the half's queries 64h + lane and 64h + 32 +
+    // lane of entry j, loaded one entry ahead by every warp for itself and
+    // passed between lanes by shuffles (no barrier between the warps)
+    float la_next = 0.f, lb_next = 0.f, da_next = 0.f, db_next = 0.f;
+    auto fetch = [&](int i) {
+      int bhq = 0, qbi = 0;
+      entry(i, bhq, qbi);
+      const int qrow = bhq * p.S + qbi * kBlock + 64 * h + lane;
+      la_next = p.lse[qrow] * kLog2e;
+      lb_next = p.lse[qrow + 32] * kLog2e;
+      da_next = p.dl[qrow];
+      db_next = p.dl[qrow + 32];
+    };
+    fetch(0);
+    for (int j = 0; j < n; ++j) {
+      int bhj = 0, qb = 0;
+      entry(j, bhj, qb);
+      const float la = la_next, lb = lb_next, da = da_next, db = db_next;
+      if (j + 1 < n) fetch(j + 1);
+      ok = bwd_wait(smem_u32(&bars->st_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
+      if (!ok) break;
+      tc_fence_after();
       const bool diag = p.causal && qb == kb;  // key r is allowed for query q iff r <= q
-      const float sl = p.scale_log2;
-      const uint32_t tS = tmem + C::kTS + lane_off;
-      const uint32_t tdP = tmem + C::kTdP + lane_off;
-      const uint32_t sdS = base + C::kdSOff;
 #pragma unroll 1
-      for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tS + ch * 32, s);
+      for (int ch = 2 * h; ch < 2 * h + 2; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS + ch * 32, sv);
         tmem_ld32(tdP + ch * 32, dp);
         tmem_wait_ld();
-        reg_fence(s, 32);
+        reg_fence(sv, 32);
         reg_fence(dp, 32);
+        const float lsrc = (ch & 1) ? lb : la;  // queries 64h + 32 (ch & 1) + lane
+        const float dsrc = (ch & 1) ? db : da;
         uint32_t pk[16], dk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const int q = ch * 32 + i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(s[i]), sl, -sL[q]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(s[i + 1]), sl, -sL[q + 1]));
+          const float l0 = __shfl_sync(0xffffffffu, lsrc, i);
+          const float l1 = __shfl_sync(0xffffffffu, lsrc, i + 1);
+          const float d0l = __shfl_sync(0xffffffffu, dsrc, i);
+          const float d1l = __shfl_sync(0xffffffffu, dsrc, i + 1);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l0));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l1));
           if (diag) {
             p0 = r > q ? 0.f : p0;
             p1 = r > q + 1 ? 0.f : p1;
           }
-          const float d0 = p0 * (__uint_as_float(dp[i]) - sD[q]);
-          const float d1 = p1 * (__uint_as_float(dp[i + 1]) - sD[q + 1]);
+          const float d0 = p0 * (__uint_as_float(dp[i]) - d0l);
+          const float d1 = p1 * (__uint_as_float(dp[i + 1]) - d1l);
           pk[i >> 1] = pack_bf16x2(p0, p1);
           dk[i >> 1] = pack_bf16x2(d0, d1);
         }
@@ -376,55 +425,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
+      __syncwarp();  // the warp's P^T and dS^T are written
+      if (lane == 0) mbar_arrive(smem_u32(&bars->pds_done[h]));
     }
-    __syncthreads();  // P^T in tensor memory, dS^T in shared memory
-
-    // dV += P^T dO, dK += dS^T Q (K = 128 queries)
-    if (warp == 0) {
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t qoff = base + C::kQOff + b * C::kTileBytes;
-        const uint32_t dooff = base + C::kdOOff + b * C::kTileBytes;
-        const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
-        const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
-        const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
-          const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-          const uint32_t pcol = (kk < 4) ? kk * 8 : 64 + (kk - 4) * 8;  // queries 16kk ..
-          mma_ts(tmem + C::kTdV, tmem + C::kTS + pcol, do_mn + mn, C::kIdescKV, acc);
-          mma_ss(tmem + C::kTdK, ds_k + km, q_mn + mn, C::kIdescKV, acc);
-        }
-        mma_commit(smem_u32(&bars->grad_done));
-      }
-      __syncwarp();
-    }
-    ok = bwd_wait(smem_u32(&bars->grad_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-
-    tc_fence_before();
-    __syncthreads();  // S^T / dP^T columns and sL / sD free for the next block
   }
-
-  // Drain: every copy issued and every MMA issued completes before tensor
-  // memory is freed and the CTA exits.
-  if (warp == 0) {
-    if (!kv_waited) bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
-    for (int i = n_waited; i < n_issued; ++i)
-      bwd_drain_wait(smem_u32(&bars->qd_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
-    if (elect_one()) mma_commit(smem_u32(&bars->drain));
-    __syncwarp();
-    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
-  }
-  __syncthreads();
+  // Every role has left its loop; the MMA warp drained all copies and MMAs.
+  const bool all_ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (ok) {  // dV and dK (times scale), one key row and half of the columns per thread
+  if (all_ok && warp < kMmaWarp) {  // dV and dK (times scale), one key row and half the columns
+    const int r = tid & (kBlock - 1);
+    const int half = warp >> 2;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float* dvr = p.dv + (size_t)(krow0 + r) * D;
     float* dkr = p.dk + (size_t)(krow0 + r) * D;
 #pragma unroll 1
@@ -467,8 +478,9 @@ struct DqCfg {
   static constexpr int kdSOff = 6 * kTileBytes;  // 128 queries x 128 keys bf16: two boxes
   static constexpr int kBarOff = kdSOff + 2 * kBoxBytes;
   static constexpr int kSmem = kBarOff + 256;
-  // S = Q K^T and dP = dO V^T: M = 128 queries, N = 128 keys, both K-major
-  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false);
+  // S = Q K^T and dP = dO V^T, per half of the key block: M = 128 queries,
+  // N = 64 keys, both K-major
+  static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);
   // dQ += dS K: M = 128 queries, N = D, B (K) read MN-major
   static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true);
   static constexpr uint32_t kTS = 0;     // S (fp32)
@@ -477,18 +489,22 @@ struct DqCfg {
 };
 static_assert(DqCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 
+// The dQ kernel works on each key block in two halves h (keys 64h .. 64h+63)
+// with a barrier per half for every step, as the dK/dV kernel does.
 struct __align__(8) DqBars {
-  uint64_t qd_full;     // Q and dO of the tile loaded
-  uint64_t kv_full[2];  // K and V of a key block loaded (by buffer)
-  uint64_t st_done;     // S and dP computed
-  uint64_t grad_done;   // dQ updated
-  uint64_t drain;       // every MMA issued so far complete
+  uint64_t qd_full;      // Q and dO of the tile loaded
+  uint64_t kv_full[2];   // K and V of a key block loaded (by buffer)
+  uint64_t st_done[2];   // S and dP of half h computed
+  uint64_t ds_done[2];   // dS of half h written
+  uint64_t grad_done[2]; // dQ updated with half h
+  uint64_t drain;        // every MMA issued so far complete
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(DqBars) <= 256, "barrier block must fit its 256-byte region");
 
 template <int D>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(kBwdKvThreads, 1)
     bsattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                          const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v,
@@ -496,6 +512,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   using C = DqCfg<D>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+  const int lane = tid & 31;
+  constexpr int kMmaWarp = 8;   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3
   const int tile = blockIdx.x;  // (b * H + h) * nb + qb
   const int bh = tile / p.nb;
   const int qb = tile - bh * p.nb;
@@ -506,11 +524,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       p.kv_group > 1 ? (bh / p.H) * (p.H / p.kv_group) + (bh % p.H) / p.kv_group : bh;
   if (n <= 0) {  // no live key block: dQ = 0
     float4* dq4 = reinterpret_cast<float4*>(p.dq + (size_t)qrow0 * D);
-    for (int i = tid; i < kBlock * D / 4; i += kBwdThreads) dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = tid; i < kBlock * D / 4; i += kBwdKvThreads)
+      dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
   bool bad = n > p.nb;
-  for (int i = tid; !bad && i < n; i += kBwdThreads) {
+  for (int i = tid; !bad && i < n; i += kBwdKvThreads) {
     const int kb = p.col_idx[r0 + i];
     bad = kb < 0 || kb >= p.nb || (p.causal && kb > qb);
   }
@@ -527,10 +546,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
   if (tid == 0) {
     mbar_init(smem_u32(&bars->qd_full), 1);
-    mbar_init(smem_u32(&bars->kv_full[0]), 1);
-    mbar_init(smem_u32(&bars->kv_full[1]), 1);
-    mbar_init(smem_u32(&bars->st_done), 1);
-    mbar_init(smem_u32(&bars->grad_done), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->kv_full[i]), 1);
+      mbar_init(smem_u32(&bars->st_done[i]), 1);
+      mbar_init(smem_u32(&bars->ds_done[i]), 4);  // the half's four warps
+      mbar_init(smem_u32(&bars->grad_done[i]), 1);
+    }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
     fence_mbar_init();
@@ -547,91 +568,124 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
-  const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-  const int r = tid & (kBlock - 1);  // TMEM lane: query row
-  const int half = tid >> 7;         // which half of the key (or output) columns
-  const float l2 = p.lse[qrow0 + r] * kLog2e;  // this row's LSE in log2 units
-  const float dlr = p.dl[qrow0 + r];
-
-  auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
-#pragma unroll
-    for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
-  };
-  auto load_kv = [&](int i) {  // K and V of key block number i into buffer i % 2 (thread 0)
-    const int b = i & 1;
-    const uint32_t bar = smem_u32(&bars->kv_full[b]);
-    const int row = kvbh * p.S + p.col_idx[r0 + i] * kBlock;
-    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-    load_tile(&tm_k, base + C::kKOff + b * C::kTileBytes, bar, row);
-    load_tile(&tm_v, base + C::kVOff + b * C::kTileBytes, bar, row);
-  };
-  if (tid == 0) {
-    const uint32_t bar = smem_u32(&bars->qd_full);
-    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-    load_tile(&tm_q, base + C::kQOff, bar, qrow0);
-    load_tile(&tm_do, base + C::kdOOff, bar, qrow0);
-    load_kv(0);
-  }
-  int n_issued = 1, n_waited = 0;
-  bool qd_waited = false;
-
   bool ok = true;
-  for (int j = 0; j < n; ++j) {
-    const int kb = p.col_idx[r0 + j];
-    const int b = j & 1;
-    if (j + 1 < n) {
-      // the other buffer was last read by the previous block's MMAs, which are complete
-      if (tid == 0) load_kv(j + 1);
-      n_issued = j + 2;
+
+  if (warp == kMmaWarp) {
+    // ---- copies and MMAs (elected lane): per key block j, for each half h,
+    // S_h = Q K_h^T and dP_h = dO V_h^T once the half's columns and dS are
+    // free (dQ of the previous block's half h complete), then, once the CUDA
+    // cores have written dS_h, dQ += dS_h K_h.
+    auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+    };
+    auto load_kv = [&](int i) {  // K and V of key block number i into buffer i % 2
+      const int b = i & 1;
+      const uint32_t bar = smem_u32(&bars->kv_full[b]);
+      const int row = kvbh * p.S + p.col_idx[r0 + i] * kBlock;
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      load_tile(&tm_k, base + C::kKOff + b * C::kTileBytes, bar, row);
+      load_tile(&tm_v, base + C::kVOff + b * C::kTileBytes, bar, row);
+    };
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&bars->qd_full);
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      load_tile(&tm_q, base + C::kQOff, bar, qrow0);
+      load_tile(&tm_do, base + C::kdOOff, bar, qrow0);
+      load_kv(0);
+      if (n > 1) load_kv(1);
     }
-    // S = Q K^T and dP = dO V^T (queries are the TMEM lanes)
-    if (warp == 0) {
-      bool w = qd_waited || bwd_wait(smem_u32(&bars->qd_full), 0, abort_flag, p.status, lim);
-      qd_waited = qd_waited || w;
-      w = w && bwd_wait(smem_u32(&bars->kv_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
-                        lim);
-      if (w) {
-        n_waited = j + 1;
+    __syncwarp();
+    int n_issued = n > 1 ? 2 : 1, n_waited = 0;
+    ok = bwd_wait(smem_u32(&bars->qd_full), 0, abort_flag, p.status, lim);
+    const bool qd_ok = ok;
+    const uint64_t qd = smem_desc_sw128(base + C::kQOff, 16, 1024);
+    const uint64_t dd = smem_desc_sw128(base + C::kdOOff, 16, 1024);
+    const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
+    for (int j = 0; ok && j < n; ++j) {
+      const int b = j & 1;
+      ok = bwd_wait(smem_u32(&bars->kv_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
+                    lim);
+      if (!ok) break;
+      n_waited = j + 1;
+      for (int h = 0; ok && h < 2; ++h) {
+        if (j > 0) {  // half h of the previous block multiplied: its columns and dS free
+          ok = bwd_wait(smem_u32(&bars->grad_done[h]), (uint32_t)(j - 1) & 1u, abort_flag,
+                        p.status, lim);
+          if (!ok) break;
+          if (h == 1 && j + 1 < n) {  // the previous block's K, V are free: next K, V
+            if (elect_one()) load_kv(j + 1);
+            __syncwarp();
+            n_issued = j + 2;
+          }
+        }
         tc_fence_after();
         if (elect_one()) {
-          const uint64_t qd = smem_desc_sw128(base + C::kQOff, 16, 1024);
-          const uint64_t dd = smem_desc_sw128(base + C::kdOOff, 16, 1024);
-          const uint64_t kd = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, 16, 1024);
-          const uint64_t vd = smem_desc_sw128(base + C::kVOff + b * C::kTileBytes, 16, 1024);
+          // keys 64h .. 64h+63: rows 64h.. of the K and V tiles (8 KB into each box)
+          const uint32_t rows_h = (uint32_t)h * 64u * 128u;
+          const uint64_t kd = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes + rows_h, 16, 1024);
+          const uint64_t vd = smem_desc_sw128(base + C::kVOff + b * C::kTileBytes + rows_h, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTS, qd + off, kd + off, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kTS + 64u * h, qd + off, kd + off, C::kIdescS, kk > 0 ? 1u : 0u);
           }
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTdP, dd + off, vd + off, C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_ss(tmem + C::kTdP + 64u * h, dd + off, vd + off, C::kIdescS, kk > 0 ? 1u : 0u);
           }
-          mma_commit(smem_u32(&bars->st_done));
+          mma_commit(smem_u32(&bars->st_done[h]));
         }
         __syncwarp();
       }
-      ok = w;
+      for (int h = 0; ok && h < 2; ++h) {
+        ok = bwd_wait(smem_u32(&bars->ds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
+        if (!ok) break;
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t k_mn = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, C::kBoxBytes,
+                                                1024);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * h + k4;  // keys 16kk .. 16kk+15
+            const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
+            mma_ss(tmem + C::kTdQ, ds_k + km, k_mn + mn, C::kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->grad_done[h]));
+        }
+        __syncwarp();
+      }
     }
-    if (ok) ok = bwd_wait(smem_u32(&bars->st_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-
-    // dS = P (dP - Dl), one query row and 64 keys per thread, 32 at a time, to
-    // shared memory (bf16, 128-byte swizzled: row r, 16-byte chunk c of
-    // 64-key box x at x * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16)).
-    {
+    // Drain copies and MMAs in flight.
+    if (!qd_ok) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
+    for (int i = n_waited; i < n_issued; ++i)
+      bwd_drain_wait(smem_u32(&bars->kv_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+    if (elect_one()) mma_commit(smem_u32(&bars->drain));
+    __syncwarp();
+    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
+  } else {
+    // ---- dS = P (dP - Dl) of half h (keys 64h .. 64h+63), one query row and
+    // 32 keys at a time, to shared memory (bf16, 128-byte swizzled: row r,
+    // 16-byte chunk c of 64-key box h at h * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16)).
+    const int h = warp >> 2;
+    const int r = tid & (kBlock - 1);  // TMEM lane: query row
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float l2 = p.lse[qrow0 + r] * kLog2e;  // this row's LSE in log2 units
+    const float dlr = p.dl[qrow0 + r];
+    const float sl = p.scale_log2;
+    const uint32_t tS = tmem + C::kTS + lane_off;
+    const uint32_t tdP = tmem + C::kTdP + lane_off;
+    const uint32_t sdS = base + C::kdSOff;
+    for (int j = 0; j < n; ++j) {
+      const int kb = p.col_idx[r0 + j];
+      ok = bwd_wait(smem_u32(&bars->st_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
+      if (!ok) break;
+      tc_fence_after();
       const bool diag = p.causal && kb == qb;  // key c is allowed for query r iff c <= r
-      const float sl = p.scale_log2;
-      const uint32_t tS = tmem + C::kTS + lane_off;
-      const uint32_t tdP = tmem + C::kTdP + lane_off;
-      const uint32_t sdS = base + C::kdSOff;
 #pragma unroll 1
-      for (int ch = 2 * half; ch < 2 * half + 2; ++ch) {
+      for (int ch = 2 * h; ch < 2 * h + 2; ++ch) {
         uint32_t sv[32], dp[32];
         tmem_ld32(tS + ch * 32, sv);
         tmem_ld32(tdP + ch * 32, dp);
@@ -661,44 +715,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-    }
-    __syncthreads();  // dS in shared memory
-
-    // dQ += dS K (K = 128 keys)
-    if (warp == 0) {
-      tc_fence_after();
-      if (elect_one()) {
-        const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
-        const uint64_t k_mn = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, C::kBoxBytes,
-                                              1024);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
-          mma_ss(tmem + C::kTdQ, ds_k + km, k_mn + mn, C::kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(smem_u32(&bars->grad_done));
-      }
-      __syncwarp();
-    }
-    ok = bwd_wait(smem_u32(&bars->grad_done), (uint32_t)j & 1u, abort_flag, p.status, lim);
-    if (!__syncthreads_and(ok)) {  // dS, this K buffer and S / dP free for the next block
-      ok = false;
-      break;
+      __syncwarp();  // the warp's dS is written (and its S, dP reads are complete)
+      if (lane == 0) mbar_arrive(smem_u32(&bars->ds_done[h]));
     }
   }
-
-  if (warp == 0) {  // drain copies and MMAs in flight
-    if (!qd_waited) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
-    for (int i = n_waited; i < n_issued; ++i)
-      bwd_drain_wait(smem_u32(&bars->kv_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
-    if (elect_one()) mma_commit(smem_u32(&bars->drain));
-    __syncwarp();
-    bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
-  }
-  __syncthreads();
+  const bool all_ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (ok) {  // dQ times scale, one query row and half of the columns per thread
+  if (all_ok && warp < kMmaWarp) {  // dQ times scale, one query row and half of the columns
+    const int r = tid & (kBlock - 1);
+    const int half = warp >> 2;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     float* dqr = p.dq + (size_t)(qrow0 + r) * D;
 #pragma unroll 1
     for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
@@ -737,7 +763,7 @@ cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const 
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_bwd_dq_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  bsattn_bwd_dq_kernel<D><<<grid, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
@@ -756,7 +782,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_bwd_kernel<D><<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  bsattn_bwd_kernel<D><<<grid, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p);
   return cudaGetLastError();
 }
 
