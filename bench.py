@@ -538,7 +538,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
             "data": "synthetic",
-            "config": {"workload": f"{w.id}:{w.name}", "shape": w.describe(),
+            "config": {"workload": f"{w.id}:{w.name}", "shape": w.describe(args.in_dtype),
                        "out_dtype": "f32" if args.out_f32 else "bf16",
                        "key_block": args.key_block, "in_dtype": args.in_dtype,
                        "live_blocks": nlive, "flop_per_step": flop,

@@ -211,9 +211,9 @@ class Workload:
     def mask_seed(self) -> int:
         return 2000 + self.id
 
-    def describe(self) -> str:
+    def describe(self, in_dtype: str = "bf16") -> str:
         return (f"B={self.B} H={self.H} S={self.S} D={self.D} mask={self.mask_kind}"
-                f"{' causal' if self.causal else ''} inputs=N(0,1)*{self.mult:g} bf16")
+                f"{' causal' if self.causal else ''} inputs=N(0,1)*{self.mult:g} {in_dtype}")
 
 
 WORKLOADS = {
