@@ -379,12 +379,13 @@ bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const 
   if (!get_tensor_map_encoder()) return BSATTN_ERR_CUDA;
   const long long rows = (long long)B * H * S;
   const long long kv_rows = (long long)B * Hkv * S;
+  // The backward kernels load tiles by halves: 64-row boxes.
   CUtensorMap tq, tk, tv, tdo;
   bsattn_status rc;
-  if ((rc = encode_bf16_map(&tq, q, D, rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tk, k, D, kv_rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tv, v, D, kv_rows)) != BSATTN_OK) return rc;
-  if ((rc = encode_bf16_map(&tdo, dout, D, rows)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tq, q, D, rows, 64)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tk, k, D, kv_rows, 64)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tv, v, D, kv_rows, 64)) != BSATTN_OK) return rc;
+  if ((rc = encode_bf16_map(&tdo, dout, D, rows, 64)) != BSATTN_OK) return rc;
   BwdParams prm{};
   prm.col_ptr = plan->dev.col_ptr;
   prm.row_idx = plan->dev.row_idx;

@@ -19,30 +19,32 @@
 // either were measured to bound the whole pass by L2 atomic throughput).
 //
 // bsattn_bwd_kernel (dK, dV): one CTA per key tile (128 keys of one (batch,
-// head)), 288 threads: eight CUDA-core warps (two per TMEM sub-partition,
+// head)), 320 threads: eight CUDA-core warps (two per TMEM sub-partition,
 // warps 4h .. 4h+3 working on half h of each query block: queries 64h ..
-// 64h+63) and one copy / MMA warp.  It walks the plan's transposed list (the
-// live query blocks of its key block) and keeps dV and dK in tensor memory.
-// Per query block and half h, with keys as TMEM lanes:
+// 64h+63), an MMA warp and a load warp.  It walks the plan's transposed list
+// (the live query blocks of its key block) and keeps dV and dK in tensor
+// memory.  Per query block and half h, with keys as TMEM lanes:
 //   S^T_h = K Q_h^T, dP^T_h = V dO_h^T                 (tcgen05, N = 64, operands in smem)
 //   P^T = 2^(S^T scale log2 e - LSE log2 e), dS^T = P^T (dP^T - Dl)   (CUDA cores)
-//   P^T (bf16) goes back to tensor memory over S^T_h (queries 64h + 2c,
-//   64h + 2c + 1 in column 64h + c: each half writes inside the scores it read);
-//   dS^T (bf16) goes to shared memory
-//   dV += P^T_h dO_h   (A from tensor memory, B = dO read MN-major, K = 64)
-//   dK += dS^T_h Q_h   (A = dS^T, B = Q read MN-major, K = 64)
-// Each step has a barrier per half, so the CUDA cores work on one half while
-// the tensor core computes the other half's products: half 0's P^T / dS^T
-// overlaps S^T_1 and dP^T_1, half 1's overlaps dV, dK of half 0 and the next
-// block's S^T_0, dP^T_0.  Q and dO are double-buffered: the next query
-// block's tiles load once the previous block's products are done with them.
+//   P^T and dS^T (bf16) go back to tensor memory over S^T_h and dP^T_h
+//   (queries 64h + 2c, 64h + 2c + 1 in column 64h + c: each half writes
+//   inside the values it read)
+//   dV += P^T_h dO_h   (A = P^T from tensor memory, B = dO read MN-major, K = 64)
+//   dK += dS^T_h Q_h   (A = dS^T from tensor memory, B = Q read MN-major, K = 64)
+// The MMA warp interleaves the halves (gradients of half 0 of block j, S^T_0
+// of block j + 1, gradients of half 1, S^T_1 of block j + 1), so that each
+// half's CUDA-core phase overlaps the other half's products.  A thread that
+// issues MMAs is held for about as long as they run, so the MMA warp does
+// nothing but wait and issue; the load warp streams Q_h and dO_h (64-row TMA
+// boxes, two buffers per half) as the gradient steps free their buffers.
 //
 // bsattn_bwd_dq_kernel (dQ): one CTA per query tile, walking the forward
 // plan's list of live key blocks with queries as TMEM lanes: S = Q K^T and
-// dP = dO V^T recomputed, dS = P (dP - Dl) to shared memory, dQ += dS K in
-// tensor memory (K and V double-buffered), dQ written once at the end; the
-// same 288 threads and per-half pipeline as the dK/dV kernel, halves of the
-// key block (keys 64h .. 64h+63) instead of the query block.
+// dP = dO V^T recomputed, dS = P (dP - Dl) back to tensor memory over dP,
+// dQ += dS K in tensor memory (K_h and V_h streamed by the load warp), dQ
+// written once at the end; the same 320 threads and interleaved halves as
+// the dK/dV kernel, halves of the key block (keys 64h .. 64h+63) instead of
+// the query block.
 //
 // Every mbarrier wait is bounded; on expiry the status word records a
 // timeout and the CTA drains its copies and MMAs before it frees tensor memory.
@@ -64,43 +66,60 @@ struct BwdCfg {
   static constexpr int kTileBytes = kBlock * D * 2;  // one 128 x D bf16 tile
   static constexpr int kBoxes = D / 64;              // 64-column (128-byte) TMA boxes
   static constexpr int kBoxBytes = kBlock * 128;     // 16 KB per box
+  static constexpr int kHalfBoxBytes = kBoxBytes / 2;  // 64 rows of one box
+  static constexpr int kHalfBytes = kTileBytes / 2;    // 64 rows of one tile
   static constexpr int kKOff = 0;
   static constexpr int kVOff = kKOff + kTileBytes;
-  static constexpr int kQOff = kVOff + kTileBytes;     // two buffers
+  static constexpr int kQOff = kVOff + kTileBytes;       // two buffers
   static constexpr int kdOOff = kQOff + 2 * kTileBytes;  // two buffers
-  static constexpr int kdSOff = kdOOff + 2 * kTileBytes;  // 128 x 128 bf16: two boxes
-  static constexpr int kBarOff = kdSOff + 2 * kBoxBytes;
-  static constexpr int kGrpOff = kBarOff + 128;  // per query head of the group: list start, prefix
+  static constexpr int kVecBytes = 2 * 64 * 4;  // per CUDA-core warp: LSE and Dl of 64 queries
+  static constexpr int kVecOff = kdOOff + 2 * kTileBytes;
+  static constexpr int kBarOff = kVecOff + 8 * kVecBytes;
+  static constexpr int kGrpOff = kBarOff + 256;  // per query head of the group: list start, prefix
   static constexpr int kSmem = kGrpOff + 4 * (2 * kMaxKvGroup + 1) + 124;
   // S^T = K Q^T and dP^T = V dO^T, per half of the query block: M = 128 keys,
   // N = 64 queries, both K-major
   static constexpr uint32_t kIdescT = idesc_bf16_f32(128, 64, false);
-  // dV += P^T dO and dK += dS^T Q: M = 128 keys, N = D, B MN-major
+  // dV += P^T dO and dK += dS^T Q: M = 128 keys, A from tensor memory, N = D, B MN-major
   static constexpr uint32_t kIdescKV = idesc_bf16_f32(128, D, true);
   // tensor-memory columns
-  static constexpr uint32_t kTS = 0;         // S^T (fp32), then P^T (bf16) in [0,32) and [64,96)
+  static constexpr uint32_t kTS = 0;         // S^T (fp32)
   static constexpr uint32_t kTdP = 128;      // dP^T (fp32)
   static constexpr uint32_t kTdV = 256;      // dV accumulator (D columns)
   static constexpr uint32_t kTdK = 256 + D;  // dK accumulator (D columns)
+  // P^T and dS^T (bf16 pairs, 32 columns per half): at D = 64 in columns of
+  // their own, so that the next block's S^T_h may be computed while the
+  // gradient step still reads them; at D = 128 (no columns left) over the
+  // half's S^T and dP^T columns, so S^T_h of the next block waits for it.
+  static constexpr bool kSep = D == 64;
+  static constexpr uint32_t kTP = kSep ? 256 + 2 * D : kTS;          // half h: + (kSep ? 32 : 64) h
+  static constexpr uint32_t kTdS = kSep ? 256 + 2 * D + 64 : kTdP;
+  static constexpr uint32_t kHalfStride = kSep ? 32 : 64;
 };
 static_assert(BwdCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 static_assert(BwdCfg<128>::kTdK + 128 <= kBwdTmemCols, "tensor memory exceeded");
 
-// The dK/dV kernel works on each query block in two halves h (queries
-// 64h .. 64h+63), with a barrier per half for every step, so that one half's
-// CUDA-core work overlaps the tensor core's work on the other half.
+// Barriers of the dK/dV kernel, per half h of each query block (queries
+// 64h .. 64h+63) where the halves have their own.
 struct __align__(8) BwdBars {
-  uint64_t kv_full;      // K and V of the key tile loaded
-  uint64_t qd_full[2];   // Q and dO of a query block loaded (by buffer)
-  uint64_t st_done[2];   // S^T and dP^T of half h computed
-  uint64_t pds_done[2];  // P^T (tensor memory) and dS^T (shared memory) of half h written
-  uint64_t grad_done[2]; // dV and dK updated with half h
-  uint64_t drain;        // every MMA issued so far complete
+  uint64_t kv_full;        // K and V of the key tile loaded
+  // Q_h and dO_h of a query block loaded (by half, buffer); at D = 128 also
+  // the previous block's gradient step of the half complete (its operands
+  // sit where the next S^T_h goes): two arrivals, the copy's and the commit's
+  uint64_t qd_full[2][2];
+  uint64_t qd_empty[2][2]; // the gradients of the block in that buffer complete (by half)
+  uint64_t st_done[2];     // S^T and dP^T of half h computed
+  uint64_t pds_done[2];    // P^T and dS^T of half h written (tensor memory)
+  uint64_t drain;          // every MMA issued so far complete
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(BwdBars) <= 128, "barrier block must fit its 128-byte region");
-constexpr int kBwdKvThreads = 288;  // dK/dV kernel: 8 CUDA-core warps and an MMA / copy warp
+static_assert(sizeof(BwdBars) <= 256, "barrier block must fit its 256-byte region");
+// Both kernels: 8 CUDA-core warps, an MMA warp and a load warp.
+constexpr int kBwdKvThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+
 
 // Dl_i = dO_i . O_i (fp32 over the stored O and dO); one warp per row.
 template <int D, bool O_F32>
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  constexpr int kMmaWarp = 8;   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3
+  // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
   const int tile = blockIdx.x;  // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk
   const int kvbh = tile / p.nb;
   const int kb = tile - kvbh * p.nb;
@@ -167,10 +186,11 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw);
   // The CTA walks the transposed lists of the group's query heads one after
   // the other: head bh0 + i contributes entries [g_st[i], g_st[i+1]) of the
   // walk, starting at row_idx[g_c0[i]].
-  int* g_c0 = reinterpret_cast<int*>(smem_raw + (base - raw) + C::kGrpOff);
+  int* g_c0 = reinterpret_cast<int*>(sbase + C::kGrpOff);
   int* g_st = g_c0 + kMaxKvGroup;
   if (tid < g) {
     const int t = (bh0 + tid) * p.nb + kb;
@@ -213,17 +233,19 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     return;
   }
 
-  BwdBars* bars = reinterpret_cast<BwdBars*>(smem_raw + (base - raw) + C::kBarOff);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sbase + C::kBarOff);
   const uint64_t lim = p.timeout_ns;
   volatile int* abort_flag = &bars->abort_flag;
 
   if (tid == 0) {
     mbar_init(smem_u32(&bars->kv_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->qd_full[i]), 1);
-      mbar_init(smem_u32(&bars->st_done[i]), 1);
-      mbar_init(smem_u32(&bars->pds_done[i]), 4);  // the half's four warps
-      mbar_init(smem_u32(&bars->grad_done[i]), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&bars->qd_full[h][0]), C::kSep ? 1 : 2);
+      mbar_init(smem_u32(&bars->qd_full[h][1]), C::kSep ? 1 : 2);
+      mbar_init(smem_u32(&bars->qd_empty[h][0]), 1);
+      mbar_init(smem_u32(&bars->qd_empty[h][1]), 1);
+      mbar_init(smem_u32(&bars->st_done[h]), 1);
+      mbar_init(smem_u32(&bars->pds_done[h]), 4);  // the half's four warps
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
@@ -244,131 +266,167 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   bool ok = true;
 
   if (warp == kMmaWarp) {
-    // ---- copies and MMAs (elected lane): per block j, for each half h,
-    // S^T_h = K Q_h^T and dP^T_h = V dO_h^T once the half's buffers are free
-    // (dV, dK of the previous block's half h complete), then, once the CUDA
-    // cores have written P^T_h and dS^T_h, dV += P^T_h dO_h and dK += dS^T_h Q_h.
-    auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
-#pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
-    };
-    auto load_qd = [&](int i) {  // Q and dO of entry i into buffer i % 2
-      const int b = i & 1;
-      const uint32_t bar = smem_u32(&bars->qd_full[b]);
-      int bhq = 0, qbi = 0;
-      entry(i, bhq, qbi);
-      const int row = bhq * p.S + qbi * kBlock;
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      load_tile(&tm_q, base + C::kQOff + b * C::kTileBytes, bar, row);
-      load_tile(&tm_do, base + C::kdOOff + b * C::kTileBytes, bar, row);
-    };
-    int n_issued = 0, n_waited = 0;  // Q-dO loads issued / awaited
-    if (elect_one()) {
-      const uint32_t bar = smem_u32(&bars->kv_full);
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      load_tile(&tm_k, base + C::kKOff, bar, krow0);
-      load_tile(&tm_v, base + C::kVOff, bar, krow0);
-      load_qd(0);
-      if (n > 1) load_qd(1);
-    }
-    __syncwarp();
-    n_issued = n > 1 ? 2 : 1;
-    ok = bwd_wait(smem_u32(&bars->kv_full), 0, abort_flag, p.status, lim);
-    const bool kv_ok = ok;
+    // ---- MMAs (one elected lane), in one fixed order per block j:
+    //   dV, dK += half 0 of block j;  S^T_0, dP^T_0 of block j + 1;
+    //   dV, dK += half 1 of block j;  S^T_1, dP^T_1 of block j + 1.
+    // At D = 128, S^T_h of block j + 1 overwrites the tensor-memory operands
+    // of the gradient step before it, so it waits (on its readiness barrier)
+    // until that step is complete.  The order also fixes the order in which
+    // dV and dK accumulate (the gradients repeat bit for bit).  The issuing lane is held for about as long as its
+    // MMAs run, so it does nothing else: the loads are the load warp's.
     const uint64_t kd = smem_desc_sw128(base + C::kKOff, 16, 1024);
     const uint64_t vd = smem_desc_sw128(base + C::kVOff, 16, 1024);
-    const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
-    for (int j = 0; ok && j < n; ++j) {
-      const int b = j & 1;
-      ok = bwd_wait(smem_u32(&bars->qd_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
-                    lim);
-      if (!ok) break;
-      n_waited = j + 1;
-      for (int h = 0; ok && h < 2; ++h) {
-        if (j > 0) {  // half h of the previous block multiplied: its columns and dS^T free
-          ok = bwd_wait(smem_u32(&bars->grad_done[h]), (uint32_t)(j - 1) & 1u, abort_flag,
-                        p.status, lim);
-          if (!ok) break;
-          if (h == 1 && j + 1 < n) {  // the previous block's buffers are free: next Q, dO
-            if (elect_one()) load_qd(j + 1);
-            __syncwarp();
-            n_issued = j + 2;
-          }
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          // queries 64h .. 64h+63: rows 64h.. of the Q and dO tiles (8 KB into each box)
-          const uint32_t rows_h = (uint32_t)h * 64u * 128u;
-          const uint64_t qd = smem_desc_sw128(base + C::kQOff + b * C::kTileBytes + rows_h, 16, 1024);
-          const uint64_t dd = smem_desc_sw128(base + C::kdOOff + b * C::kTileBytes + rows_h, 16, 1024);
+    auto issue_st = [&](int h, int j) {  // S^T_h = K Q_h^T, dP^T_h = V dO_h^T of block j
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t off = (uint32_t)((j & 1) * C::kTileBytes + h * C::kHalfBoxBytes);
+        const uint64_t qd = smem_desc_sw128(base + C::kQOff + off, 16, 1024);
+        const uint64_t dd = smem_desc_sw128(base + C::kdOOff + off, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTS + 64u * h, kd + off, qd + off, C::kIdescT, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTdP + 64u * h, vd + off, dd + off, C::kIdescT, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bars->st_done[h]));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kTS + 64u * h, kd + o, qd + o, C::kIdescT, kk > 0 ? 1u : 0u);
         }
-        __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kTdP + 64u * h, vd + o, dd + o, C::kIdescT, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->st_done[h]));
       }
+      __syncwarp();
+    };
+    auto issue_grad = [&](int h, int j) {  // dV += P^T_h dO_h, dK += dS^T_h Q_h of block j
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t qoff = base + C::kQOff + (j & 1) * C::kTileBytes;
+        const uint32_t dooff = base + C::kdOOff + (j & 1) * C::kTileBytes;
+        const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
+        const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * h + k4;                       // queries 16kk .. 16kk+15
+          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
+          const uint32_t acc = (j > 0 || h > 0 || k4 > 0) ? 1u : 0u;
+          const uint32_t pcol = C::kHalfStride * h + 8u * k4;  // P^T, dS^T of queries 16kk ..
+          mma_ts(tmem + C::kTdV, tmem + C::kTP + pcol, do_mn + mn, C::kIdescKV, acc);
+          mma_ts(tmem + C::kTdK, tmem + C::kTdS + pcol, q_mn + mn, C::kIdescKV, acc);
+        }
+        mma_commit(smem_u32(&bars->qd_empty[h][j & 1]));
+        // at D = 128 the next S^T_h overwrites this step's operands: its
+        // readiness barrier waits for this step too
+        if (!C::kSep && j + 1 < n) mma_commit(smem_u32(&bars->qd_full[h][(j + 1) & 1]));
+      }
+      __syncwarp();
+    };
+    ok = bwd_wait(smem_u32(&bars->kv_full), 0, abort_flag, p.status, lim);
+    for (int h = 0; ok && h < 2; ++h) {
+      ok = bwd_wait(smem_u32(&bars->qd_full[h][0]), 0, abort_flag, p.status, lim);
+      if (ok) issue_st(h, 0);
+    }
+    for (int j = 0; ok && j < n; ++j) {
       for (int h = 0; ok && h < 2; ++h) {
         ok = bwd_wait(smem_u32(&bars->pds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
         if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) {
-          const uint32_t qoff = base + C::kQOff + b * C::kTileBytes;
-          const uint32_t dooff = base + C::kdOOff + b * C::kTileBytes;
-          const uint64_t do_mn = smem_desc_sw128(dooff, C::kBoxBytes, 1024);
-          const uint64_t q_mn = smem_desc_sw128(qoff, C::kBoxBytes, 1024);
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = 4 * h + k4;                       // queries 16kk .. 16kk+15
-            const uint32_t mn = (uint32_t)(kk * 2048) >> 4;  // 16 rows of 128 bytes
-            const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
-            const uint32_t pcol = 64u * h + 8u * k4;  // P^T of queries 16kk .. in bf16 pairs
-            mma_ts(tmem + C::kTdV, tmem + C::kTS + pcol, do_mn + mn, C::kIdescKV, acc);
-            mma_ss(tmem + C::kTdK, ds_k + km, q_mn + mn, C::kIdescKV, acc);
-          }
-          mma_commit(smem_u32(&bars->grad_done[h]));
+        issue_grad(h, j);
+        if (j + 1 < n) {
+          ok = bwd_wait(smem_u32(&bars->qd_full[h][(j + 1) & 1]), (uint32_t)((j + 1) >> 1) & 1u,
+                        abort_flag, p.status, lim);
+          if (ok) issue_st(h, j + 1);
         }
-        __syncwarp();
       }
     }
-    // Drain: every copy issued and every MMA issued completes before tensor
-    // memory is freed and the CTA exits.
-    if (!kv_ok) bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
-    for (int i = n_waited; i < n_issued; ++i)
-      bwd_drain_wait(smem_u32(&bars->qd_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+    // Every MMA issued completes before tensor memory is freed.
     if (elect_one()) mma_commit(smem_u32(&bars->drain));
     __syncwarp();
     bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
-  } else {
+  } else if (warp == kLoadWarp) {
+    // ---- loads (one elected lane): K and V once; then, in the order of the
+    // walk, Q_h and dO_h of entry i into buffer i % 2 of half h once the
+    // gradients of entry i - 2's half h are complete.
+    auto load_half = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+    };
+    // First Q/dO row of each entry, 32 entries per window held one per lane;
+    // the next window is loaded a window ahead.
+    auto window_rows = [&](int w0) {
+      int row = 0;
+      if (w0 + lane < n) {
+        int bhq = 0, qbi = 0;
+        entry(w0 + lane, bhq, qbi);
+        row = bhq * p.S + qbi * kBlock;
+      }
+      return row;
+    };
+    int win0 = 0;
+    int row_cur = window_rows(0), row_next = window_rows(32);
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&bars->kv_full);
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      for (int hh = 0; hh < 2; ++hh) {
+        load_half(&tm_k, base + C::kKOff + hh * C::kHalfBoxBytes, bar, krow0 + 64 * hh);
+        load_half(&tm_v, base + C::kVOff + hh * C::kHalfBoxBytes, bar, krow0 + 64 * hh);
+      }
+    }
+    __syncwarp();
+    int loaded[2] = {0, 0};  // entries 0 .. loaded[h] - 1 loaded for half h
+    for (int i = 0; ok && i < n; ++i) {
+      while (i >= win0 + 32) {
+        win0 += 32;
+        row_cur = row_next;
+        row_next = window_rows(win0 + 32);
+      }
+      const int row0 = __shfl_sync(0xffffffffu, row_cur, i - win0);
+      const int b = i & 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (i >= 2) {
+          ok = bwd_wait(smem_u32(&bars->qd_empty[h][b]), (uint32_t)((i >> 1) - 1) & 1u,
+                        abort_flag, p.status, lim);
+          if (!ok) break;
+        }
+        if (elect_one()) {
+          const uint32_t bar = smem_u32(&bars->qd_full[h][b]);
+          const uint32_t off = (uint32_t)(b * C::kTileBytes + h * C::kHalfBoxBytes);
+          mbar_arrive_expect_tx(bar, 2 * C::kHalfBytes);
+          if (!C::kSep && i == 0) mbar_arrive(bar);  // no gradient step before the first block
+          load_half(&tm_q, base + C::kQOff + off, bar, row0 + 64 * h);
+          load_half(&tm_do, base + C::kdOOff + off, bar, row0 + 64 * h);
+        }
+        __syncwarp();
+        loaded[h] = i + 1;
+      }
+    }
+    // Every copy issued lands before the CTA exits.
+    bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
+    for (int h = 0; h < 2; ++h)  // the last one or two entries loaded
+      for (int i = loaded[h] > 2 ? loaded[h] - 2 : 0; i < loaded[h]; ++i)
+        bwd_drain_wait(smem_u32(&bars->qd_full[h][i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+  } else if (warp < kMmaWarp) {
     // ---- P^T and dS^T of half h (queries 64h .. 64h+63), one key row (TMEM
-    // lane) per thread, 32 queries at a time.  P^T (bf16 pairs) goes over
-    // the scores just read: queries 64h + 2c, 64h + 2c + 1 in column 64h + c.
-    // dS^T (bf16) goes to shared memory, 128-byte swizzled like a TMA tile:
-    // row r, 16-byte chunk c of 64-query box h at h * 16 KB + r * 128 +
-    // ((c ^ (r mod 8)) * 16).
+    // lane) per thread, 32 queries at a time; both go back to tensor memory
+    // as bf16 pairs over the fp32 values just read: queries 64h + 2c and
+    // 64h + 2c + 1 in column 64h + c of the S^T (P^T) and dP^T (dS^T) columns.
+    // LSE (log2 units) and Dl of the half's 64 queries sit in a shared vector
+    // of this warp (written by the warp for itself, read as broadcasts).
     const int h = warp >> 2;
     const int r = tid & (kBlock - 1);  // TMEM lane: key row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
     const float sl = p.scale_log2;
     const uint32_t tS = tmem + C::kTS + lane_off;
     const uint32_t tdP = tmem + C::kTdP + lane_off;
-    const uint32_t sdS = base + C::kdSOff;
-    // LSE (log2 units) and Dl of the half's queries 64h + lane and 64h + 32 +
-    // lane of entry j, loaded one entry ahead by every warp for itself and
-    // passed between lanes by shuffles (no barrier between the warps)
+    float* vl = reinterpret_cast<float*>(sbase + C::kVecOff + warp * C::kVecBytes);  // [64] LSE
+    float* vd = vl + 64;                                                             // [64] Dl
+    // LSE and Dl of the half's queries 64h + lane and 64h + 32 + lane of
+    // entry i, loaded one entry ahead
     float la_next = 0.f, lb_next = 0.f, da_next = 0.f, db_next = 0.f;
+    int qb_next = 0;
     auto fetch = [&](int i) {
-      int bhq = 0, qbi = 0;
-      entry(i, bhq, qbi);
-      const int qrow = bhq * p.S + qbi * kBlock + 64 * h + lane;
+      int bhq = 0;
+      entry(i, bhq, qb_next);
+      const int qrow = bhq * p.S + qb_next * kBlock + 64 * h + lane;
       la_next = p.lse[qrow] * kLog2e;
       lb_next = p.lse[qrow + 32] * kLog2e;
       da_next = p.dl[qrow];
@@ -376,9 +434,12 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     };
     fetch(0);
     for (int j = 0; j < n; ++j) {
-      int bhj = 0, qb = 0;
-      entry(j, bhj, qb);
-      const float la = la_next, lb = lb_next, da = da_next, db = db_next;
+      const int qb = qb_next;
+      vl[lane] = la_next;
+      vl[lane + 32] = lb_next;
+      vd[lane] = da_next;
+      vd[lane + 32] = db_next;
+      __syncwarp();
       if (j + 1 < n) fetch(j + 1);
       ok = bwd_wait(smem_u32(&bars->st_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
       if (!ok) break;
@@ -392,44 +453,38 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
         tmem_wait_ld();
         reg_fence(sv, 32);
         reg_fence(dp, 32);
-        const float lsrc = (ch & 1) ? lb : la;  // queries 64h + 32 (ch & 1) + lane
-        const float dsrc = (ch & 1) ? db : da;
+        const float4* l4 = reinterpret_cast<const float4*>(vl + 32 * (ch & 1));
+        const float4* d4 = reinterpret_cast<const float4*>(vd + 32 * (ch & 1));
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int q = ch * 32 + i;
-          const float l0 = __shfl_sync(0xffffffffu, lsrc, i);
-          const float l1 = __shfl_sync(0xffffffffu, lsrc, i + 1);
-          const float d0l = __shfl_sync(0xffffffffu, dsrc, i);
-          const float d1l = __shfl_sync(0xffffffffu, dsrc, i + 1);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l0));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l1));
-          if (diag) {
-            p0 = r > q ? 0.f : p0;
-            p1 = r > q + 1 ? 0.f : p1;
-          }
-          const float d0 = p0 * (__uint_as_float(dp[i]) - d0l);
-          const float d1 = p1 * (__uint_as_float(dp[i + 1]) - d1l);
-          pk[i >> 1] = pack_bf16x2(p0, p1);
-          dk[i >> 1] = pack_bf16x2(d0, d1);
-        }
-        tmem_st32_16(tS + (uint32_t)(64 * (ch >> 1) + 16 * (ch & 1)), pk);
-        const uint32_t rowa = sdS + (uint32_t)(ch >> 1) * C::kBoxBytes + (uint32_t)r * 128u;
+        for (int i = 0; i < 32; i += 4) {
+          const float4 l = l4[i >> 2];  // same address in every lane: a broadcast
+          const float4 d = d4[i >> 2];
+          const float lq[4] = {l.x, l.y, l.z, l.w};
+          const float dq[4] = {d.x, d.y, d.z, d.w};
+          float pe[4], de[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t c = (uint32_t)((ch & 1) * 4 + u);
-          st_shared_v4(rowa + ((c ^ (uint32_t)(r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
-                       dk[4 * u + 2], dk[4 * u + 3]);
+          for (int e = 0; e < 4; ++e) {
+            pe[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sl, -lq[e]));
+            if (diag) pe[e] = r > ch * 32 + i + e ? 0.f : pe[e];
+            de[e] = pe[e] * (__uint_as_float(dp[i + e]) - dq[e]);
+          }
+          pk[i >> 1] = pack_bf16x2(pe[0], pe[1]);
+          pk[(i >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+          dk[i >> 1] = pack_bf16x2(de[0], de[1]);
+          dk[(i >> 1) + 1] = pack_bf16x2(de[2], de[3]);
         }
+        const uint32_t col = C::kHalfStride * h + 16u * (ch & 1);
+        tmem_st32_16(tmem + C::kTP + lane_off + col, pk);
+        tmem_st32_16(tmem + C::kTdS + lane_off + col, dk);
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
-      __syncwarp();  // the warp's P^T and dS^T are written
+      __syncwarp();  // the warp's P^T and dS^T are written (and its vectors read)
       if (lane == 0) mbar_arrive(smem_u32(&bars->pds_done[h]));
     }
   }
-  // Every role has left its loop; the MMA warp drained all copies and MMAs.
+  // Every role has left its loop; the MMA thread drained all copies and MMAs.
   const bool all_ok = __syncthreads_and(ok);
   tc_fence_after();
   if (all_ok && warp < kMmaWarp) {  // dV and dK (times scale), one key row and half the columns
@@ -464,40 +519,43 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   }
 }
 
-// dQ kernel layout: Q, dO once per tile; K and V double-buffered; dS with
-// queries as rows.
+// dQ kernel layout: Q, dO once per tile; K and V double-buffered by halves.
 template <int D>
 struct DqCfg {
   static constexpr int kTileBytes = kBlock * D * 2;
   static constexpr int kBoxes = D / 64;
   static constexpr int kBoxBytes = kBlock * 128;
+  static constexpr int kHalfBoxBytes = kBoxBytes / 2;    // 64 rows of one box
+  static constexpr int kHalfBytes = kTileBytes / 2;      // 64 rows of one tile
   static constexpr int kQOff = 0;
   static constexpr int kdOOff = kTileBytes;
   static constexpr int kKOff = 2 * kTileBytes;   // two buffers
   static constexpr int kVOff = 4 * kTileBytes;   // two buffers
-  static constexpr int kdSOff = 6 * kTileBytes;  // 128 queries x 128 keys bf16: two boxes
-  static constexpr int kBarOff = kdSOff + 2 * kBoxBytes;
+  static constexpr int kBarOff = 6 * kTileBytes;
   static constexpr int kSmem = kBarOff + 256;
   // S = Q K^T and dP = dO V^T, per half of the key block: M = 128 queries,
   // N = 64 keys, both K-major
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, false);
-  // dQ += dS K: M = 128 queries, N = D, B (K) read MN-major
+  // dQ += dS K: M = 128 queries, A = dS from tensor memory, N = D, B (K) read MN-major
   static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true);
   static constexpr uint32_t kTS = 0;     // S (fp32)
   static constexpr uint32_t kTdP = 128;  // dP (fp32)
   static constexpr uint32_t kTdQ = 256;  // dQ accumulator (D columns)
+  // dS (bf16 pairs) in columns of its own, 32 per half: the next key block's
+  // S_h may be computed while the dQ step still reads them
+  static constexpr uint32_t kTdS = 384;
 };
 static_assert(DqCfg<128>::kSmem + 1024 <= 232448, "shared memory per CTA (227 KB) exceeded");
 
-// The dQ kernel works on each key block in two halves h (keys 64h .. 64h+63)
-// with a barrier per half for every step, as the dK/dV kernel does.
+// The dQ kernel works on each key block in two halves h (keys 64h .. 64h+63),
+// interleaved as the dK/dV kernel's halves are.
 struct __align__(8) DqBars {
-  uint64_t qd_full;      // Q and dO of the tile loaded
-  uint64_t kv_full[2];   // K and V of a key block loaded (by buffer)
-  uint64_t st_done[2];   // S and dP of half h computed
-  uint64_t ds_done[2];   // dS of half h written
-  uint64_t grad_done[2]; // dQ updated with half h
-  uint64_t drain;        // every MMA issued so far complete
+  uint64_t qd_full;        // Q and dO of the tile loaded
+  uint64_t kv_full[2][2];  // K_h and V_h of a key block loaded (by half, buffer)
+  uint64_t kv_empty[2][2]; // dQ has taken the key block in that buffer (by half)
+  uint64_t st_done[2];     // S and dP of half h computed
+  uint64_t ds_done[2];     // dS of half h written
+  uint64_t drain;          // every MMA issued so far complete
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -513,7 +571,7 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  constexpr int kMmaWarp = 8;   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3
+  // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
   const int tile = blockIdx.x;  // (b * H + h) * nb + qb
   const int bh = tile / p.nb;
   const int qb = tile - bh * p.nb;
@@ -546,11 +604,13 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   volatile int* abort_flag = &bars->abort_flag;
   if (tid == 0) {
     mbar_init(smem_u32(&bars->qd_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->kv_full[i]), 1);
-      mbar_init(smem_u32(&bars->st_done[i]), 1);
-      mbar_init(smem_u32(&bars->ds_done[i]), 4);  // the half's four warps
-      mbar_init(smem_u32(&bars->grad_done[i]), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&bars->kv_full[h][0]), 1);
+      mbar_init(smem_u32(&bars->kv_full[h][1]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[h][0]), 1);
+      mbar_init(smem_u32(&bars->kv_empty[h][1]), 1);
+      mbar_init(smem_u32(&bars->st_done[h]), 1);
+      mbar_init(smem_u32(&bars->ds_done[h]), 4);  // the half's four warps
     }
     mbar_init(smem_u32(&bars->drain), 1);
     bars->abort_flag = 0;
@@ -571,104 +631,131 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   bool ok = true;
 
   if (warp == kMmaWarp) {
-    // ---- copies and MMAs (elected lane): per key block j, for each half h,
-    // S_h = Q K_h^T and dP_h = dO V_h^T once the half's columns and dS are
-    // free (dQ of the previous block's half h complete), then, once the CUDA
-    // cores have written dS_h, dQ += dS_h K_h.
-    auto load_tile = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
-#pragma unroll
-      for (int c = 0; c < C::kBoxes; ++c) tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
-    };
-    auto load_kv = [&](int i) {  // K and V of key block number i into buffer i % 2
-      const int b = i & 1;
-      const uint32_t bar = smem_u32(&bars->kv_full[b]);
-      const int row = kvbh * p.S + p.col_idx[r0 + i] * kBlock;
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      load_tile(&tm_k, base + C::kKOff + b * C::kTileBytes, bar, row);
-      load_tile(&tm_v, base + C::kVOff + b * C::kTileBytes, bar, row);
-    };
-    if (elect_one()) {
-      const uint32_t bar = smem_u32(&bars->qd_full);
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      load_tile(&tm_q, base + C::kQOff, bar, qrow0);
-      load_tile(&tm_do, base + C::kdOOff, bar, qrow0);
-      load_kv(0);
-      if (n > 1) load_kv(1);
-    }
-    __syncwarp();
-    int n_issued = n > 1 ? 2 : 1, n_waited = 0;
-    ok = bwd_wait(smem_u32(&bars->qd_full), 0, abort_flag, p.status, lim);
-    const bool qd_ok = ok;
+    // ---- MMAs (one elected lane), in one fixed order per key block j:
+    //   dQ += half 0 of block j;  S_0, dP_0 of block j + 1;
+    //   dQ += half 1 of block j;  S_1, dP_1 of block j + 1,
+    // as in the dK/dV kernel (dQ accumulates in a fixed order; the loads are
+    // the load warp's).  dS has columns of its own, so S_h of the next block
+    // waits for its K_h, V_h only; the commit of that S also covers the dQ
+    // step before it, which the half's warps wait on before they write dS.
     const uint64_t qd = smem_desc_sw128(base + C::kQOff, 16, 1024);
     const uint64_t dd = smem_desc_sw128(base + C::kdOOff, 16, 1024);
-    const uint64_t ds_k = smem_desc_sw128(base + C::kdSOff, 16, 1024);
-    for (int j = 0; ok && j < n; ++j) {
-      const int b = j & 1;
-      ok = bwd_wait(smem_u32(&bars->kv_full[b]), (uint32_t)(j >> 1) & 1u, abort_flag, p.status,
-                    lim);
-      if (!ok) break;
-      n_waited = j + 1;
-      for (int h = 0; ok && h < 2; ++h) {
-        if (j > 0) {  // half h of the previous block multiplied: its columns and dS free
-          ok = bwd_wait(smem_u32(&bars->grad_done[h]), (uint32_t)(j - 1) & 1u, abort_flag,
-                        p.status, lim);
-          if (!ok) break;
-          if (h == 1 && j + 1 < n) {  // the previous block's K, V are free: next K, V
-            if (elect_one()) load_kv(j + 1);
-            __syncwarp();
-            n_issued = j + 2;
-          }
-        }
-        tc_fence_after();
-        if (elect_one()) {
-          // keys 64h .. 64h+63: rows 64h.. of the K and V tiles (8 KB into each box)
-          const uint32_t rows_h = (uint32_t)h * 64u * 128u;
-          const uint64_t kd = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes + rows_h, 16, 1024);
-          const uint64_t vd = smem_desc_sw128(base + C::kVOff + b * C::kTileBytes + rows_h, 16, 1024);
+    auto issue_st = [&](int h, int j) {  // S_h = Q K_h^T, dP_h = dO V_h^T of key block j
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t off = (uint32_t)((j & 1) * C::kTileBytes + h * C::kHalfBoxBytes);
+        const uint64_t kd = smem_desc_sw128(base + C::kKOff + off, 16, 1024);
+        const uint64_t vd = smem_desc_sw128(base + C::kVOff + off, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTS + 64u * h, qd + off, kd + off, C::kIdescS, kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            mma_ss(tmem + C::kTdP + 64u * h, dd + off, vd + off, C::kIdescS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bars->st_done[h]));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kTS + 64u * h, qd + o, kd + o, C::kIdescS, kk > 0 ? 1u : 0u);
         }
-        __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + C::kTdP + 64u * h, dd + o, vd + o, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->st_done[h]));
       }
+      __syncwarp();
+    };
+    auto issue_grad = [&](int h, int j) {  // dQ += dS_h K_h of key block j
+      tc_fence_after();
+      if (elect_one()) {
+        const uint64_t k_mn =
+            smem_desc_sw128(base + C::kKOff + (j & 1) * C::kTileBytes, C::kBoxBytes, 1024);
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const int kk = 4 * h + k4;  // keys 16kk .. 16kk+15
+          const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
+          mma_ts(tmem + C::kTdQ, tmem + C::kTdS + 32u * h + 8u * k4, k_mn + mn, C::kIdescQ,
+                 (j > 0 || h > 0 || k4 > 0) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(&bars->kv_empty[h][j & 1]));
+      }
+      __syncwarp();
+    };
+    ok = bwd_wait(smem_u32(&bars->qd_full), 0, abort_flag, p.status, lim);
+    for (int h = 0; ok && h < 2; ++h) {
+      ok = bwd_wait(smem_u32(&bars->kv_full[h][0]), 0, abort_flag, p.status, lim);
+      if (ok) issue_st(h, 0);
+    }
+    for (int j = 0; ok && j < n; ++j) {
       for (int h = 0; ok && h < 2; ++h) {
         ok = bwd_wait(smem_u32(&bars->ds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
         if (!ok) break;
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t k_mn = smem_desc_sw128(base + C::kKOff + b * C::kTileBytes, C::kBoxBytes,
-                                                1024);
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const int kk = 4 * h + k4;  // keys 16kk .. 16kk+15
-            const uint32_t km = (uint32_t)((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-            const uint32_t mn = (uint32_t)(kk * 2048) >> 4;
-            mma_ss(tmem + C::kTdQ, ds_k + km, k_mn + mn, C::kIdescQ, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(smem_u32(&bars->grad_done[h]));
+        issue_grad(h, j);
+        if (j + 1 < n) {
+          ok = bwd_wait(smem_u32(&bars->kv_full[h][(j + 1) & 1]), (uint32_t)((j + 1) >> 1) & 1u,
+                        abort_flag, p.status, lim);
+          if (ok) issue_st(h, j + 1);
         }
-        __syncwarp();
       }
     }
-    // Drain copies and MMAs in flight.
-    if (!qd_ok) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
-    for (int i = n_waited; i < n_issued; ++i)
-      bwd_drain_wait(smem_u32(&bars->kv_full[i & 1]), (uint32_t)(i >> 1) & 1u, lim);
     if (elect_one()) mma_commit(smem_u32(&bars->drain));
     __syncwarp();
     bwd_drain_wait(smem_u32(&bars->drain), 0, lim);
-  } else {
+  } else if (warp == kLoadWarp) {
+    // ---- loads (one elected lane): Q and dO once; then K_h and V_h of key
+    // block i into buffer i % 2 of half h once dQ has taken block i - 2's half h.
+    auto load_half = [&](const CUtensorMap* tm, uint32_t dst, uint32_t bar, int row) {
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c)
+        tma_load_2d(dst + c * C::kBoxBytes, tm, bar, c * 64, row);
+    };
+    // First K/V row of each key block of the list, 32 per window held one per
+    // lane; the next window is loaded a window ahead.
+    auto window_rows = [&](int w0) {
+      return w0 + lane < n ? kvbh * p.S + p.col_idx[r0 + w0 + lane] * kBlock : 0;
+    };
+    int win0 = 0;
+    int row_cur = window_rows(0), row_next = window_rows(32);
+    if (elect_one()) {
+      const uint32_t bar = smem_u32(&bars->qd_full);
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      for (int hh = 0; hh < 2; ++hh) {
+        load_half(&tm_q, base + C::kQOff + hh * C::kHalfBoxBytes, bar, qrow0 + 64 * hh);
+        load_half(&tm_do, base + C::kdOOff + hh * C::kHalfBoxBytes, bar, qrow0 + 64 * hh);
+      }
+    }
+    __syncwarp();
+    int loaded[2] = {0, 0};  // key blocks 0 .. loaded[h] - 1 loaded for half h
+    for (int i = 0; ok && i < n; ++i) {
+      while (i >= win0 + 32) {
+        win0 += 32;
+        row_cur = row_next;
+        row_next = window_rows(win0 + 32);
+      }
+      const int row0 = __shfl_sync(0xffffffffu, row_cur, i - win0);
+      const int b = i & 1;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (i >= 2) {
+          ok = bwd_wait(smem_u32(&bars->kv_empty[h][b]), (uint32_t)((i >> 1) - 1) & 1u,
+                        abort_flag, p.status, lim);
+          if (!ok) break;
+        }
+        if (elect_one()) {
+          const uint32_t bar = smem_u32(&bars->kv_full[h][b]);
+          const uint32_t off = (uint32_t)(b * C::kTileBytes + h * C::kHalfBoxBytes);
+          mbar_arrive_expect_tx(bar, 2 * C::kHalfBytes);
+          load_half(&tm_k, base + C::kKOff + off, bar, row0 + 64 * h);
+          load_half(&tm_v, base + C::kVOff + off, bar, row0 + 64 * h);
+        }
+        __syncwarp();
+        loaded[h] = i + 1;
+      }
+    }
+    // Every copy issued lands before the CTA exits.
+    bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
+    for (int h = 0; h < 2; ++h)  // the last one or two key blocks loaded
+      for (int i = loaded[h] > 2 ? loaded[h] - 2 : 0; i < loaded[h]; ++i)
+        bwd_drain_wait(smem_u32(&bars->kv_full[h][i & 1]), (uint32_t)(i >> 1) & 1u, lim);
+  } else if (warp < kMmaWarp) {
     // ---- dS = P (dP - Dl) of half h (keys 64h .. 64h+63), one query row and
-    // 32 keys at a time, to shared memory (bf16, 128-byte swizzled: row r,
-    // 16-byte chunk c of 64-key box h at h * 16 KB + r * 128 + ((c ^ (r mod 8)) * 16)).
+    // 32 keys at a time, back to tensor memory as bf16 pairs over the dP just
+    // read: keys 64h + 2c and 64h + 2c + 1 in column 64h + c of the dP columns.
     const int h = warp >> 2;
     const int r = tid & (kBlock - 1);  // TMEM lane: query row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
@@ -677,7 +764,6 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     const float sl = p.scale_log2;
     const uint32_t tS = tmem + C::kTS + lane_off;
     const uint32_t tdP = tmem + C::kTdP + lane_off;
-    const uint32_t sdS = base + C::kdSOff;
     for (int j = 0; j < n; ++j) {
       const int kb = p.col_idx[r0 + j];
       ok = bwd_wait(smem_u32(&bars->st_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
@@ -705,15 +791,9 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
           dk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - dlr),
                                    p1 * (__uint_as_float(dp[i + 1]) - dlr));
         }
-        const uint32_t rowa = sdS + (uint32_t)(ch >> 1) * C::kBoxBytes + (uint32_t)r * 128u;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint32_t c = (uint32_t)((ch & 1) * 4 + u);
-          st_shared_v4(rowa + ((c ^ (uint32_t)(r & 7)) << 4), dk[4 * u], dk[4 * u + 1],
-                       dk[4 * u + 2], dk[4 * u + 3]);
-        }
+        tmem_st32_16(tmem + C::kTdS + lane_off + (uint32_t)(32 * h + 16 * (ch & 1)), dk);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();  // the warp's dS is written (and its S, dP reads are complete)
       if (lane == 0) mbar_arrive(smem_u32(&bars->ds_done[h]));
