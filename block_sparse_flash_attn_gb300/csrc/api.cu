@@ -114,6 +114,7 @@ void free_plan_memory(bsattn_plan_s* p) {
   cudaFree(p->dev.work);
   cudaFree(p->dev.col_ptr);
   cudaFree(p->dev.row_idx);
+  cudaFree(p->dev.kv_order);
   cudaFree(p->dev.dl);
   p->dev = PlanDevice{};
 }
@@ -288,8 +289,11 @@ bsattn_status bsattn_plan(const uint8_t* d_mask, int B, int H, int S, unsigned f
       return fail(from_cuda(e));
     if ((e = cudaMalloc(&p->dev.dl, sizeof(float) * (size_t)B * H * S)) != cudaSuccess)
       return fail(from_cuda(e));
-    if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, p->dev.col_ptr, p->dev.row_idx, st,
-                      mdiv)) != cudaSuccess)
+    if ((e = cudaMalloc(&p->dev.kv_order, sizeof(int) * (size_t)rows)) != cudaSuccess)
+      return fail(from_cuda(e));
+    if ((e = plan_csc(d_mask, BH, nb, causal, d_counts, d_live_off, d_totals, p->dev.col_ptr,
+                      p->dev.row_idx, p->dev.kv_order, device_sm_count(p->device), st, mdiv)) !=
+        cudaSuccess)
       return fail(from_cuda(e));
   }
   if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return fail(from_cuda(e));
@@ -405,6 +409,10 @@ bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const 
   prm.timeout_ns = kDefaultWaitTimeoutNs;
   prm.H = H;
   prm.kv_group = H / Hkv;
+  prm.tile_order = plan->dev.tile_order;
+  prm.empty_tiles = plan->dev.empty_tiles;
+  prm.kv_order = plan->dev.kv_order;
+  prm.n_live = (int)plan->n_live;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_prep(D, (plan->flags & BSATTN_OUT_F32) != 0, o, dout, plan->dev.dl,
                                   rows, st);

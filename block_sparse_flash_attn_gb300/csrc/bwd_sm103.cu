@@ -164,6 +164,39 @@ __device__ __forceinline__ void bwd_drain_wait(uint32_t bar, uint32_t parity, ui
     if (globaltimer_ns() - t0 > limit_ns) return;
 }
 
+// Accumulator rows out to global memory, coalesced: the warp's 32 TMEM lanes
+// (rows row0 .. row0+31 of `out`, row stride D floats), columns c .. c+31,
+// times `scale`.  Each thread holds one row after tcgen05.ld; the 32 x 32 fp32
+// piece goes through this warp's 4 KB of shared memory (16-byte chunk q of
+// row r at r * 128 + ((q ^ (r mod 8)) * 16), conflict-free both ways) and
+// leaves as full 128-byte lines, four rows per warp-wide store.
+template <int D>
+__device__ __forceinline__ void store_rows32(uint32_t taddr, float scale, float* out, int row0,
+                                             int c, uint32_t scratch, int lane) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+  tmem_wait_ld();
+  reg_fence(v, 32);
+  const uint32_t mine = scratch + (uint32_t)lane * 128u;
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(mine + (((uint32_t)q ^ (uint32_t)(lane & 7)) << 4),
+                 __float_as_uint(__uint_as_float(v[4 * q]) * scale),
+                 __float_as_uint(__uint_as_float(v[4 * q + 1]) * scale),
+                 __float_as_uint(__uint_as_float(v[4 * q + 2]) * scale),
+                 __float_as_uint(__uint_as_float(v[4 * q + 3]) * scale));
+  __syncwarp();
+  const int q = lane & 7;
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int r = it * 4 + (lane >> 3);
+    uint32_t w[4];
+    ld_shared_v4(scratch + (uint32_t)r * 128u + (((uint32_t)q ^ (uint32_t)(r & 7)) << 4), w);
+    st_global_v4(out + (size_t)(row0 + r) * D + c + 4 * q, w[0], w[1], w[2], w[3]);
+  }
+  __syncwarp();  // the piece is read before the next one is written
+}
+
 template <int D>
 __global__ void __launch_bounds__(kBwdKvThreads, 1)
     bsattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -175,7 +208,8 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
-  const int tile = blockIdx.x;  // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk
+  // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk; long tiles first
+  const int tile = p.kv_group == 1 ? p.kv_order[blockIdx.x] : (int)blockIdx.x;
   const int kvbh = tile / p.nb;
   const int kb = tile - kvbh * p.nb;
   const int g = p.kv_group;     // query heads reading this K/V head
@@ -326,12 +360,19 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     }
     for (int j = 0; ok && j < n; ++j) {
       for (int h = 0; ok && h < 2; ++h) {
-        ok = bwd_wait(smem_u32(&bars->pds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
+        // At D = 64 the next S^T_h depends on its Q_h, dO_h only: both
+        // barriers are tested first and the two steps issued back to back.
+        if (C::kSep && j + 1 < n)
+          ok = bwd_wait(smem_u32(&bars->qd_full[h][(j + 1) & 1]), (uint32_t)((j + 1) >> 1) & 1u,
+                        abort_flag, p.status, lim);
+        ok = ok && bwd_wait(smem_u32(&bars->pds_done[h]), (uint32_t)j & 1u, abort_flag, p.status,
+                            lim);
         if (!ok) break;
         issue_grad(h, j);
         if (j + 1 < n) {
-          ok = bwd_wait(smem_u32(&bars->qd_full[h][(j + 1) & 1]), (uint32_t)((j + 1) >> 1) & 1u,
-                        abort_flag, p.status, lim);
+          if (!C::kSep)
+            ok = bwd_wait(smem_u32(&bars->qd_full[h][(j + 1) & 1]),
+                          (uint32_t)((j + 1) >> 1) & 1u, abort_flag, p.status, lim);
           if (ok) issue_st(h, j + 1);
         }
       }
@@ -487,28 +528,16 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   // Every role has left its loop; the MMA thread drained all copies and MMAs.
   const bool all_ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (all_ok && warp < kMmaWarp) {  // dV and dK (times scale), one key row and half the columns
-    const int r = tid & (kBlock - 1);
+  if (all_ok && warp < kMmaWarp) {  // dV and dK (times scale): the warp's 32 key rows, half the columns
     const int half = warp >> 2;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float* dvr = p.dv + (size_t)(krow0 + r) * D;
-    float* dkr = p.dk + (size_t)(krow0 + r) * D;
+    const int row0 = krow0 + (warp & 3) * 32;
+    // every copy and MMA is complete: the Q buffers serve as scratch, 4 KB per warp
+    const uint32_t scratch = base + C::kQOff + (uint32_t)warp * 4096u;
 #pragma unroll 1
     for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
-      uint32_t v[32], k[32];
-      tmem_ld32(tmem + C::kTdV + lane_off + c, v);
-      tmem_ld32(tmem + C::kTdK + lane_off + c, k);
-      tmem_wait_ld();
-      reg_fence(v, 32);
-      reg_fence(k, 32);
-#pragma unroll
-      for (int i = 0; i < 32; i += 4) {
-        st_global_v4(dvr + c + i, v[i], v[i + 1], v[i + 2], v[i + 3]);
-        st_global_v4(dkr + c + i, __float_as_uint(__uint_as_float(k[i]) * p.scale),
-                     __float_as_uint(__uint_as_float(k[i + 1]) * p.scale),
-                     __float_as_uint(__uint_as_float(k[i + 2]) * p.scale),
-                     __float_as_uint(__uint_as_float(k[i + 3]) * p.scale));
-      }
+      store_rows32<D>(tmem + C::kTdV + lane_off + c, 1.0f, p.dv, row0, c, scratch, lane);
+      store_rows32<D>(tmem + C::kTdK + lane_off + c, p.scale, p.dk, row0, c, scratch, lane);
     }
   }
   tc_fence_before();
@@ -572,7 +601,9 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
-  const int tile = blockIdx.x;  // (b * H + h) * nb + qb
+  // (b * H + h) * nb + qb: the forward plan's tiles, long ones first, then the empty ones
+  const int tile = (int)blockIdx.x < p.n_live ? p.tile_order[blockIdx.x]
+                                              : p.empty_tiles[blockIdx.x - p.n_live];
   const int bh = tile / p.nb;
   const int qb = tile - bh * p.nb;
   const int r0 = p.row_ptr[tile];
@@ -683,14 +714,15 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     }
     for (int j = 0; ok && j < n; ++j) {
       for (int h = 0; ok && h < 2; ++h) {
-        ok = bwd_wait(smem_u32(&bars->ds_done[h]), (uint32_t)j & 1u, abort_flag, p.status, lim);
-        if (!ok) break;
-        issue_grad(h, j);
-        if (j + 1 < n) {
+        // both barriers first, then the two steps back to back
+        if (j + 1 < n)
           ok = bwd_wait(smem_u32(&bars->kv_full[h][(j + 1) & 1]), (uint32_t)((j + 1) >> 1) & 1u,
                         abort_flag, p.status, lim);
-          if (ok) issue_st(h, j + 1);
-        }
+        ok = ok && bwd_wait(smem_u32(&bars->ds_done[h]), (uint32_t)j & 1u, abort_flag, p.status,
+                            lim);
+        if (!ok) break;
+        issue_grad(h, j);
+        if (j + 1 < n) issue_st(h, j + 1);
       }
     }
     if (elect_one()) mma_commit(smem_u32(&bars->drain));
@@ -801,24 +833,15 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   }
   const bool all_ok = __syncthreads_and(ok);
   tc_fence_after();
-  if (all_ok && warp < kMmaWarp) {  // dQ times scale, one query row and half of the columns
-    const int r = tid & (kBlock - 1);
+  if (all_ok && warp < kMmaWarp) {  // dQ times scale: the warp's 32 query rows, half the columns
     const int half = warp >> 2;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    float* dqr = p.dq + (size_t)(qrow0 + r) * D;
+    const int row0 = qrow0 + (warp & 3) * 32;
+    // every copy and MMA is complete: the K buffers serve as scratch, 4 KB per warp
+    const uint32_t scratch = base + C::kKOff + (uint32_t)warp * 4096u;
 #pragma unroll 1
-    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + C::kTdQ + lane_off + c, v);
-      tmem_wait_ld();
-      reg_fence(v, 32);
-#pragma unroll
-      for (int i = 0; i < 32; i += 4)
-        st_global_v4(dqr + c + i, __float_as_uint(__uint_as_float(v[i]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[i + 1]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[i + 2]) * p.scale),
-                     __float_as_uint(__uint_as_float(v[i + 3]) * p.scale));
-    }
+    for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32)
+      store_rows32<D>(tmem + C::kTdQ + lane_off + c, p.scale, p.dq, row0, c, scratch, lane);
   }
   tc_fence_before();
   __syncthreads();

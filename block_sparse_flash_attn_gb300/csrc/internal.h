@@ -32,6 +32,9 @@ struct PlanDevice {
   // query blocks row_idx[col_ptr[c] .. col_ptr[c+1])
   int* col_ptr = nullptr;      // [R + 1]
   int* row_idx = nullptr;      // [nnz]
+  // key tiles in the dK/dV kernel's launch order: those with live query
+  // blocks longest first (within head chunks, as tile_order), then the empty ones
+  int* kv_order = nullptr;     // [R]
   float* dl = nullptr;         // [B*H*S] backward scratch: dO_i . O_i
 };
 
@@ -87,6 +90,13 @@ struct BwdParams {
   unsigned long long timeout_ns;
   int H = 1;         // query heads; kv_group query heads share one K/V head
   int kv_group = 1;
+  // launch orders: the dQ kernel's CTA i takes tile_order[i] (i < n_live),
+  // then empty_tiles[i - n_live]; the dK/dV kernel's CTA i takes kv_order[i]
+  // (kv_group == 1) or key tile i (grouped-query attention)
+  const int* tile_order = nullptr;
+  const int* empty_tiles = nullptr;
+  const int* kv_order = nullptr;
+  int n_live = 0;
 };
 
 constexpr unsigned long long kDefaultWaitTimeoutNs = 2000ull * 1000 * 1000;  // 2 s per wait
@@ -136,7 +146,8 @@ cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causa
 // Transposed plan (per key block, the ascending live query blocks); d_counts
 // is scratch of R ints.
 cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
-                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream, int mdiv = 1);
+                     int* d_live_off, int* d_totals, int* d_col_ptr, int* d_row_idx,
+                     int* d_kv_order, int nsm, cudaStream_t stream, int mdiv = 1);
 // Heads per schedule chunk for S/128 = nb key blocks per head.
 int schedule_chunk_heads(int nb);
 

@@ -138,10 +138,13 @@ __global__ void fill_kernel(const uint8_t* __restrict__ mask, int rows, int nb, 
 // k).  Empty tiles are listed head by head, qb ascending.  With kdiv = 2
 // (64-key blocks, run in pairs) a tile's length is its pairs,
 // ceil(live blocks / 2), and a chunk's blocks count in pairs likewise.
+// With empty_rev > 0, empty tile number e is written to
+// empty_tiles[empty_rev - 1 - e] instead of empty_tiles[e] (so that one array
+// of empty_rev entries holds the live tiles in order followed by the empty ones).
 __global__ void __launch_bounds__(1024)
     order_kernel(const int* __restrict__ row_ptr, const int* __restrict__ live_off, int BH, int nb,
                  int kdiv, int kh, int nsm, int* __restrict__ tile_order,
-                 int* __restrict__ empty_tiles) {
+                 int* __restrict__ empty_tiles, int empty_rev) {
   extern __shared__ uint32_t keys[];
   __shared__ int n_in, n_moved;
   const int k = blockIdx.x;
@@ -212,7 +215,10 @@ __global__ void __launch_bounds__(1024)
       const int r = h * nb + qb;
       const bool empty = qb < nb && row_ptr[r + 1] == row_ptr[r];
       const unsigned bal = __ballot_sync(0xffffffffu, empty);
-      if (empty) empty_tiles[pos + __popc(bal & ((1u << lane) - 1u))] = r;
+      if (empty) {
+        const int e = pos + __popc(bal & ((1u << lane) - 1u));
+        empty_tiles[empty_rev > 0 ? empty_rev - 1 - e : e] = r;
+      }
       pos += __popc(bal);
     }
   }
@@ -226,7 +232,8 @@ __device__ __forceinline__ bool col_live(const uint8_t* mask_bh, int nb, int qb,
 }
 
 __global__ void csc_count_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
-                                 int mdiv, int* __restrict__ counts) {
+                                 int mdiv, int* __restrict__ counts,
+                                 int* __restrict__ live_per_head) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= cols) return;
@@ -235,13 +242,10 @@ __global__ void csc_count_kernel(const uint8_t* __restrict__ mask, int cols, int
   int c = 0;
   for (int qb = lane; qb < nb; qb += 32) c += col_live(mbh, nb, qb, kb, causal) ? 1 : 0;
   c = __reduce_add_sync(0xffffffffu, c);
-  if (lane == 0) counts[warp] = c;
-}
-
-__global__ void __launch_bounds__(kScanThreads)
-    csc_scan_kernel(const int* __restrict__ counts, int cols, int* __restrict__ col_ptr) {
-  __shared__ long long sh[kScanThreads];
-  block_exclusive_scan(counts, col_ptr, cols, sh);
+  if (lane == 0) {
+    counts[warp] = c;
+    if (c > 0) atomicAdd(&live_per_head[warp / nb], 1);
+  }
 }
 
 __global__ void csc_fill_kernel(const uint8_t* __restrict__ mask, int cols, int nb, int causal,
@@ -296,20 +300,33 @@ cudaError_t plan_fill_and_order(const uint8_t* d_mask, int BH, int nb, int causa
   int n2 = 1;
   while (n2 < 2 * kh * nb) n2 <<= 1;
   order_kernel<<<chunks, 1024, sizeof(uint32_t) * n2, stream>>>(
-      d_row_ptr, d_live_off, BH, nb, kdiv, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles);
+      d_row_ptr, d_live_off, BH, nb, kdiv, kh, nsm > 0 ? nsm : 1, d_tile_order, d_empty_tiles, 0);
   return cudaGetLastError();
 }
 
 cudaError_t plan_csc(const uint8_t* d_mask, int BH, int nb, int causal, int* d_counts,
-                     int* d_col_ptr, int* d_row_idx, cudaStream_t stream, int mdiv) {
+                     int* d_live_off, int* d_totals, int* d_col_ptr, int* d_row_idx,
+                     int* d_kv_order, int nsm, cudaStream_t stream, int mdiv) {
   const int cols = BH * nb;
+  int* live_per_head = d_counts + cols;  // caller sized d_counts as cols + BH
+  cudaError_t e = cudaMemsetAsync(live_per_head, 0, sizeof(int) * BH, stream);
+  if (e != cudaSuccess) return e;
   const int warps_per_block = 8;
   const int grid = (cols + warps_per_block - 1) / warps_per_block;
   csc_count_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, mdiv,
-                                                              d_counts);
-  csc_scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, cols, d_col_ptr);
+                                                              d_counts, live_per_head);
+  scan_kernel<<<1, kScanThreads, 0, stream>>>(d_counts, cols, live_per_head, BH, d_col_ptr,
+                                              d_live_off, reinterpret_cast<long long*>(d_totals));
   csc_fill_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(d_mask, cols, nb, causal, mdiv,
                                                              d_col_ptr, d_row_idx);
+  // the key tiles for the dK/dV kernel: the same longest-first order within
+  // head chunks as the forward tiles, empty key tiles at the end
+  const int kh = schedule_chunk_heads(nb);
+  const int chunks = (BH + kh - 1) / kh;
+  int n2 = 1;
+  while (n2 < 2 * kh * nb) n2 <<= 1;
+  order_kernel<<<chunks, 1024, sizeof(uint32_t) * n2, stream>>>(
+      d_col_ptr, d_live_off, BH, nb, 1, kh, nsm > 0 ? nsm : 1, d_kv_order, d_kv_order, cols);
   return cudaGetLastError();
 }
 
