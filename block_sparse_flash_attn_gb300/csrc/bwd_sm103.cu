@@ -50,6 +50,7 @@
 // timeout and the CTA drains its copies and MMAs before it frees tensor memory.
 #include <atomic>
 #include <cstdint>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -497,24 +498,32 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
         const float4* l4 = reinterpret_cast<const float4*>(vl + 32 * (ch & 1));
         const float4* d4 = reinterpret_cast<const float4*>(vd + 32 * (ch & 1));
         uint32_t pk[16], dk[16];
+        // the causal diagonal block in its own copy of the loop, so that the
+        // loop of every other block has no test in it
+        auto chunk = [&](auto diag_c) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 l = l4[i >> 2];  // same address in every lane: a broadcast
-          const float4 d = d4[i >> 2];
-          const float lq[4] = {l.x, l.y, l.z, l.w};
-          const float dq[4] = {d.x, d.y, d.z, d.w};
-          float pe[4], de[4];
+          for (int i = 0; i < 32; i += 4) {
+            const float4 l = l4[i >> 2];  // same address in every lane: a broadcast
+            const float4 d = d4[i >> 2];
+            const float lq[4] = {l.x, l.y, l.z, l.w};
+            const float dq[4] = {d.x, d.y, d.z, d.w};
+            float pe[4], de[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            pe[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sl, -lq[e]));
-            if (diag) pe[e] = r > ch * 32 + i + e ? 0.f : pe[e];
-            de[e] = pe[e] * (__uint_as_float(dp[i + e]) - dq[e]);
+            for (int e = 0; e < 4; ++e) {
+              pe[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sl, -lq[e]));
+              if constexpr (decltype(diag_c)::value) pe[e] = r > ch * 32 + i + e ? 0.f : pe[e];
+              de[e] = pe[e] * (__uint_as_float(dp[i + e]) - dq[e]);
+            }
+            pk[i >> 1] = pack_bf16x2(pe[0], pe[1]);
+            pk[(i >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
+            dk[i >> 1] = pack_bf16x2(de[0], de[1]);
+            dk[(i >> 1) + 1] = pack_bf16x2(de[2], de[3]);
           }
-          pk[i >> 1] = pack_bf16x2(pe[0], pe[1]);
-          pk[(i >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
-          dk[i >> 1] = pack_bf16x2(de[0], de[1]);
-          dk[(i >> 1) + 1] = pack_bf16x2(de[2], de[3]);
-        }
+        };
+        if (diag)
+          chunk(std::true_type{});
+        else
+          chunk(std::false_type{});
         const uint32_t col = C::kHalfStride * h + 16u * (ch & 1);
         tmem_st32_16(tmem + C::kTP + lane_off + col, pk);
         tmem_st32_16(tmem + C::kTdS + lane_off + col, dk);
@@ -811,18 +820,25 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
         reg_fence(sv, 32);
         reg_fence(dp, 32);
         uint32_t dk[16];
+        // the causal diagonal block in its own copy of the loop
+        auto chunk = [&](auto diag_c) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int c = ch * 32 + i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l2));
-          if (diag) {
-            p0 = c > r ? 0.f : p0;
-            p1 = c + 1 > r ? 0.f : p1;
+          for (int i = 0; i < 32; i += 2) {
+            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l2));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l2));
+            if constexpr (decltype(diag_c)::value) {
+              const int c = ch * 32 + i;
+              p0 = c > r ? 0.f : p0;
+              p1 = c + 1 > r ? 0.f : p1;
+            }
+            dk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - dlr),
+                                     p1 * (__uint_as_float(dp[i + 1]) - dlr));
           }
-          dk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - dlr),
-                                   p1 * (__uint_as_float(dp[i + 1]) - dlr));
-        }
+        };
+        if (diag)
+          chunk(std::true_type{});
+        else
+          chunk(std::false_type{});
         tmem_st32_16(tmem + C::kTdS + lane_off + (uint32_t)(32 * h + 16 * (ch & 1)), dk);
       }
       tmem_wait_st();
