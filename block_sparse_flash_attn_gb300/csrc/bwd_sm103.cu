@@ -122,32 +122,47 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 
 
-// Dl_i = dO_i . O_i (fp32 over the stored O and dO); one warp per row.
+// Dl_i = dO_i . O_i (fp32 over the stored O and dO).  Each lane takes 8
+// consecutive elements of a row with 16-byte loads (D / 8 lanes per row,
+// 32 / (D / 8) rows per warp); the lanes of a row add their partial sums.
 template <int D, bool O_F32>
 __global__ void bwd_prep_kernel(const void* __restrict__ o, const uint16_t* __restrict__ dout,
                                 float* __restrict__ dl, long long rows) {
-  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int kLanes = D / 8;
+  constexpr int kRowsPerWarp = 32 / kLanes;
+  const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;  // elements per lane: 4 (D = 128) or 2 (D = 64)
-  const size_t base = (size_t)row * D + (size_t)lane * kPer;
+  const long long row = gwarp * kRowsPerWarp + lane / kLanes;
   float acc = 0.f;
+  if (row < rows) {
+    const size_t base = (size_t)row * D + (size_t)(lane % kLanes) * 8;
+    const uint4 gv = *reinterpret_cast<const uint4*>(dout + base);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    float x[8];
+    if constexpr (O_F32) {
+      const float4 a = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + base);
+      const float4 b =
+          *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(o) + base + 4);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+      x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+      const uint4 ov = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(o) + base);
+      const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w};
 #pragma unroll
-  for (int e = 0; e < kPer; ++e) {
-    const float g = __uint_as_float((uint32_t)dout[base + e] << 16);
-    float x;
-    if constexpr (O_F32)
-      x = reinterpret_cast<const float*>(o)[base + e];
-    else
-      x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(o)[base + e] << 16);
-    acc = fmaf(g, x, acc);
+      for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __uint_as_float(ow[e] << 16);
+        x[2 * e + 1] = __uint_as_float(ow[e] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(__uint_as_float(gw[e] << 16), x[2 * e], acc);
+      acc = fmaf(__uint_as_float(gw[e] & 0xFFFF0000u), x[2 * e + 1], acc);
+    }
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 16);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 8);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  if (lane == 0) dl[row] = acc;
+#pragma unroll
+  for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && lane % kLanes == 0) dl[row] = acc;
 }
 
 __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
@@ -255,14 +270,11 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     }
     return;
   }
-  // The plan's lists must hold valid query blocks; anything else is an internal error.
+  // The plan's lists must hold valid query blocks; anything else is an
+  // internal error.  The list lengths are checked here; each entry is
+  // checked where the load warp reads it (and never used out of range).
   bool bad = n > p.nb * g;
   for (int gi = 0; !bad && gi < g; ++gi) bad = g_st[gi + 1] - g_st[gi] > p.nb;
-  for (int i = tid; !bad && i < n; i += kBwdKvThreads) {
-    int bhq = 0, qb = 0;
-    entry(i, bhq, qb);
-    bad = qb < 0 || qb >= p.nb || (p.causal && qb < kb);
-  }
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(p.status, kStatusInternal);
     return;
@@ -398,6 +410,11 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
       if (w0 + lane < n) {
         int bhq = 0, qbi = 0;
         entry(w0 + lane, bhq, qbi);
+        if (qbi < 0 || qbi >= p.nb || (p.causal && qbi < kb)) {  // not a valid list entry
+          atomicOr(p.status, kStatusInternal);
+          *abort_flag = 1;
+          qbi = 0;
+        }
         row = bhq * p.S + qbi * kBlock;
       }
       return row;
@@ -468,6 +485,7 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     auto fetch = [&](int i) {
       int bhq = 0;
       entry(i, bhq, qb_next);
+      if (qb_next < 0 || qb_next >= p.nb) qb_next = 0;  // reported by the load warp
       const int qrow = bhq * p.S + qb_next * kBlock + 64 * h + lane;
       la_next = p.lse[qrow] * kLog2e;
       lb_next = p.lse[qrow + 32] * kLog2e;
@@ -626,11 +644,8 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
       dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  bool bad = n > p.nb;
-  for (int i = tid; !bad && i < n; i += kBwdKvThreads) {
-    const int kb = p.col_idx[r0 + i];
-    bad = kb < 0 || kb >= p.nb || (p.causal && kb > qb);
-  }
+  // The list length is checked here; each entry where the load warp reads it.
+  const bool bad = n > p.nb;
   if (__syncthreads_or(bad)) {
     if (tid == 0) atomicOr(p.status, kStatusInternal);
     return;
@@ -748,7 +763,14 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
     // First K/V row of each key block of the list, 32 per window held one per
     // lane; the next window is loaded a window ahead.
     auto window_rows = [&](int w0) {
-      return w0 + lane < n ? kvbh * p.S + p.col_idx[r0 + w0 + lane] * kBlock : 0;
+      if (w0 + lane >= n) return 0;
+      int kbi = p.col_idx[r0 + w0 + lane];
+      if (kbi < 0 || kbi >= p.nb || (p.causal && kbi > qb)) {  // not a valid list entry
+        atomicOr(p.status, kStatusInternal);
+        *abort_flag = 1;
+        kbi = 0;
+      }
+      return kvbh * p.S + kbi * kBlock;
     };
     int win0 = 0;
     int row_cur = window_rows(0), row_next = window_rows(32);
@@ -910,7 +932,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
                             long long rows, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
-  const long long blocks = (rows + 7) / 8;  // 8 warps (rows) per 256-thread block
+  const long long per_block = 8 * (32 / (D / 8));  // 8 warps, 32 / (D / 8) rows each
+  const long long blocks = (rows + per_block - 1) / per_block;
   const uint16_t* g = static_cast<const uint16_t*>(dout);
   if (D == 128) {
     if (o_f32) bwd_prep_kernel<128, true><<<(unsigned)blocks, 256, 0, stream>>>(o, g, dl, rows);
