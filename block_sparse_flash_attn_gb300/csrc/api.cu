@@ -417,9 +417,7 @@ bsattn_status bsattn_bwd_gqa(const void* q, const void* k, const void* v, const 
   cudaError_t e = launch_bwd_prep(D, (plan->flags & BSATTN_OUT_F32) != 0, o, dout, plan->dev.dl,
                                   rows, st);
   if (e != cudaSuccess) return from_cuda(e);
-  if ((e = launch_bwd(D, tq, tk, tv, tdo, prm, B * Hkv * plan->nb, st)) != cudaSuccess)
-    return from_cuda(e);
-  return from_cuda(launch_bwd_dq(D, tq, tk, tv, tdo, prm, B * H * plan->nb, st));
+  return from_cuda(launch_bwd(D, tq, tk, tv, tdo, prm, B * Hkv * plan->nb, B * H * plan->nb, st));
 }
 
 bsattn_status bsattn_bwd(const void* q, const void* k, const void* v, const void* o,

@@ -213,19 +213,18 @@ __device__ __forceinline__ void store_rows32(uint32_t taddr, float scale, float*
   __syncwarp();  // the piece is read before the next one is written
 }
 
+// One CTA of dK, dV: key tile number `cta` of the launch order.
 template <int D>
-__global__ void __launch_bounds__(kBwdKvThreads, 1)
-    bsattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                      const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+__device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                           const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                           const BwdParams& p, int cta) {
   using C = BwdCfg<D>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
   // (b * Hkv + hk) * nb + kb: a key tile of K/V head hk; long tiles first
-  const int tile = p.kv_group == 1 ? p.kv_order[blockIdx.x] : (int)blockIdx.x;
+  const int tile = p.kv_group == 1 ? p.kv_order[cta] : cta;
   const int kvbh = tile / p.nb;
   const int kb = tile - kvbh * p.nb;
   const int g = p.kv_group;     // query heads reading this K/V head
@@ -617,20 +616,18 @@ struct __align__(8) DqBars {
 };
 static_assert(sizeof(DqBars) <= 256, "barrier block must fit its 256-byte region");
 
+// One CTA of dQ: query tile number `cta` of the launch order.
 template <int D>
-__global__ void __launch_bounds__(kBwdKvThreads, 1)
-    bsattn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
-                         const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v,
-                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+__device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                           const CUtensorMap& tm_v, const CUtensorMap& tm_do,
+                                           const BwdParams& p, int cta) {
   using C = DqCfg<D>;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
   // warps 0-7: CUDA-core work, half h = warps 4h .. 4h+3; kMmaWarp, kLoadWarp
   // (b * H + h) * nb + qb: the forward plan's tiles, long ones first, then the empty ones
-  const int tile = (int)blockIdx.x < p.n_live ? p.tile_order[blockIdx.x]
-                                              : p.empty_tiles[blockIdx.x - p.n_live];
+  const int tile = cta < p.n_live ? p.tile_order[cta] : p.empty_tiles[cta - p.n_live];
   const int bh = tile / p.nb;
   const int qb = tile - bh * p.nb;
   const int r0 = p.row_ptr[tile];
@@ -889,31 +886,27 @@ __global__ void __launch_bounds__(kBwdKvThreads, 1)
   }
 }
 
+// The backward pass in one launch: CTAs 0 .. n_kv-1 compute dK, dV (key
+// tiles, longest first), the rest dQ (query tiles, longest first), so that
+// the hardware's CTA scheduler fills the end of the one with the other.
 template <int D>
-cudaError_t launch_bwd_dq_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, int grid,
-                            cudaStream_t stream) {
-  static std::atomic<bool> opted_in[64];
-  const size_t smem = DqCfg<D>::kSmem + 1024;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!opted_in[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(bsattn_bwd_dq_kernel<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    opted_in[dev].store(true, std::memory_order_release);
-  }
-  bsattn_bwd_dq_kernel<D><<<grid, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p);
-  return cudaGetLastError();
+__global__ void __launch_bounds__(kBwdKvThreads, 1)
+    bsattn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v,
+                      const __grid_constant__ CUtensorMap tm_do, const BwdParams p, int n_kv) {
+  if ((int)blockIdx.x < n_kv)
+    bwd_kv_cta<D>(tm_q, tm_k, tm_v, tm_do, p, (int)blockIdx.x);
+  else
+    bwd_dq_cta<D>(tm_q, tm_k, tm_v, tm_do, p, (int)blockIdx.x - n_kv);
 }
 
 template <int D>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdParams& p, int grid,
+                         const CUtensorMap& tdo, const BwdParams& p, int n_kv, int n_q,
                          cudaStream_t stream) {
   static std::atomic<bool> opted_in[64];
-  const size_t smem = BwdCfg<D>::kSmem + 1024;
+  const size_t smem = (BwdCfg<D>::kSmem > DqCfg<D>::kSmem ? BwdCfg<D>::kSmem : DqCfg<D>::kSmem) + 1024;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -923,7 +916,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_bwd_kernel<D><<<grid, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p);
+  bsattn_bwd_kernel<D><<<n_kv + n_q, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p, n_kv);
   return cudaGetLastError();
 }
 
@@ -946,18 +939,11 @@ cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, 
 }
 
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
-  return D == 128 ? launch_bwd_t<128>(tq, tk, tv, tdo, p, grid, stream)
-                  : launch_bwd_t<64>(tq, tk, tv, tdo, p, grid, stream);
-}
-
-cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                          int grid, cudaStream_t stream) {
-  if (grid <= 0) return cudaSuccess;
-  return D == 128 ? launch_bwd_dq_t<128>(tq, tk, tv, tdo, p, grid, stream)
-                  : launch_bwd_dq_t<64>(tq, tk, tv, tdo, p, grid, stream);
+                       const CUtensorMap& tdo, const BwdParams& p, int n_kv, int n_q,
+                       cudaStream_t stream) {
+  if (n_kv + n_q <= 0) return cudaSuccess;
+  return D == 128 ? launch_bwd_t<128>(tq, tk, tv, tdo, p, n_kv, n_q, stream)
+                  : launch_bwd_t<64>(tq, tk, tv, tdo, p, n_kv, n_q, stream);
 }
 
 }  // namespace bsattn

@@ -164,10 +164,10 @@ cudaError_t launch_selftest_wait(unsigned long long timeout_ns, int* d_status,
 cudaError_t launch_bwd_prep(int D, bool o_f32, const void* o, const void* dout, float* dl,
                             long long rows, cudaStream_t stream);
 // dK, dV (grid: one CTA per key tile) and dQ (one CTA per query tile)
+// The backward pass: n_kv dK/dV CTAs (key tiles) and n_q dQ CTAs (query
+// tiles) in one launch.
 cudaError_t launch_bwd(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_bwd_dq(int D, const CUtensorMap& tq, const CUtensorMap& tk,
-                          const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                          int grid, cudaStream_t stream);
+                       const CUtensorMap& tdo, const BwdParams& p, int n_kv, int n_q,
+                       cudaStream_t stream);
 
 }  // namespace bsattn
