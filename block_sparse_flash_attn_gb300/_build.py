@@ -19,7 +19,7 @@ LIBDIR = os.path.join(_PKG, "_lib")
 LIB = os.path.join(LIBDIR, "libbsattn.so")
 
 SOURCES = ["api.cu", "plan.cu", "fwd_sm103.cu", "bwd_sm103.cu", "noalloc.cu", "pipeline.cu"]
-HEADERS = ["ptx.cuh", "internal.h"]
+HEADERS = ["ptx.cuh", "internal.h", "bwd.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

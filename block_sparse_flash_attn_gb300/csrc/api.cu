@@ -10,6 +10,7 @@
 
 #include <cudaTypedefs.h>
 
+#include "bwd.h"
 #include "internal.h"
 
 using namespace bsattn;

@@ -52,6 +52,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "bwd.h"
 #include "internal.h"
 #include "ptx.cuh"
 
