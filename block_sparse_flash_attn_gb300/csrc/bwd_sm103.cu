@@ -237,6 +237,38 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* const sbase = smem_raw + (base - raw);
+  BwdBars* bars = reinterpret_cast<BwdBars*>(sbase + C::kBarOff);
+  const uint64_t lim = p.timeout_ns;
+  volatile int* abort_flag = &bars->abort_flag;
+  // Barriers first, then the tile's K and V: they need nothing but the tile,
+  // so their load overlaps the list and tensor-memory set-up below.
+  if (tid == 0) {
+    mbar_init(smem_u32(&bars->kv_full), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(smem_u32(&bars->qd_full[h][0]), C::kSep ? 1 : 2);
+      mbar_init(smem_u32(&bars->qd_full[h][1]), C::kSep ? 1 : 2);
+      mbar_init(smem_u32(&bars->qd_empty[h][0]), 1);
+      mbar_init(smem_u32(&bars->qd_empty[h][1]), 1);
+      mbar_init(smem_u32(&bars->st_done[h]), 1);
+      mbar_init(smem_u32(&bars->pds_done[h]), 4);  // the half's four warps
+    }
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    const uint32_t bar = smem_u32(&bars->kv_full);
+    mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+      for (int c = 0; c < C::kBoxes; ++c) {
+        const uint32_t off = (uint32_t)(hh * C::kHalfBoxBytes + c * C::kBoxBytes);
+        tma_load_2d(base + C::kKOff + off, &tm_k, bar, c * 64, krow0 + 64 * hh);
+        tma_load_2d(base + C::kVOff + off, &tm_v, bar, c * 64, krow0 + 64 * hh);
+      }
+  }
   // The CTA walks the transposed lists of the group's query heads one after
   // the other: head bh0 + i contributes entries [g_st[i], g_st[i+1]) of the
   // walk, starting at row_idx[g_c0[i]].
@@ -268,6 +300,7 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
       dk4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       dv4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    if (tid == 0) bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);  // the K/V copy lands first
     return;
   }
   // The plan's lists must hold valid query blocks; anything else is an
@@ -276,32 +309,13 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
   bool bad = n > p.nb * g;
   for (int gi = 0; !bad && gi < g; ++gi) bad = g_st[gi + 1] - g_st[gi] > p.nb;
   if (__syncthreads_or(bad)) {
-    if (tid == 0) atomicOr(p.status, kStatusInternal);
+    if (tid == 0) {
+      atomicOr(p.status, kStatusInternal);
+      bwd_drain_wait(smem_u32(&bars->kv_full), 0, lim);
+    }
     return;
   }
 
-  BwdBars* bars = reinterpret_cast<BwdBars*>(sbase + C::kBarOff);
-  const uint64_t lim = p.timeout_ns;
-  volatile int* abort_flag = &bars->abort_flag;
-
-  if (tid == 0) {
-    mbar_init(smem_u32(&bars->kv_full), 1);
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(smem_u32(&bars->qd_full[h][0]), C::kSep ? 1 : 2);
-      mbar_init(smem_u32(&bars->qd_full[h][1]), C::kSep ? 1 : 2);
-      mbar_init(smem_u32(&bars->qd_empty[h][0]), 1);
-      mbar_init(smem_u32(&bars->qd_empty[h][1]), 1);
-      mbar_init(smem_u32(&bars->st_done[h]), 1);
-      mbar_init(smem_u32(&bars->pds_done[h]), 4);  // the half's four warps
-    }
-    mbar_init(smem_u32(&bars->drain), 1);
-    bars->abort_flag = 0;
-    fence_mbar_init();
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
-  }
   if (warp == 0) {
     tmem_alloc(smem_u32(&bars->tmem_base), kBwdTmemCols);
     tmem_relinquish();
@@ -421,15 +435,7 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
     };
     int win0 = 0;
     int row_cur = window_rows(0), row_next = window_rows(32);
-    if (elect_one()) {
-      const uint32_t bar = smem_u32(&bars->kv_full);
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      for (int hh = 0; hh < 2; ++hh) {
-        load_half(&tm_k, base + C::kKOff + hh * C::kHalfBoxBytes, bar, krow0 + 64 * hh);
-        load_half(&tm_v, base + C::kVOff + hh * C::kHalfBoxBytes, bar, krow0 + 64 * hh);
-      }
-    }
-    __syncwarp();
+    // (K and V were loaded by thread 0 at the start)
     int loaded[2] = {0, 0};  // entries 0 .. loaded[h] - 1 loaded for half h
     for (int i = 0; ok && i < n; ++i) {
       while (i >= win0 + 32) {
@@ -631,30 +637,18 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
   const int tile = cta < p.n_live ? p.tile_order[cta] : p.empty_tiles[cta - p.n_live];
   const int bh = tile / p.nb;
   const int qb = tile - bh * p.nb;
-  const int r0 = p.row_ptr[tile];
-  const int n = p.row_ptr[tile + 1] - r0;
   const int qrow0 = bh * p.S + qb * kBlock;  // first query row of the tile
   const int kvbh =  // the K/V head it attends with
       p.kv_group > 1 ? (bh / p.H) * (p.H / p.kv_group) + (bh % p.H) / p.kv_group : bh;
-  if (n <= 0) {  // no live key block: dQ = 0
-    float4* dq4 = reinterpret_cast<float4*>(p.dq + (size_t)qrow0 * D);
-    for (int i = tid; i < kBlock * D / 4; i += kBwdKvThreads)
-      dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
-  }
-  // The list length is checked here; each entry where the load warp reads it.
-  const bool bad = n > p.nb;
-  if (__syncthreads_or(bad)) {
-    if (tid == 0) atomicOr(p.status, kStatusInternal);
-    return;
-  }
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   DqBars* bars = reinterpret_cast<DqBars*>(smem_raw + (base - raw) + C::kBarOff);
   const uint64_t lim = p.timeout_ns;
   volatile int* abort_flag = &bars->abort_flag;
+  const bool live = cta < p.n_live;  // the empty tiles come last
+  // Barriers first, then (for a live tile) its Q and dO: they need nothing
+  // but the tile, so their load overlaps the set-up below.
   if (tid == 0) {
     mbar_init(smem_u32(&bars->qd_full), 1);
     for (int h = 0; h < 2; ++h) {
@@ -672,6 +666,35 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
+    if (live) {
+      const uint32_t bar = smem_u32(&bars->qd_full);
+      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int c = 0; c < C::kBoxes; ++c) {
+          const uint32_t off = (uint32_t)(hh * C::kHalfBoxBytes + c * C::kBoxBytes);
+          tma_load_2d(base + C::kQOff + off, &tm_q, bar, c * 64, qrow0 + 64 * hh);
+          tma_load_2d(base + C::kdOOff + off, &tm_do, bar, c * 64, qrow0 + 64 * hh);
+        }
+    }
+  }
+  const int r0 = p.row_ptr[tile];
+  const int n = p.row_ptr[tile + 1] - r0;
+  if (n <= 0) {  // no live key block: dQ = 0
+    float4* dq4 = reinterpret_cast<float4*>(p.dq + (size_t)qrow0 * D);
+    for (int i = tid; i < kBlock * D / 4; i += kBwdKvThreads)
+      dq4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (tid == 0 && live) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
+    return;
+  }
+  // The list length is checked here; each entry where the load warp reads it.
+  const bool bad = n > p.nb;
+  if (__syncthreads_or(bad || !live)) {  // a tile with blocks sits among the live ones
+    if (tid == 0) {
+      atomicOr(p.status, kStatusInternal);
+      if (live) bwd_drain_wait(smem_u32(&bars->qd_full), 0, lim);
+    }
+    return;
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(&bars->tmem_base), kBwdTmemCols);
@@ -772,15 +795,7 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
     };
     int win0 = 0;
     int row_cur = window_rows(0), row_next = window_rows(32);
-    if (elect_one()) {
-      const uint32_t bar = smem_u32(&bars->qd_full);
-      mbar_arrive_expect_tx(bar, 2 * C::kTileBytes);
-      for (int hh = 0; hh < 2; ++hh) {
-        load_half(&tm_q, base + C::kQOff + hh * C::kHalfBoxBytes, bar, qrow0 + 64 * hh);
-        load_half(&tm_do, base + C::kdOOff + hh * C::kHalfBoxBytes, bar, qrow0 + 64 * hh);
-      }
-    }
-    __syncwarp();
+    // (Q and dO were loaded by thread 0 at the start)
     int loaded[2] = {0, 0};  // key blocks 0 .. loaded[h] - 1 loaded for half h
     for (int i = 0; ok && i < n; ++i) {
       while (i >= win0 + 32) {
