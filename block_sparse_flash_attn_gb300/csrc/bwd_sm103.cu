@@ -131,6 +131,9 @@ __global__ void bwd_prep_kernel(const void* __restrict__ o, const uint16_t* __re
                                 float* __restrict__ dl, long long rows) {
   constexpr int kLanes = D / 8;
   constexpr int kRowsPerWarp = 32 / kLanes;
+  // The backward kernel is launched as this kernel's programmatic dependent:
+  // it may start now; its warps that read Dl wait for this grid to finish.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long gwarp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long row = gwarp * kRowsPerWarp + lane / kLanes;
@@ -498,6 +501,9 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
       da_next = p.dl[qrow];
       db_next = p.dl[qrow + 32];
     };
+    // Dl is the row-term kernel's output: that grid must be complete (this
+    // kernel may have been launched before it finished).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     fetch(0);
     for (int j = 0; j < n; ++j) {
       const int qb = qb_next;
@@ -836,6 +842,9 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
     const int r = tid & (kBlock - 1);  // TMEM lane: query row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float l2 = p.lse[qrow0 + r] * kLog2e;  // this row's LSE in log2 units
+    // Dl is the row-term kernel's output: that grid must be complete (this
+    // kernel may have been launched before it finished).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const float dlr = p.dl[qrow0 + r];
     const float sl = p.scale_log2;
     const uint32_t tS = tmem + C::kTS + lane_off;
@@ -932,8 +941,20 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  bsattn_bwd_kernel<D><<<n_kv + n_q, kBwdKvThreads, smem, stream>>>(tq, tk, tv, tdo, p, n_kv);
-  return cudaGetLastError();
+  // A programmatic dependent of the row-term kernel launched just before it
+  // on the stream: the CTAs start while that kernel finishes; the warps that
+  // read its output (Dl) wait for it with griddepcontrol.wait.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(n_kv + n_q));
+  cfg.blockDim = dim3(kBwdKvThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bsattn_bwd_kernel<D>, tq, tk, tv, tdo, p, n_kv);
 }
 
 }  // namespace
