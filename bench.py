@@ -116,6 +116,32 @@ def live_blocks(mask: np.ndarray, causal: bool) -> int:
     return int(np.count_nonzero(m))
 
 
+def allowed_pairs(mask: np.ndarray, causal: bool) -> int:
+    """(query, key) pairs the attention actually weighs: every pair of a
+    live block, except that under causal a diagonal block (128 x 128, or a
+    64-key block that reaches past its query rows) has only its pairs with
+    key <= query.  The metric counts whole live blocks; this is the exact
+    element count beside it."""
+    m = mask.astype(bool)
+    nbq, nbk = mask.shape[-2:]
+    kdiv = nbk // nbq
+    kb = 128 // kdiv
+    if not causal:
+        return int(np.count_nonzero(m)) * 128 * kb
+    qb = np.arange(nbq)[:, None]
+    kk = np.arange(nbk)[None, :]
+    # allowed pairs of block (qb, kk): query rows 128 qb + r, keys kb * kk + c, c <= ...
+    per = np.zeros((nbq, nbk), dtype=np.int64)
+    r = np.arange(128)
+    for off in range(kdiv):  # key blocks kk = kdiv * qb + off overlap the diagonal
+        first_key = kb * off  # relative to the query block's first row
+        per_diag = int(np.clip(r[:, None] - (first_key + np.arange(kb))[None, :] + 1, 0, 1).sum())
+        per[np.arange(nbq), kdiv * np.arange(nbq) + off] = per_diag
+    below = kk < kdiv * qb
+    per = np.where(below, 128 * kb, per)
+    return int((m * per[None, None]).sum())
+
+
 def flop_per_block(D: int, key_block: int = 128) -> int:
     return 4 * 128 * key_block * D
 
@@ -461,6 +487,7 @@ def run_ours(args):
         nbytes = algorithmic_bytes(mask, w.causal, w.S, w.D, 4 if out_f32 else 2,
                                    1 if fp8 else 2)
         entry = {"workload": f"{w.id}:{w.name}", "out_dtype": "f32" if out_f32 else "bf16",
+                 "flop_elementwise": allowed_pairs(mask, w.causal) * 4 * w.D,
                  "steps": steps_c, "ms_per_step": ms_max,
                  "value": whole_job_tflops(flop, world, ms_max), "unit": UNIT,
                  "wall_s_timed_region": wall,
@@ -542,6 +569,7 @@ def run_ours(args):
                        "out_dtype": "f32" if args.out_f32 else "bf16",
                        "key_block": args.key_block, "in_dtype": args.in_dtype,
                        "live_blocks": nlive, "flop_per_step": flop,
+                       "flop_elementwise": allowed_pairs(mask, w.causal) * 4 * w.D,
                        "l2": "flushed (512 MB write) before every timed step",
                        "parallelism": f"replicas x{world} (independent problems, no collective)"},
             "e2e": e2e,
