@@ -44,7 +44,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 # The parameter space: macro -> candidate values (the first is not special;
 # the library's defaults are the values compiled in without -D flags).
 SPACE = {
-    "BSATTN_EXP2_POLY_PAIRS": [0, 6, 8, 10, 12, 14, 16],
+    "BSATTN_EXP2_POLY_PAIRS": [0, 2, 4, 6, 8, 10, 12, 14, 16],
     "BSATTN_CLAIM_AHEAD": [2, 4, 6],
     "BSATTN_SCHED_CHUNK_BLOCKS": [384, 768, 1536],
     "BSATTN_D128_QSTAGES": [1, 2],
