@@ -483,10 +483,11 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
     const int r = tid & (kBlock - 1);  // TMEM lane: key row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // this warp's TMEM lanes
     const float sl = p.scale_log2;
+    const uint64_t sl2 = f2_pack(sl, sl);
     const uint32_t tS = tmem + C::kTS + lane_off;
     const uint32_t tdP = tmem + C::kTdP + lane_off;
-    float* vl = reinterpret_cast<float*>(sbase + C::kVecOff + warp * C::kVecBytes);  // [64] LSE
-    float* vd = vl + 64;                                                             // [64] Dl
+    float* vl = reinterpret_cast<float*>(sbase + C::kVecOff + warp * C::kVecBytes);  // [64] -LSE log2 e
+    float* vd = vl + 64;                                                             // [64] -Dl
     // LSE and Dl of the half's queries 64h + lane and 64h + 32 + lane of
     // entry i, loaded one entry ahead
     float la_next = 0.f, lb_next = 0.f, da_next = 0.f, db_next = 0.f;
@@ -496,10 +497,10 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
       entry(i, bhq, qb_next);
       if (qb_next < 0 || qb_next >= p.nb) qb_next = 0;  // reported by the load warp
       const int qrow = bhq * p.S + qb_next * kBlock + 64 * h + lane;
-      la_next = p.lse[qrow] * kLog2e;
-      lb_next = p.lse[qrow + 32] * kLog2e;
-      da_next = p.dl[qrow];
-      db_next = p.dl[qrow + 32];
+      la_next = -p.lse[qrow] * kLog2e;  // held negated: the loop adds them
+      lb_next = -p.lse[qrow + 32] * kLog2e;
+      da_next = -p.dl[qrow];
+      db_next = -p.dl[qrow + 32];
     };
     // Dl is the row-term kernel's output: that grid must be complete (this
     // kernel may have been launched before it finished).
@@ -525,29 +526,39 @@ __device__ __forceinline__ void bwd_kv_cta(const CUtensorMap& tm_q, const CUtens
         tmem_wait_ld();
         reg_fence(sv, 32);
         reg_fence(dp, 32);
+        // -LSE log2 e and -Dl of the chunk's queries
         const float4* l4 = reinterpret_cast<const float4*>(vl + 32 * (ch & 1));
         const float4* d4 = reinterpret_cast<const float4*>(vd + 32 * (ch & 1));
         uint32_t pk[16], dk[16];
         // the causal diagonal block in its own copy of the loop, so that the
-        // loop of every other block has no test in it
+        // loop of every other block has no test in it; pairs of queries with
+        // packed f32x2 arithmetic
         auto chunk = [&](auto diag_c) {
 #pragma unroll
           for (int i = 0; i < 32; i += 4) {
             const float4 l = l4[i >> 2];  // same address in every lane: a broadcast
             const float4 d = d4[i >> 2];
-            const float lq[4] = {l.x, l.y, l.z, l.w};
-            const float dq[4] = {d.x, d.y, d.z, d.w};
-            float pe[4], de[4];
+            const uint64_t nl[2] = {f2_pack(l.x, l.y), f2_pack(l.z, l.w)};
+            const uint64_t nd[2] = {f2_pack(d.x, d.y), f2_pack(d.z, d.w)};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              pe[e] = ex2_approx(fmaf(__uint_as_float(sv[i + e]), sl, -lq[e]));
-              if constexpr (decltype(diag_c)::value) pe[e] = r > ch * 32 + i + e ? 0.f : pe[e];
-              de[e] = pe[e] * (__uint_as_float(dp[i + e]) - dq[e]);
+            for (int e = 0; e < 4; e += 2) {
+              const uint64_t x2 = f2_fma(
+                  f2_pack(__uint_as_float(sv[i + e]), __uint_as_float(sv[i + e + 1])), sl2,
+                  nl[e >> 1]);
+              float x0, x1;
+              f2_unpack(x2, x0, x1);
+              float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if constexpr (decltype(diag_c)::value) {
+                p0 = r > ch * 32 + i + e ? 0.f : p0;
+                p1 = r > ch * 32 + i + e + 1 ? 0.f : p1;
+              }
+              const uint64_t dd2 = f2_add(
+                  f2_pack(__uint_as_float(dp[i + e]), __uint_as_float(dp[i + e + 1])), nd[e >> 1]);
+              float d0, d1;
+              f2_unpack(f2_mul(f2_pack(p0, p1), dd2), d0, d1);
+              pk[(i + e) >> 1] = pack_bf16x2(p0, p1);
+              dk[(i + e) >> 1] = pack_bf16x2(d0, d1);
             }
-            pk[i >> 1] = pack_bf16x2(pe[0], pe[1]);
-            pk[(i >> 1) + 1] = pack_bf16x2(pe[2], pe[3]);
-            dk[i >> 1] = pack_bf16x2(de[0], de[1]);
-            dk[(i >> 1) + 1] = pack_bf16x2(de[2], de[3]);
           }
         };
         if (diag)
@@ -842,11 +853,14 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
     const int r = tid & (kBlock - 1);  // TMEM lane: query row
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const float l2 = p.lse[qrow0 + r] * kLog2e;  // this row's LSE in log2 units
+    const uint64_t nl2 = f2_pack(-l2, -l2);
     // Dl is the row-term kernel's output: that grid must be complete (this
     // kernel may have been launched before it finished).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const float dlr = p.dl[qrow0 + r];
+    const uint64_t nd2 = f2_pack(-dlr, -dlr);
     const float sl = p.scale_log2;
+    const uint64_t sl2 = f2_pack(sl, sl);
     const uint32_t tS = tmem + C::kTS + lane_off;
     const uint32_t tdP = tmem + C::kTdP + lane_off;
     for (int j = 0; j < n; ++j) {
@@ -867,16 +881,22 @@ __device__ __forceinline__ void bwd_dq_cta(const CUtensorMap& tm_q, const CUtens
         // the causal diagonal block in its own copy of the loop
         auto chunk = [&](auto diag_c) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float p0 = ex2_approx(fmaf(__uint_as_float(sv[i]), sl, -l2));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sv[i + 1]), sl, -l2));
+          for (int i = 0; i < 32; i += 2) {  // pairs of keys with packed f32x2 arithmetic
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1])), sl2, nl2);
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if constexpr (decltype(diag_c)::value) {
               const int c = ch * 32 + i;
               p0 = c > r ? 0.f : p0;
               p1 = c + 1 > r ? 0.f : p1;
             }
-            dk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - dlr),
-                                     p1 * (__uint_as_float(dp[i + 1]) - dlr));
+            const uint64_t dd2 =
+                f2_add(f2_pack(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), nd2);
+            float d0, d1;
+            f2_unpack(f2_mul(f2_pack(p0, p1), dd2), d0, d1);
+            dk[i >> 1] = pack_bf16x2(d0, d1);
           }
         };
         if (diag)
