@@ -173,9 +173,9 @@ struct Cfg {
   // its load; with e4m3 inputs they convert it into the fp16 ring; at
   // D = 128 with bf16 inputs P V stays in bf16.
   static constexpr bool kF16PV = D == 64 || IN8;
-  // A row's block sum above this (formed against a stale reference) makes the
-  // softmax redo the block with its max; in fp16 it also keeps every P below
-  // fp16's largest finite value: each P <= the sum <= 2^15.
+  // A half row's block sum above this (formed against a stale reference)
+  // makes the softmax redo the block with its max; in fp16 it also keeps every
+  // P below fp16's largest finite value: each P <= its half's sum <= 2^15.
   static constexpr float kGrowSum = kF16PV ? 32768.0f : 4294967296.0f;
   static constexpr int kOnesOff = kVOff + kBoxes * kVGroup;
   static constexpr int kBarOff = kOnesOff + (kOnes ? kVStages * kBoxBytes : 0);
@@ -830,6 +830,8 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
   write_empty_tiles<D, OUT_F32>(p);
 
   int tq_cnt = 0, g = 0;  // g: blocks processed by this CTA (selects S buffer / ring stages)
+  int sb = 0;             // g % kSBufs: S buffer (and P barrier) of block g
+  uint32_t sph = 0;       // (g / kSBufs) & 1: phase of s_full[sb] for block g
   int ntile = 0;          // tiles handed to the epilogue warps
   for (;;) {
     const int e = tq_cnt & 1;
@@ -852,13 +854,10 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     uint64_t a2 = 0;            // partial sums of this half row: fp32 p (an f32x2 pair)
     float r32[2] = {0.f, 0.f};  // and bf16-rounded p
     for (int jb = 0; jb < n; ++jb, ++g) {
-      const int b = g % kSBufs;  // P barrier of this block
       // S(g) ready
-      if (!wait_warp(smem_u32(&bars->s_full[g % kSBufs]), (uint32_t)(g / kSBufs) & 1u,
-                     abort_flag, p.status, lim))
-        return;
+      if (!wait_warp(smem_u32(&bars->s_full[sb]), sph, abort_flag, p.status, lim)) return;
       tc_fence_after();
-      const uint32_t tS = tmem + kTmemS + (g % kSBufs) * 128 + lane_off;  // S buffer of this block
+      const uint32_t tS = tmem + kTmemS + sb * 128 + lane_off;  // S buffer of this block
       // Keys c (0..63) of this thread's half of the block with c > klim are
       // masked: the causal diagonal of 128-key blocks (key 64 ch + c allowed
       // for query row r iff it is <= r); with 64-key blocks in pairs, the
@@ -906,7 +905,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       };
       // After a tile's first block the probabilities are formed against the
       // current reference m without a max pass (any common reference gives
-      // the exact softmax).  Only when a row's sum over the block shows that
+      // the exact softmax).  Only when a half row's sum over the block shows that
       // its scores rose far above m (C::kGrowSum) -- or on the tile's first
       // block, where m = -inf -- is the block redone with its max, by the
       // lazy rule, as the new reference.  The redo reads the scores again
@@ -919,13 +918,15 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         uint32_t sr[64];
         load_scores(sr);
         exp_pass(sr, m);
+        // Each half row is tested on its own sum (no exchange with the other
+        // half on this path): a P element never exceeds its half's sum, so
+        // the bound that C::kGrowSum keeps on P holds all the same.
         float b0, b1;
         f2_unpack(b2, b0, b1);
-        float bs = b0 + b1;
-        bs += __shfl_xor_sync(0xffffffffu, bs, 16);  // the other half of the row
-        redo = __any_sync(0xffffffffu, !(bs <= C::kGrowSum));  // also catches inf / NaN
+        redo = __any_sync(0xffffffffu, !(b0 + b1 <= C::kGrowSum));  // also catches inf / NaN
       }
-      bool need = false;
+      bool need = false;     // this thread's row takes a new reference max
+      bool rescale = false;  // some row of the warp does (set on the redo path only)
       float f = 1.f;
       if (redo) {
         uint32_t sr[64];
@@ -934,6 +935,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));  // the other half of the row
         const float xm = mx * sl;
         need = xm > m + kTau;  // always true on the first block (m = -inf)
+        rescale = __any_sync(0xffffffffu, need);
         if (need) {
           f = ex2_approx(m - xm);  // 0 when m = -inf
           m = xm;
@@ -952,7 +954,7 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
 
       // O rescale (this thread's columns) when a row's max moved: first wait
       // until PV(g-1) has landed in O (PV(g) is not issued before P(g)).
-      if (jb > 0 && __any_sync(0xffffffffu, need)) {
+      if (jb > 0 && rescale) {
         if (!wait_warp(smem_u32(&bars->v_empty[(g - 1) % C::kVStages]),
                        (uint32_t)((g - 1) / C::kVStages) & 1u, abort_flag, p.status, lim))
           return;
@@ -979,7 +981,11 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();  // the warp's stores of P(g) are complete (each lane waited for its own)
-      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[b]));
+      if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[sb]));
+      if (++sb == kSBufs) {
+        sb = 0;
+        sph ^= 1u;
+      }
     }
 
     // Hand the tile over to the epilogue warps and go straight on to the next
