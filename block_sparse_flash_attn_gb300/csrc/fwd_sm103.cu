@@ -194,6 +194,8 @@ constexpr int kMaxStages = 3;  // deepest K / V ring of any Cfg
 // and softmax warps.
 struct TileInfo {
   int t;     // tile id (b*H + h)*nb + qb, or -1 when no tiles are left
+  int bh;    // its head b*H + h and query block qb (t = bh*nb + qb)
+  int qb;
   int r0;    // first CSR entry of the tile
   int n;     // blocks of the stream: live key blocks (64-key blocks: their pairs)
   int diag;  // causal and the last live block is the diagonal one (128-key blocks)
@@ -320,6 +322,8 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
     idx = __shfl_sync(0xffffffffu, idx, 0);
     const int t = idx < p.n_live ? p.tile_order[idx] : -1;
     int r0 = 0, cnt = 0, diag = 0, l0 = -1, l1 = -1;
+    const int bh = t >= 0 ? t / p.nb : 0;
+    const int qb = t - bh * p.nb;
     if (t >= 0) {
       if (t >= rows) {
         raise_internal(abort_flag, p.status);
@@ -334,7 +338,7 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
         break;
       }
       if constexpr (!KB64) {
-        diag = (p.causal && p.col_idx[r0 + cnt - 1] == t % p.nb) ? 1 : 0;
+        diag = (p.causal && p.col_idx[r0 + cnt - 1] == qb) ? 1 : 0;
       } else {
         l0 = cnt >= 2 ? p.col_idx[r0 + cnt - 2] : -1;
         l1 = p.col_idx[r0 + cnt - 1];
@@ -344,6 +348,8 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
     if (lane == 0) {
       volatile TileInfo* slot = &bars->tq[e];
       slot->t = t;
+      slot->bh = bh;
+      slot->qb = qb;
       slot->r0 = r0;
       slot->n = KB64 ? (cnt + 1) / 2 : cnt;
       slot->diag = diag;
@@ -364,8 +370,7 @@ __device__ void run_scheduler(const CUtensorMap* tm_q, const FwdParams& p, Bars*
       break;
     }
     if (elect_one()) {
-      const int bh = t / p.nb;
-      const int row = bh * p.S + (t - bh * p.nb) * kBlock;
+      const int row = bh * p.S + qb * kBlock;
       const uint32_t full = smem_u32(&bars->q_full[qs]);
       const uint32_t dst = smem_base + C::kQOff + qs * C::kQKBytes;
       mbar_arrive_expect_tx(full, C::kQKBytes);
@@ -839,6 +844,8 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     if (!wait_warp(smem_u32(&bars->tq_full[e]), ph, abort_flag, p.status, lim)) return;
     const volatile TileInfo* slot = &bars->tq[e];
     const int t = slot->t;
+    const int bh = slot->bh;
+    const int qb = slot->qb;
     const int n = slot->n;
     const int diag_last = slot->diag;
     const int n64 = slot->n64;
@@ -847,8 +854,6 @@ __device__ void run_softmax(const FwdParams& p, Bars* bars, uint32_t tmem,
     if (lane == 0) mbar_arrive(smem_u32(&bars->tq_empty[e]));
     ++tq_cnt;
     if (t < 0) return;
-    const int bh = t / p.nb;
-    const int qb = t - bh * p.nb;
 
     float m = __uint_as_float(kNegInf);  // running max of scale*log2(e)*score (lazy)
     uint64_t a2 = 0;            // partial sums of this half row: fp32 p (an f32x2 pair)
