@@ -36,7 +36,7 @@ EXPORTS = ["bsattn_plan", "bsattn_plan_csr", "bsattn_plan_schedule", "bsattn_fwd
            "bsattn_selftest_wait_timeout", "bsattn_fwd_noalloc", "bsattn_pipeline_create",
            "bsattn_pipeline_run", "bsattn_pipeline_status", "bsattn_pipeline_free",
            "bsattn_plan_csc", "bsattn_bwd", "bsattn_fwd_gqa", "bsattn_bwd_gqa",
-           "bsattn_fwd_fp8"]
+           "bsattn_fwd_fp8", "bsattn_plan_v16"]
 
 
 class BsattnError(RuntimeError):
@@ -82,6 +82,8 @@ def load():
     lib.bsattn_fwd_fp8.restype = i32
     lib.bsattn_plan_csc.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), ctypes.POINTER(i64)]
     lib.bsattn_plan_csc.restype = i32
+    lib.bsattn_plan_v16.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
+    lib.bsattn_plan_v16.restype = i32
     lib.bsattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32,
                                ctypes.c_float, vp]
     lib.bsattn_bwd.restype = i32
@@ -348,6 +350,14 @@ def plan_schedule(p: Plan):
     _check(load().bsattn_plan_schedule(p.handle, ctypes.byref(to), ctypes.byref(nl),
                                        ctypes.byref(et), ctypes.byref(ne)), "bsattn_plan_schedule")
     return _view_i32(to.value, nl.value), _view_i32(et.value, ne.value)
+
+
+def plan_v16_bytes(p: Plan) -> int:
+    """Size in bytes of the plan's fp16 copy of V (head_dim 64), 0 while none exists."""
+    ptr, nbytes = ctypes.c_void_p(), ctypes.c_size_t()
+    _check(load().bsattn_plan_v16(p.handle, ctypes.byref(ptr), ctypes.byref(nbytes)),
+           "bsattn_plan_v16")
+    return int(nbytes.value)
 
 
 def selftest_wait_timeout(timeout_ns: int = 1_000_000, stream=None) -> int:

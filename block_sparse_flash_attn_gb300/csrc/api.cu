@@ -117,6 +117,7 @@ void free_plan_memory(bsattn_plan_s* p) {
   cudaFree(p->dev.row_idx);
   cudaFree(p->dev.kv_order);
   cudaFree(p->dev.dl);
+  cudaFree(p->dev.v16);
   p->dev = PlanDevice{};
 }
 
@@ -126,7 +127,8 @@ namespace bsattn {
 
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf, int Hkv, bool in8, float v_scale) {
+                          PreparedFwd* pf, int Hkv, bool in8, float v_scale, bool v16_ok,
+                          cudaStream_t stream) {
   if (!plan_ok(plan) || !pf) return BSATTN_ERR_INVALID_ARG;
   if (!q || !k || !v || !out || !lse) return BSATTN_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
@@ -148,7 +150,39 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   auto encode = in8 ? encode_e4m3_map : encode_bf16_map;
   if ((rc = encode(&pf->tq, q, D, rows, kBlock)) != BSATTN_OK) return rc;
   if ((rc = encode(&pf->tk, k, D, kv_rows, kv_box)) != BSATTN_OK) return rc;
-  if ((rc = encode(&pf->tv, v, D, kv_rows, kv_box)) != BSATTN_OK) return rc;
+
+  // head_dim 64 multiplies P by V in fp16.  The kernel can convert each V
+  // tile in shared memory after its load, once per (query tile, key block)
+  // pair; when the key blocks are shared by several query tiles on average
+  // and V is not tiny, one conversion pass over V before the launch costs
+  // less (one read and one write of V).  Never allocated during stream
+  // capture; if the allocation fails the kernel converts V itself.
+  bool v_pre = false;
+  const size_t v16_bytes = (size_t)kv_rows * D * 2;
+  const long long kv_units = (long long)B * Hkv * plan->nb * plan->kdiv;  // key blocks of V
+  if (v16_ok && D == 64 && !in8 && kv_rows >= kV16MinRows &&
+      plan->nnz >= kV16MinReuse * kv_units) {
+    if (plan->dev.v16_bytes >= v16_bytes) {
+      v_pre = true;
+    } else {
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusActive;
+      void* buf = nullptr;
+      if (cudaStreamIsCapturing(stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
+          cudaMallocAsync(&buf, v16_bytes, stream) == cudaSuccess) {
+        if (plan->dev.v16) cudaFreeAsync(plan->dev.v16, stream);
+        plan->dev.v16 = buf;
+        plan->dev.v16_bytes = v16_bytes;
+        v_pre = true;
+      } else {
+        (void)cudaGetLastError();  // the kernel converts V itself
+      }
+    }
+  }
+  if ((rc = encode(&pf->tv, v_pre ? plan->dev.v16 : v, D, kv_rows, kv_box)) != BSATTN_OK)
+    return rc;
+  pf->v_src = v_pre ? v : nullptr;
+  pf->v16 = v_pre ? plan->dev.v16 : nullptr;
+  pf->v16_elems = v_pre ? kv_rows * D : 0;
 
   FwdParams& prm = pf->prm;
   prm = FwdParams{};
@@ -172,6 +206,7 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   prm.kv_group = H / Hkv;
   prm.kdiv = plan->kdiv;
   prm.v_scale = v_scale;
+  prm.v_pre = v_pre ? 1 : 0;
   pf->D = D;
   pf->in8 = in8;
   pf->out_f32 = (plan->flags & BSATTN_OUT_F32) != 0;
@@ -180,6 +215,11 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
 }
 
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream) {
+  if (pf.prm.v_pre) {
+    const cudaError_t e =
+        launch_v16_convert(pf.v_src, pf.v16, pf.v16_elems, pf.prm.status, pf.grid, stream);
+    if (e != cudaSuccess) return e;
+  }
   return launch_fwd(pf.D, pf.out_f32, pf.tq, pf.tk, pf.tv, pf.prm, pf.grid, stream, pf.in8);
 }
 
@@ -324,6 +364,13 @@ bsattn_status bsattn_plan_csc(bsattn_plan_t plan, const int32_t** d_col_ptr,
   return BSATTN_OK;
 }
 
+bsattn_status bsattn_plan_v16(bsattn_plan_t plan, const void** d_v16, size_t* bytes) {
+  if (!plan_ok(plan) || !d_v16 || !bytes) return BSATTN_ERR_INVALID_ARG;
+  *d_v16 = plan->dev.v16;
+  *bytes = plan->dev.v16_bytes;
+  return BSATTN_OK;
+}
+
 bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_order,
                                    int64_t* n_live, const int32_t** d_empty_tiles,
                                    int64_t* n_empty) {
@@ -340,7 +387,8 @@ bsattn_status bsattn_fwd(const void* q, const void* k, const void* v, bsattn_pla
                          void* out, float* lse, int B, int H, int S, int D, float scale,
                          void* stream) {
   PreparedFwd pf;
-  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, H);
+  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, H, false,
+                                       1.0f, true, static_cast<cudaStream_t>(stream));
   if (rc != BSATTN_OK) return rc;
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }
@@ -349,7 +397,8 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
                              void* out, float* lse, int B, int H, int Hkv, int S, int D,
                              float scale, void* stream) {
   PreparedFwd pf;
-  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, Hkv);
+  const bsattn_status rc = prepare_fwd(q, k, v, plan, out, lse, B, H, S, D, scale, &pf, Hkv, false,
+                                       1.0f, true, static_cast<cudaStream_t>(stream));
   if (rc != BSATTN_OK) return rc;
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }

@@ -675,8 +675,9 @@ __device__ void run_mma_pv(const FwdParams& p, Bars* bars, uint32_t tmem, uint32
         break;
       }
       const int st = vc % C::kVStages;
-      // V(vc) loaded (fp16 P V: and converted to fp16 by the epilogue warps)
-      if (!wait_warp(smem_u32(C::kF16PV ? &bars->v_conv[st] : &bars->v_full[st]),
+      // V(vc) loaded (fp16 P V: and converted to fp16 by the epilogue warps,
+      // unless V was converted before the launch)
+      if (!wait_warp(smem_u32((C::kF16PV && !p.v_pre) ? &bars->v_conv[st] : &bars->v_full[st]),
                      (uint32_t)(vc / C::kVStages) & 1u, abort_flag, p.status, lim)) {
         ok = false;
         break;
@@ -1428,10 +1429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     else if (warp == kWarpMmaPV)
       run_mma_pv<D, IN8>(p, bars, tmem, base, abort_flag);
     else if (warp >= kWarpEpi0) {
-      if constexpr (C::kF16PV)
-        run_epilogue_convert<D, OUT_F32, IN8>(p, bars, tmem, base, abort_flag);
-      else
+      if constexpr (C::kF16PV) {
+        if (!p.v_pre)  // V tiles arrive in bf16 or e4m3: these warps convert them
+          run_epilogue_convert<D, OUT_F32, IN8>(p, bars, tmem, base, abort_flag);
+        else
+          run_epilogue<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
+      } else {
         run_epilogue<D, OUT_F32, IN8>(p, bars, tmem, abort_flag);
+      }
     }
     else if (warp == kWarpSched)
       run_scheduler<D, IN8, KB64>(&tm_q, p, bars, base, abort_flag);
@@ -1493,7 +1498,42 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
   return cudaGetLastError();
 }
 
+// The fp16 copy of V that head_dim 64's P V product reads (FwdParams::v_pre):
+// 8 values per thread and step, 16-byte loads and stores, grid-stride.  bf16
+// converts to fp16 exactly for 2^-14 <= |v| <= 65504 (below, to fp16's
+// subnormals, off by < 2^-25); a larger or non-finite value becomes an fp16
+// infinity or NaN and raises kStatusRange, as the in-kernel conversion does.
+__global__ void __launch_bounds__(256) v16_convert_kernel(const uint4* __restrict__ v,
+                                                          uint4* __restrict__ v16, long long n16,
+                                                          int* status) {
+  uint32_t emax = 0;  // per 16-bit half, the largest fp16 exponent field written
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(v + i);
+    uint32_t o[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      o[j] = pack_f16x2(__uint_as_float(o[j] << 16), __uint_as_float(o[j] & 0xFFFF0000u));
+      emax = max_u16x2(emax, o[j] & 0x7C007C00u);
+    }
+    v16[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  const bool bad = (emax & 0xFFFFu) == 0x7C00u || (emax >> 16) == 0x7C00u;
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
+}
+
 }  // namespace
+
+cudaError_t launch_v16_convert(const void* v, void* v16, long long n, int* status, int grid,
+                               cudaStream_t stream) {
+  const long long n16 = n / 8;
+  if (n16 <= 0) return cudaSuccess;
+  const long long blocks = (n16 + 255) / 256;
+  const int g = (int)(blocks < 8LL * grid ? blocks : 8LL * grid);  // grid-stride beyond that
+  v16_convert_kernel<<<g, 256, 0, stream>>>(static_cast<const uint4*>(v), static_cast<uint4*>(v16),
+                                          n16, status);
+  return cudaGetLastError();
+}
 
 size_t fwd_smem_bytes(int D) {
   return D == 64 ? Cfg<64>::kSmem + 1024 : Cfg<128>::kSmem + 1024;

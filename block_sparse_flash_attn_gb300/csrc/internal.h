@@ -36,6 +36,10 @@ struct PlanDevice {
   // blocks longest first (within head chunks, as tile_order), then the empty ones
   int* kv_order = nullptr;     // [R]
   float* dl = nullptr;         // [B*H*S] backward scratch: dO_i . O_i
+  // head_dim-64 forward: an fp16 copy of V (allocated by the first forward
+  // call that uses it, stream-ordered; grows when a call needs more)
+  void* v16 = nullptr;
+  size_t v16_bytes = 0;
 };
 
 // Everything the forward kernel needs besides the three tensor maps.
@@ -68,6 +72,10 @@ struct FwdParams {
   // pairs (two consecutive entries of a tile's list fill one 128-key stage;
   // the K and V tensor maps then have 64-row boxes)
   int kdiv = 1;
+  // head_dim 64: V's tensor map reads an fp16 copy of V that v16_convert_kernel
+  // wrote before the launch (P V runs in fp16), so the epilogue warps do not
+  // convert each V tile in shared memory
+  int v_pre = 0;
 };
 
 
@@ -94,12 +102,26 @@ struct PreparedFwd {
   bool out_f32 = false;
   bool in8 = false;
   int grid = 0;
+  // prm.v_pre: convert v_src (bf16) into v16 (fp16, v16_elems values) first
+  const void* v_src = nullptr;
+  void* v16 = nullptr;
+  long long v16_elems = 0;
 };
+// The head_dim-64 V conversion pass runs when V has at least kV16MinRows rows
+// (2 MiB; below, its launch costs more than it saves) and the plan has at
+// least kV16MinReuse live blocks per key block of V on average (the kernel
+// would otherwise convert each V tile that many times).
+constexpr long long kV16MinRows = 16384;
+constexpr long long kV16MinReuse = 4;
 // Hkv: K/V heads (H % Hkv == 0; Hkv == H for plain multi-head attention).
 // in8: q, k, v are e4m3 (D = 128); v_scale multiplies O.
+// v16_ok: at head_dim 64 the call may give V an fp16 copy in the plan's
+// scratch (allocated on `stream` when missing, never during stream capture),
+// converted once per launch instead of once per query tile in the kernel.
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
-                          PreparedFwd* pf, int Hkv, bool in8 = false, float v_scale = 1.0f);
+                          PreparedFwd* pf, int Hkv, bool in8 = false, float v_scale = 1.0f,
+                          bool v16_ok = false, cudaStream_t stream = nullptr);
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream);
 
 // plan.cu
@@ -125,6 +147,10 @@ int schedule_chunk_heads(int nb);
 
 // fwd_sm103.cu
 // in8: Q, K, V are e4m3 (D = 128 only; the tensor maps are of uint8 elements)
+// bf16 -> fp16 copy of V (n values, a multiple of 8, both pointers 16-byte
+// aligned); a value fp16 cannot hold (|v| > 65504, inf, NaN) sets kStatusRange.
+cudaError_t launch_v16_convert(const void* v, void* v16, long long n, int* status, int grid,
+                               cudaStream_t stream);
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream,
                        bool in8 = false);

@@ -133,9 +133,14 @@ extern "C" bsattn_status bsattn_pipeline_create(const uint8_t* d_mask, int B, in
                      static_cast<const char*>(p->dk) + off * 2,
                      static_cast<const char*>(p->dv) + off * 2, pl,
                      static_cast<char*>(p->dout) + off * p->out_elem, p->dlse + (size_t)a * S, 1,
-                     h, S, D, 1.0f, &p->prep[c], h);
+                     h, S, D, 1.0f, &p->prep[c], h, false, 1.0f, true,
+                     static_cast<cudaStream_t>(stream));
     if (rc != BSATTN_OK) return fail(rc);
   }
+  // the parts' fp16 V copies (head_dim 64) are allocated on `stream`; the
+  // runs use them from the pipeline's own streams
+  if ((e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return fail(from_cuda(e));
   p->magic = kPipeMagic;
   *out = p;
   return BSATTN_OK;

@@ -124,6 +124,12 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
                                    int64_t* n_live, const int32_t** d_empty_tiles,
                                    int64_t* n_empty);
 
+/* Device pointer and size in bytes of the plan's fp16 copy of V (head_dim 64,
+   see bsattn_fwd), or NULL and 0 while no forward call has made one; valid
+   until the next forward call with the plan or bsattn_plan_free.  For
+   tests/tools. */
+bsattn_status bsattn_plan_v16(bsattn_plan_t plan, const void** d_v16, size_t* bytes);
+
 /*
  * bsattn_fwd -- O, LSE = block-sparse attention(Q, K, V; plan's mask).
  *
@@ -139,6 +145,16 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
  * with the same plan must not overlap on the GPU.  A kernel-side failure
  * (bounded wait ran out) is recorded in the plan and returned by
  * bsattn_plan_status.
+ * At D = 64 P V runs in fp16 (V converts exactly for 2^-14 <= |v| <= 65504; a
+ * V entry beyond 65504, or not finite, is reported as BSATTN_ERR_RANGE by
+ * bsattn_plan_status).  When V has at least 16384 rows (B*Hkv*S) and the plan
+ * has at least 4 live blocks per key block of V on average, the call first
+ * converts V into an fp16 copy held by the plan (one extra kernel launch;
+ * B*Hkv*S*64*2 bytes, allocated with cudaMallocAsync on `stream` by the first
+ * call that needs it, or a larger one, and freed by bsattn_plan_free); it
+ * allocates nothing while `stream` is being captured, and if the allocation
+ * fails the forward kernel converts each V tile itself, as it does below
+ * those sizes.
  * Errors: INVALID_ARG (null/misaligned, sizes differ from the plan, non-finite
  * scale), UNSUPPORTED (D), CUDA (launch failure).
  */

@@ -378,22 +378,25 @@ def test_scores_jump_in_a_later_block(bs, D):
 # D = 64 multiplies P by V in fp16: a V entry beyond fp16's range is reported
 # ----------------------------------------------------------------------------
 
-@pytest.mark.parametrize("D", [64, 128])
-def test_v_beyond_fp16_range(bs, D):
+# (D, B, H, S): at D = 64 the small size converts V in the kernel, the large
+# one through the plan's fp16 copy of V (16 heads x 2048 rows, ~5 live blocks
+# per key block)
+@pytest.mark.parametrize("D,B,H,S", [(64, 1, 2, 512), (64, 1, 16, 2048), (128, 1, 2, 512)])
+def test_v_beyond_fp16_range(bs, D, B, H, S):
     import torch
-    B, H, S = 1, 2, 512
     qb, kb, vb = workloads.custom(417 + D, B, H, S, D)
     mask = _mask_iid(12, B, H, S // 128, 0.6, diag=True)
     v = _bf16_float(vb)
     v_big = v.copy()
-    v_big[0, 1, 300, 7] = 70000.0     # rounds to a bf16 above 65504
+    v_big[0, 1, S - 212, 7] = 70000.0     # rounds to a bf16 above 65504
     v_edge = v.copy()
-    v_edge[0, 1, 300, 7] = 65280.0    # the largest bf16 below 65504: exact in fp16
+    v_edge[0, 1, S - 212, 7] = 65280.0    # the largest bf16 below 65504: exact in fp16
     p = bs.plan(torch.from_numpy(mask).cuda(), out_f32=True)
     q, k = to_dev(qb), to_dev(kb)
     o, _ = bs.fwd(q, k, to_dev(_bf16_bits(v_edge)), p, D ** -0.5)
     bs.plan_status(p)
     assert bool(torch.isfinite(o).all())
+    assert (bs.plan_v16_bytes(p) > 0) == (D == 64 and H * S >= 16384)
     o, _ = bs.fwd(q, k, to_dev(_bf16_bits(v_big)), p, D ** -0.5)
     if D == 64:
         with pytest.raises(bs.BsattnError) as e:
@@ -408,4 +411,34 @@ def test_v_beyond_fp16_range(bs, D):
     p.close()
     O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(D ** -0.5), False)
     ok, rep = compare(o.cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref)
+    assert ok, rep
+
+
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_v16_copy_matches_in_kernel_conversion(bs, causal):
+    """At head_dim 64 a plan whose key blocks serve several query tiles gets an
+    fp16 copy of V before the launch, and the kernel reads it instead of
+    converting each V tile in shared memory.  Both give the same fp16 values,
+    so O and LSE must agree bit for bit with the in-kernel conversion (which
+    bsattn_fwd_noalloc always uses), and every row with the oracle."""
+    import torch
+    B, H, S, D = 1, 16, 2048, 64
+    qb, kb, vb = workloads.custom(611 + causal, B, H, S, D)
+    mask = _mask_iid(13, B, H, S // 128, 0.6, diag=True)
+    mask_d = torch.from_numpy(mask).cuda()
+    q, k, v = to_dev(qb), to_dev(kb), to_dev(vb)
+    p = bs.plan(mask_d, causal=causal)
+    assert bs.plan_v16_bytes(p) == 0
+    o, lse = bs.fwd(q, k, v, p, 0.125)
+    bs.plan_status(p)
+    assert bs.plan_v16_bytes(p) == B * H * S * D * 2
+    o2, lse2 = bs.fwd(q, k, v, p, 0.125)  # the copy is reused
+    bs.plan_status(p)
+    p.close()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    o3, lse3 = bs.fwd_noalloc(q, k, v, mask_d, causal=causal, scale=0.125)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o3) and torch.equal(lse, lse3)
+    O_ref, L_ref = oracle.attention(qb, kb, vb, mask, np.float32(0.125), causal)
+    ok, rep = compare(o.float().cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref, out_bf16=True)
     assert ok, rep
