@@ -421,9 +421,10 @@ def run_ours(args):
         return f"{wid}" + ("-kb64" if args.key_block == 64 else "") + ("-e4m3" if fp8 else "")
 
     def launches_per_call(plan, D):
-        """Kernel launches of one forward call: at head_dim 64 the library may
-        first convert V to fp16 (its plan then holds the copy)."""
-        return 2 if (not fp8 and D == 64 and bsattn.plan_v16_bytes(plan) > 0) else 1
+        """Kernel launches of one forward call: where P V runs in fp16 (head_dim
+        64, e4m3 inputs) the library may first convert V to fp16 (its plan
+        then holds the copy)."""
+        return 2 if ((fp8 or D == 64) and bsattn.plan_v16_bytes(plan) > 0) else 1
 
     def timed(q, k, v, plan, scale, o, lse, steps):
         """steps forward calls, each timed by CUDA events on the launching

@@ -151,16 +151,17 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
   if ((rc = encode(&pf->tq, q, D, rows, kBlock)) != BSATTN_OK) return rc;
   if ((rc = encode(&pf->tk, k, D, kv_rows, kv_box)) != BSATTN_OK) return rc;
 
-  // head_dim 64 multiplies P by V in fp16.  The kernel can convert each V
-  // tile in shared memory after its load, once per (query tile, key block)
-  // pair; when the key blocks are shared by several query tiles on average
-  // and V is not tiny, one conversion pass over V before the launch costs
-  // less (one read and one write of V).  Never allocated during stream
-  // capture; if the allocation fails the kernel converts V itself.
+  // head_dim 64 and e4m3 inputs multiply P by V in fp16.  The kernel can
+  // convert each V tile in shared memory after its load, once per (query
+  // tile, key block) pair; when the key blocks are shared by several query
+  // tiles on average and V is not tiny, one conversion pass over V before
+  // the launch costs less (one read of V, one write of its fp16 copy).
+  // Never allocated during stream capture; if the allocation fails the
+  // kernel converts V itself.
   bool v_pre = false;
   const size_t v16_bytes = (size_t)kv_rows * D * 2;
   const long long kv_units = (long long)B * Hkv * plan->nb * plan->kdiv;  // key blocks of V
-  if (v16_ok && D == 64 && !in8 && kv_rows >= kV16MinRows &&
+  if (v16_ok && (D == 64 || in8) && kv_rows >= kV16MinRows &&
       plan->nnz >= kV16MinReuse * kv_units) {
     if (plan->dev.v16_bytes >= v16_bytes) {
       v_pre = true;
@@ -178,7 +179,9 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
       }
     }
   }
-  if ((rc = encode(&pf->tv, v_pre ? plan->dev.v16 : v, D, kv_rows, kv_box)) != BSATTN_OK)
+  // the fp16 copy is read like bf16 V (16-bit elements, 64-column boxes)
+  if ((rc = v_pre ? encode_bf16_map(&pf->tv, plan->dev.v16, D, kv_rows, kv_box)
+                  : encode(&pf->tv, v, D, kv_rows, kv_box)) != BSATTN_OK)
     return rc;
   pf->v_src = v_pre ? v : nullptr;
   pf->v16 = v_pre ? plan->dev.v16 : nullptr;
@@ -217,7 +220,10 @@ bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_pl
 cudaError_t launch_prepared(const PreparedFwd& pf, cudaStream_t stream) {
   if (pf.prm.v_pre) {
     const cudaError_t e =
-        launch_v16_convert(pf.v_src, pf.v16, pf.v16_elems, pf.prm.status, pf.grid, stream);
+        pf.in8 ? launch_v16_convert_e4m3(pf.v_src, pf.v16, pf.v16_elems, pf.prm.status, pf.grid,
+                                         stream)
+               : launch_v16_convert(pf.v_src, pf.v16, pf.v16_elems, pf.prm.status, pf.grid,
+                                    stream);
     if (e != cudaSuccess) return e;
   }
   return launch_fwd(pf.D, pf.out_f32, pf.tq, pf.tk, pf.tv, pf.prm, pf.grid, stream, pf.in8);
@@ -408,7 +414,8 @@ bsattn_status bsattn_fwd_fp8(const void* q8, const void* k8, const void* v8, bsa
                              float v_scale, void* stream) {
   PreparedFwd pf;
   const bsattn_status rc =
-      prepare_fwd(q8, k8, v8, plan, out, lse, B, H, S, D, scale, &pf, H, true, v_scale);
+      prepare_fwd(q8, k8, v8, plan, out, lse, B, H, S, D, scale, &pf, H, true, v_scale, true,
+                  static_cast<cudaStream_t>(stream));
   if (rc != BSATTN_OK) return rc;
   return from_cuda(launch_prepared(pf, static_cast<cudaStream_t>(stream)));
 }

@@ -521,20 +521,25 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     return true;
   };
   auto load_v = [&](int row, int row2) -> bool {
-    if constexpr (C::kIn8) {  // into the e4m3 staging ring, free once converted
-      const int st = vc % C::kV8Stages;
-      if (!load_tile(tm_v, smem_base + C::kV8Off + st * C::kBoxBytes, C::kBoxBytes,
-                     smem_u32(&bars->v8_full[st]), smem_u32(&bars->v8_empty[st]),
-                     ((uint32_t)(vc / C::kV8Stages) & 1u) ^ 1u, row, row2, 1, C::kBoxBytes))
-        return false;
-    } else {
-      const int st = vc % C::kVStages;
-      if (!load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
-                     smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]),
-                     ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u, row, row2, C::kBoxes,
-                     C::kTileBytes))
-        return false;
+    if constexpr (C::kIn8) {
+      if (!p.v_pre) {  // into the e4m3 staging ring, free once converted
+        const int st = vc % C::kV8Stages;
+        if (!load_tile(tm_v, smem_base + C::kV8Off + st * C::kBoxBytes, C::kBoxBytes,
+                       smem_u32(&bars->v8_full[st]), smem_u32(&bars->v8_empty[st]),
+                       ((uint32_t)(vc / C::kV8Stages) & 1u) ^ 1u, row, row2, 1, C::kBoxBytes))
+          return false;
+        ++vc;
+        return true;
+      }
     }
+    // bf16 V, or V converted to fp16 before the launch: straight into the ring
+    // the P V product reads
+    const int st = vc % C::kVStages;
+    if (!load_tile(tm_v, smem_base + C::kVOff + st * C::kBoxBytes, C::kVGroup,
+                   smem_u32(&bars->v_full[st]), smem_u32(&bars->v_empty[st]),
+                   ((uint32_t)(vc / C::kVStages) & 1u) ^ 1u, row, row2, C::kBoxes,
+                   C::kTileBytes))
+      return false;
     ++vc;
     return true;
   };
@@ -553,13 +558,17 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     // Let every TMA load this warp issued land before the CTA exits.
     for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
       wait_drain(smem_u32(&bars->k_full[i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
+    bool staged = false;  // e4m3 V went to the staging ring
+    if constexpr (C::kIn8) staged = !p.v_pre;
     if constexpr (C::kIn8) {
-      for (int i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
-        wait_drain(smem_u32(&bars->v8_full[i % C::kV8Stages]), (uint32_t)(i / C::kV8Stages) & 1u);
-    } else {
+      if (staged)
+        for (int i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
+          wait_drain(smem_u32(&bars->v8_full[i % C::kV8Stages]),
+                     (uint32_t)(i / C::kV8Stages) & 1u);
+    }
+    if (!staged)
       for (int i = (vc > C::kVStages ? vc - C::kVStages : 0); i < vc; ++i)
         wait_drain(smem_u32(&bars->v_full[i % C::kVStages]), (uint32_t)(i / C::kVStages) & 1u);
-    }
   }
 }
 
@@ -1522,7 +1531,43 @@ __global__ void __launch_bounds__(256) v16_convert_kernel(const uint4* __restric
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
 }
 
+// The same for e4m3 V (the FP8 forward): 16 values per thread and step, each
+// converted exactly; an e4m3 NaN (0x7F / 0xFF) becomes an fp16 NaN and raises
+// kStatusRange, as the in-kernel conversion does.
+__global__ void __launch_bounds__(256) v16_convert_e4m3_kernel(const uint4* __restrict__ v8,
+                                                               uint4* __restrict__ v16,
+                                                               long long n16, int* status) {
+  uint32_t emax = 0;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (long long)gridDim.x * blockDim.x) {
+    const uint4 w = __ldg(v8 + i);
+    const uint32_t in[4] = {w.x, w.y, w.z, w.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      e4m3x4_to_f16x4(in[j], o[2 * j], o[2 * j + 1]);
+      emax = max_u16x2(emax, o[2 * j] & 0x7C007C00u);
+      emax = max_u16x2(emax, o[2 * j + 1] & 0x7C007C00u);
+    }
+    v16[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    v16[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  const bool bad = (emax & 0xFFFFu) == 0x7C00u || (emax >> 16) == 0x7C00u;
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, kStatusRange);
+}
+
 }  // namespace
+
+cudaError_t launch_v16_convert_e4m3(const void* v8, void* v16, long long n, int* status,
+                                    int grid, cudaStream_t stream) {
+  const long long n16 = n / 16;
+  if (n16 <= 0) return cudaSuccess;
+  const long long blocks = (n16 + 255) / 256;
+  const int g = (int)(blocks < 8LL * grid ? blocks : 8LL * grid);  // grid-stride beyond that
+  v16_convert_e4m3_kernel<<<g, 256, 0, stream>>>(static_cast<const uint4*>(v8),
+                                                 static_cast<uint4*>(v16), n16, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_v16_convert(const void* v, void* v16, long long n, int* status, int grid,
                                cudaStream_t stream) {

@@ -72,9 +72,9 @@ struct FwdParams {
   // pairs (two consecutive entries of a tile's list fill one 128-key stage;
   // the K and V tensor maps then have 64-row boxes)
   int kdiv = 1;
-  // head_dim 64: V's tensor map reads an fp16 copy of V that v16_convert_kernel
-  // wrote before the launch (P V runs in fp16), so the epilogue warps do not
-  // convert each V tile in shared memory
+  // P V in fp16 (head_dim 64, or e4m3 inputs): V's tensor map reads an fp16
+  // copy of V written before the launch (v16_convert_kernel, or the e4m3
+  // one), so the epilogue warps do not convert each V tile in shared memory
   int v_pre = 0;
 };
 
@@ -107,7 +107,7 @@ struct PreparedFwd {
   void* v16 = nullptr;
   long long v16_elems = 0;
 };
-// The head_dim-64 V conversion pass runs when V has at least kV16MinRows rows
+// The V conversion pass (fp16 P V) runs when V has at least kV16MinRows rows
 // (2 MiB; below, its launch costs more than it saves) and the plan has at
 // least kV16MinReuse live blocks per key block of V on average (the kernel
 // would otherwise convert each V tile that many times).
@@ -115,9 +115,10 @@ constexpr long long kV16MinRows = 16384;
 constexpr long long kV16MinReuse = 4;
 // Hkv: K/V heads (H % Hkv == 0; Hkv == H for plain multi-head attention).
 // in8: q, k, v are e4m3 (D = 128); v_scale multiplies O.
-// v16_ok: at head_dim 64 the call may give V an fp16 copy in the plan's
-// scratch (allocated on `stream` when missing, never during stream capture),
-// converted once per launch instead of once per query tile in the kernel.
+// v16_ok: where P V runs in fp16 (head_dim 64, or e4m3 inputs) the call may
+// give V an fp16 copy in the plan's scratch (allocated on `stream` when
+// missing, never during stream capture), converted once per launch instead
+// of once per query tile in the kernel.
 bsattn_status prepare_fwd(const void* q, const void* k, const void* v, bsattn_plan_t plan,
                           void* out, float* lse, int B, int H, int S, int D, float scale,
                           PreparedFwd* pf, int Hkv, bool in8 = false, float v_scale = 1.0f,
@@ -151,6 +152,9 @@ int schedule_chunk_heads(int nb);
 // aligned); a value fp16 cannot hold (|v| > 65504, inf, NaN) sets kStatusRange.
 cudaError_t launch_v16_convert(const void* v, void* v16, long long n, int* status, int grid,
                                cudaStream_t stream);
+// The same from e4m3 V (n a multiple of 16); an e4m3 NaN sets kStatusRange.
+cudaError_t launch_v16_convert_e4m3(const void* v8, void* v16, long long n, int* status,
+                                    int grid, cudaStream_t stream);
 cudaError_t launch_fwd(int D, bool out_f32, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const FwdParams& p, int grid, cudaStream_t stream,
                        bool in8 = false);

@@ -124,8 +124,9 @@ bsattn_status bsattn_plan_schedule(bsattn_plan_t plan, const int32_t** d_tile_or
                                    int64_t* n_live, const int32_t** d_empty_tiles,
                                    int64_t* n_empty);
 
-/* Device pointer and size in bytes of the plan's fp16 copy of V (head_dim 64,
-   see bsattn_fwd), or NULL and 0 while no forward call has made one; valid
+/* Device pointer and size in bytes of the plan's fp16 copy of V (head_dim 64
+   and e4m3 inputs, see bsattn_fwd and bsattn_fwd_fp8), or NULL and 0 while
+   no forward call has made one; valid
    until the next forward call with the plan or bsattn_plan_free.  For
    tests/tools. */
 bsattn_status bsattn_plan_v16(bsattn_plan_t plan, const void** d_v16, size_t* bytes);
@@ -226,8 +227,9 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
  * "JAX Pallas and Blackwell", section "What the Tutorial Covers": Blackwell's
  * tensor cores take FP8 operands with fp32 accumulation.  Here S = Q K^T runs
  * on e4m3 operands (the OCP 8-bit format: sign, 4 exponent bits with bias 7,
- * 3 mantissa bits) with fp32 accumulation; each e4m3 V tile is converted to
- * fp16 in shared memory (exactly) and P V runs in fp16, fp32 accumulation.
+ * 3 mantissa bits) with fp32 accumulation; V is converted to fp16 (exactly:
+ * once per call into a copy, or tile by tile in shared memory, see below) and
+ * P V runs in fp16, fp32 accumulation.
  * The result is the attention of bsattn_fwd on the decoded values:
  *
  *   O = v_scale * softmax(scale * Q K^T + mask) V,  LSE as bsattn_fwd.
@@ -242,6 +244,10 @@ bsattn_status bsattn_fwd_gqa(const void* q, const void* k, const void* v, bsattn
  *   scale, v_scale  finite.
  * Errors: as bsattn_fwd; a NaN entry of V (e4m3 0x7F / 0xFF) is reported as
  * BSATTN_ERR_RANGE by the status calls.
+ * V's fp16 conversion: as at D = 64 in bsattn_fwd (an fp16 copy of V held
+ * by the plan, B*H*S*128*2 bytes, converted before the kernel when V has at
+ * least 16384 rows and the plan at least 4 live blocks per key block of V;
+ * otherwise the kernel converts each V tile after its load).
  */
 bsattn_status bsattn_fwd_fp8(const void* q8, const void* k8, const void* v8, bsattn_plan_t plan,
                              void* out, float* lse, int B, int H, int S, int D, float scale,

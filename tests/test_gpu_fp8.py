@@ -103,17 +103,22 @@ def test_full_size_every_row(bs, wid):
         assert ok, (h0, rep)
 
 
-def test_nan_in_v_is_reported_and_d64_unsupported(bs):
+# (B, H, S): V converted tile by tile in the kernel, and through the plan's
+# fp16 copy of V (16 heads x 2048 rows, 16 live blocks per key block)
+@pytest.mark.parametrize("B,H,S", [(1, 1, 256), (1, 16, 2048)])
+def test_nan_in_v_is_reported_and_d64_unsupported(bs, B, H, S):
     import torch
-    B, H, S, D = 1, 1, 256, 128
+    D = 128
     q8, k8, v8 = _inputs(9, B, H, S, D)
     v8 = v8.copy()
     v8[0, 0, 200, 3] = 0x7F  # e4m3 NaN
-    p = bs.plan(torch.ones((B, H, 2, 2), dtype=torch.uint8, device="cuda"))
+    nb = S // 128
+    p = bs.plan(torch.ones((B, H, nb, nb), dtype=torch.uint8, device="cuda"))
     bs.fwd_fp8(_dev8(q8), _dev8(k8), _dev8(v8), p, 0.1)
     with pytest.raises(bs.BsattnError) as e:
         bs.plan_status(p)
     assert e.value.status == bs.ERR_RANGE
+    assert (bs.plan_v16_bytes(p) > 0) == (B * H * S >= 16384)
     x = torch.zeros((B, H, S, 64), dtype=torch.uint8, device="cuda")
     with pytest.raises(bs.BsattnError) as e:
         bs.fwd_fp8(x, x, x, p, 0.1)
