@@ -73,6 +73,9 @@ def test_fwd_and_status_reject_missing_plan(lib):
     rp, ci, n = vp(), vp(), ctypes.c_int64()
     assert lib.bsattn_plan_csr(vp(0), ctypes.byref(rp), ctypes.byref(ci), ctypes.byref(n)) == \
         bs.ERR_INVALID_ARG
+    v16, nbytes = vp(), ctypes.c_size_t()
+    assert lib.bsattn_plan_v16(vp(0), ctypes.byref(v16), ctypes.byref(nbytes)) == \
+        bs.ERR_INVALID_ARG
     lib.bsattn_plan_free(vp(0))  # ignored
     assert lib.bsattn_selftest_wait_timeout(10, vp(0)) == bs.ERR_INVALID_ARG
     assert lib.bsattn_selftest_wait_timeout(10 ** 10, vp(0)) == bs.ERR_INVALID_ARG
