@@ -32,17 +32,21 @@ def _mask_iid(seed, B, H, nb, p, diag=False):
     return m
 
 
-@pytest.mark.parametrize("Hkv,D,causal", [(1, 128, True), (2, 64, False), (4, 128, False),
-                                          (8, 64, True)])
-def test_gqa_every_row(bs, Hkv, D, causal):
+# the last case is large enough for the fp16 copy of V (B * Hkv * S = 16384
+# rows, ~14 live blocks per key block of V): the copy has Hkv heads
+@pytest.mark.parametrize("Hkv,D,causal,S", [(1, 128, True, 1024), (2, 64, False, 1024),
+                                            (4, 128, False, 1024), (8, 64, True, 1024),
+                                            (4, 64, False, 2048)])
+def test_gqa_every_row(bs, Hkv, D, causal, S):
     import torch
-    B, H, S = 2, 8, 1024
+    B, H = 2, 8
     qb = workloads.custom(500 + Hkv, B, H, S, D)[0]
     _, kb, vb = workloads.custom(600 + Hkv, B, Hkv, S, D)
     mask = _mask_iid(12 + Hkv, B, H, S // 128, 0.4, diag=True)
     p = bs.plan(torch.from_numpy(mask).cuda(), causal=causal, out_f32=True)
     o, lse = bs.fwd(to_dev(qb), to_dev(kb), to_dev(vb), p, D ** -0.5)
     bs.plan_status(p)
+    assert bs.plan_v16_bytes(p) == (B * Hkv * S * D * 2 if S == 2048 else 0)
     p.close()
     O_ref, L_ref = oracle.attention_gqa(qb, kb, vb, mask, np.float32(D ** -0.5), causal)
     ok, rep = compare(o.cpu().numpy(), lse.cpu().numpy(), O_ref, L_ref)
