@@ -42,10 +42,12 @@
 // descriptors); see Cfg for the depths of each configuration.
 //
 // Precision: S = Q K^T in bf16 (e4m3 with FP8 inputs) with fp32 accumulation;
-// P V in bf16 at D = 128, in fp16 at D = 64 and with FP8 inputs (the four
-// epilogue warps convert each V tile to fp16 in shared memory: bf16 -> fp16
-// in place, e4m3 -> fp16 from a staging ring), so that the rounding of P, the
-// largest error term, is 2^-11 instead of 2^-8 where the logits are wide.
+// P V in bf16 at D = 128, in fp16 at D = 64 and with FP8 inputs, so that the
+// rounding of P, the largest error term, is 2^-11 instead of 2^-8 where the
+// logits are wide.  V reaches fp16 in one of two ways: converted once per
+// call into an fp16 copy that the kernel loads (v16_convert_kernel and its
+// e4m3 twin, FwdParams::v_pre), or tile by tile in shared memory by the four
+// epilogue warps (bf16 -> fp16 in place, e4m3 -> fp16 from a staging ring).
 //
 // The producer sees the CTA's tiles as one stream of key blocks and loads K
 // two blocks ahead of V along it; the scheduler warp loads each tile's Q as
@@ -132,9 +134,10 @@ constexpr int kMaxDevices = 64;
 
 // IN8: Q, K, V are e4m3 (FP8), at D = 128 only.  Q and K tiles are then 16 KB
 // (one 128-byte row per key or query), S = Q K^T runs as kind::f8f6f4 MMAs
-// (K = 32 per instruction), and each e4m3 V tile lands in its own staging
-// ring, from which the epilogue warps convert it to the fp16 V tile that the
-// P V product reads (P in fp16 as well).
+// (K = 32 per instruction), and P V runs in fp16 (P as well): each e4m3 V tile
+// lands in its own staging ring, from which the epilogue warps convert it to
+// the fp16 V tile that the P V product reads, unless V was converted to fp16
+// before the launch (then the fp16 tiles are loaded directly).
 template <int D, bool IN8 = false>
 struct Cfg {
   static_assert(!IN8 || D == 128, "e4m3 inputs at head_dim 128 only");
@@ -168,10 +171,10 @@ struct Cfg {
   // memory columns are not free, and the softmax threads add it up.
   static constexpr bool kOnes = D == 64;
   static constexpr int kPvN = kOnes ? D + 16 : D;
-  // P V in fp16 (P and V rounded to 11 significant bits instead of bf16's 8):
-  // at D = 64 the epilogue warps convert each V tile in shared memory after
-  // its load; with e4m3 inputs they convert it into the fp16 ring; at
-  // D = 128 with bf16 inputs P V stays in bf16.
+  // P V in fp16 (P and V rounded to 11 significant bits instead of bf16's 8)
+  // at D = 64 and with e4m3 inputs (V converted before the launch, or by the
+  // epilogue warps in shared memory); at D = 128 with bf16 inputs P V stays
+  // in bf16.
   static constexpr bool kF16PV = D == 64 || IN8;
   // A half row's block sum above this (formed against a stale reference)
   // makes the softmax redo the block with its max; in fp16 it also keeps every
@@ -559,8 +562,8 @@ __device__ void run_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
     for (int i = (kc > C::kKStages ? kc - C::kKStages : 0); i < kc; ++i)
       wait_drain(smem_u32(&bars->k_full[i % C::kKStages]), (uint32_t)(i / C::kKStages) & 1u);
     bool staged = false;  // e4m3 V went to the staging ring
-    if constexpr (C::kIn8) staged = !p.v_pre;
     if constexpr (C::kIn8) {
+      staged = !p.v_pre;
       if (staged)
         for (int i = (vc > C::kV8Stages ? vc - C::kV8Stages : 0); i < vc; ++i)
           wait_drain(smem_u32(&bars->v8_full[i % C::kV8Stages]),
@@ -1209,7 +1212,8 @@ __device__ __forceinline__ void convert_v8_quarter(uint32_t src, uint32_t dst, u
   }
 }
 
-// The epilogue warps when P V runs in fp16 (D = 64, or e4m3 inputs): besides
+// The epilogue warps when P V runs in fp16 (D = 64, or e4m3 inputs) and V was
+// not converted before the launch: besides
 // writing each tile's O (as run_epilogue does), they convert every V tile of
 // the CTA's block stream to fp16 after its load, each warp a quarter, and
 // announce it on v_conv (four arrivals): in place at D = 64; with e4m3 inputs
