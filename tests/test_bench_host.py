@@ -1,5 +1,6 @@
 """Host-side accounting of bench.py (no GPU): the exact count of (query, key)
-pairs that the metric's whole-block count stands beside."""
+pairs that the metric's whole-block count stands beside, and the lookup of
+measured DRAM traffic by kernel source hash."""
 import numpy as np
 import pytest
 
@@ -35,3 +36,19 @@ def test_allowed_pairs_causal_workload():
     mask = np.tril(np.ones((1, 1, 32, 32), dtype=np.uint8))
     assert bench.allowed_pairs(mask, True) == 496 * 128 * 128 + 32 * (128 * 129 // 2)
     assert bench.live_blocks(mask, True) == 528
+
+
+def test_traffic_table_applies_only_to_its_kernel_source(monkeypatch):
+    """A line of the committed DRAM-traffic table gives read + write bytes
+    while the kernel source hash equals the line's, and nothing (null in the
+    bench line) under any other hash."""
+    lines = [l.split() for l in open(bench.TRAFFIC_TABLE)
+             if l.strip() and not l.startswith("#")]
+    assert lines
+    for key, out, sha, rd, wr in (l[:5] for l in lines):
+        monkeypatch.setattr(bench, "kernel_source_sha16", lambda s=sha: s)
+        assert bench.measured_traffic(key, out == "f32") == int(rd) + int(wr)
+        monkeypatch.setattr(bench, "kernel_source_sha16", lambda: "0" * 16)
+        assert bench.measured_traffic(key, out == "f32") is None
+    # one capture: every line carries the same source hash
+    assert len({l[2] for l in lines}) == 1
