@@ -152,3 +152,15 @@ def test_noalloc_wrapper_rejects_bad_tensors_before_any_call(monkeypatch):
     # right shapes and dtypes, but host tensors (a host mask among them)
     with pytest.raises(TypeError, match="CUDA device"):
         bs.fwd_noalloc(q, q, q, mask)
+
+
+def test_header_states_the_v_copy_thresholds():
+    """bsattn_fwd's documentation gives the sizes at which the call converts V
+    to an fp16 copy before the launch; they are the library's constants."""
+    internal = open(os.path.join(ROOT, "block_sparse_flash_attn_gb300", "csrc",
+                                 "internal.h")).read()
+    rows = int(re.search(r"kV16MinRows = (\d+);", internal).group(1))
+    reuse = int(re.search(r"kV16MinReuse = (\d+);", internal).group(1))
+    header = " ".join(open(HEADER).read().split())
+    assert f"at least {rows} rows" in header
+    assert f"at least {reuse} live blocks per key block of V" in header
